@@ -1,0 +1,331 @@
+/*
+ * oes.h -- offloaded expert slots: the C ABI of the offloaded-MoE layer
+ * forward over a GPU slot cache, for one NVIDIA GB300 (sm_103a).
+ *
+ * The path (FreeToken PR #676 "--moe-prefill-demand-tokens", Solution):
+ * a chunk is routed top-k; its distinct experts, a sorted list of fixed
+ * length, are admitted into an LRU slot cache in queries of at most 128 ids,
+ * each query's misses copied from a pinned-host expert source before the
+ * next query evicts; routes are sorted into per-expert blocks
+ * (moe_align_block_size); the grouped SwiGLU expert GEMM runs over the slot
+ * pool through an expert->slot remap with its tiles sized by the layer's
+ * expert count, so its output is bit-identical to the same GEMM over the
+ * whole streamed layer.
+ *
+ * Conventions for every call:
+ *   - Pointers are raw addresses.  "device" = GPU global memory; "host" =
+ *     ordinary host memory; "mapped" = pinned host memory the GPU can read
+ *     (cudaHostAlloc / cudaHostRegister; on GB300 any pinned allocation).
+ *   - The caller allocates and owns every buffer.  The library owns only the
+ *     small device tables behind the two opaque handles (oes_slot_cache,
+ *     oes_expert_source), created and destroyed explicitly.
+ *   - Calls are asynchronous on the given stream and never synchronise the
+ *     host, except the *_load_state / *_read_state / *_create / *_destroy
+ *     calls, which say so.
+ *   - The return value reports what the host can check before launching:
+ *     OES_OK, OES_ERR_INVALID_ARG (null pointer, size out of range, buffer
+ *     too small), OES_ERR_UNSUPPORTED (a size this build does not handle),
+ *     OES_ERR_CAPACITY (a chunk the pool cannot hold), OES_ERR_CUDA (a CUDA
+ *     call or launch failed; oes_last_error() has the message).  On any
+ *     error nothing more is launched.
+ *   - What only the GPU can see is OR-ed into a caller-provided device word
+ *     `status` (OES_DEV_*), read by the caller at its own synchronisation.
+ *     A kernel that finds a bad condition records it and skips the work
+ *     that depends on it; it never traps.
+ *   - Layouts are row-major and contiguous; all byte offsets are 64-bit.
+ *   - bf16 / f16 values travel as uint16_t bit patterns.
+ */
+#ifndef OES_H
+#define OES_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *oes_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+enum {
+  OES_OK = 0,
+  OES_ERR_INVALID_ARG = 1,
+  OES_ERR_UNSUPPORTED = 2,
+  OES_ERR_CUDA = 3,
+  OES_ERR_CAPACITY = 4
+};
+
+enum {
+  OES_DEV_CAPACITY = 1, /* an ensure query had more misses than evictable slots */
+  OES_DEV_BAD_ID = 2,   /* an id out of range, or a query not strictly ascending */
+  OES_DEV_TIMEOUT = 4   /* a bounded wait gave up */
+};
+
+enum { OES_WFMT_BF16 = 0, OES_WFMT_NVFP4 = 1 };
+
+#define OES_QUERY_MAX 128   /* ids per ensure query (FreeToken PR #676, Solution) */
+#define OES_MAX_TOPK 32
+#define OES_MAX_EXPERTS 4096
+#define OES_MAX_SLOTS 8192
+
+/* Capacity of moe_align_block_size's sorted_ids for R routes, E experts and
+ * block size B: R + min(E, R) * (B - 1), rounded up to a multiple of B.  No
+ * routing needs more.  block_expert holds OES_ALIGN_CAPACITY / B entries. */
+#define OES_ALIGN_CAPACITY(R, E, B) \
+  ((((int64_t)(R) + (int64_t)((E) < (R) ? (E) : (R)) * ((B) - 1)) + (B) - 1) / (B) * (B))
+
+/* Message of the last error on this thread (static storage). */
+const char *oes_last_error(void);
+
+/* ------------------------------------------------------------------ route */
+
+/* Router logits of the tiny workload: logits[t, e] = sum_h x[t, h] * gate[h, e]
+ * with bf16 inputs and fp32 sums (the workload's "router logits from a bf16
+ * gate").  x: device [T, H] bf16; gate: device [H, E] bf16; logits: device
+ * [T, E] fp32.  1 <= T, 1 <= H, 1 <= E <= OES_MAX_EXPERTS. */
+int moe_gate_logits(const uint16_t *x, const uint16_t *gate, int T, int H, int E, float *logits,
+                    oes_stream_t stream);
+
+/* Top-k routing (FreeToken PR #676, Problem and Solution: each token routes
+ * to k experts; the workloads fix softmax-renormalised top-k).  For each
+ * token t: ids[t, 0..k-1] = the k largest logits[t, :] in descending order,
+ * ties to the lower expert id; weights[t, j] = softmax over the k selected
+ * logits (equal to the full softmax renormalised over the top k).
+ * logits: device [T, E] fp32, finite; ids: device [T, k] int32; weights:
+ * device [T, k] fp32.  1 <= k <= min(E, OES_MAX_TOPK), E <= OES_MAX_EXPERTS. */
+int moe_route_topk(const float *logits, int T, int E, int k, int32_t *ids, float *weights,
+                   oes_stream_t stream);
+
+/* The chunk's distinct experts as a sorted list of fixed length (FreeToken
+ * PR #676, Solution: "a sorted list of fixed length, so there is no host
+ * sync").  distinct: device [min(R, E)] int32, ascending, padded at the tail
+ * with -1; d_count: device [1] int32 = number of distinct experts.  ids out
+ * of [0, E) are ignored.  ids: device [R] int32, R >= 0. */
+int moe_distinct_experts(const int32_t *ids, int R, int E, int32_t *distinct, int32_t *d_count,
+                         oes_stream_t stream);
+
+/* ------------------------------------------------------------- slot cache */
+
+/* An LRU cache of S slots shared by L layers of E experts each, keyed by
+ * key = layer * E + expert (vLLM fork PR #48, What: one bank keyed by
+ * (layer, expert)).  Device tables: map [L*E] (slot of each key or -1),
+ * slot_key [S] (key of each slot or -1), slot_ts [S] (timestamp of the query
+ * that last touched the slot; 0 = empty), a clock (last timestamp handed
+ * out), counters hits / misses / evictions and decode_freq [L*E].
+ * The slot pool itself (S rows of expert bytes) belongs to the caller. */
+typedef struct oes_slot_cache oes_slot_cache;
+
+/* Allocates the tables (cudaMalloc, synchronous) on the current device and
+ * sets every slot empty.  1 <= S <= OES_MAX_SLOTS, 1 <= E <= OES_MAX_EXPERTS,
+ * L >= 1, L * E < 2^31. */
+int slot_cache_create(int S, int L, int E, oes_slot_cache **out);
+int slot_cache_destroy(oes_slot_cache *cache);
+
+/* Replaces the state: slot_key / slot_ts host [S] (slot_ts 0 for an empty
+ * slot, in [1, clock] otherwise), clock = last timestamp handed out, below
+ * 2^47; rebuilds map, zeroes the counters.  Synchronous. */
+int slot_cache_load_state(oes_slot_cache *cache, const int32_t *slot_key, const int64_t *slot_ts,
+                          int64_t clock);
+
+/* Copies the state to host arrays (any may be NULL): map [L*E], slot_key
+ * [S], slot_ts [S], clock [1], counters [3] = hits, misses, evictions,
+ * decode_freq [L*E].  Synchronises `stream` first. */
+int slot_cache_read_state(const oes_slot_cache *cache, int32_t *map, int32_t *slot_key,
+                          int64_t *slot_ts, int64_t *clock, int64_t *counters,
+                          int64_t *decode_freq, oes_stream_t stream);
+
+/* Device pointer to the layer's expert->slot remap: map + layer * E, [E]
+ * int32, the slot of each of the layer's experts or -1 (vLLM fork PR #48,
+ * What: "physical-row remap").  Valid until slot_cache_destroy. */
+int slot_cache_layer_map(const oes_slot_cache *cache, int layer, const int32_t **e2s);
+
+/* One LRU ensure query (FreeToken PR #676, Solution: lru_ensure is handed
+ * the chunk's distinct experts 128 at a time; the author's reply: LRU only).
+ * experts: device [n] int32, the query's experts of `layer`, strictly
+ * ascending, -1 entries ignored; n <= OES_QUERY_MAX.
+ * Effect: one clock tick; every hit slot and every filled slot gets the new
+ * timestamp; the i-th smallest missing key takes the i-th victim, victims
+ * being the slots the query does not hit in order (empty first, then
+ * ascending (timestamp, slot)); an evicted key leaves the map.
+ * miss: device [3 * OES_QUERY_MAX] int32, entry i = (key, slot, evicted key
+ * or -1) for i < *n_miss; n_miss: device [1] int32.
+ * record_stats = 0 (demand admission): hits / misses / evictions /
+ * decode_freq are not touched (FreeToken PR #676, Solution: "the admissions
+ * stay out of collect_decode_freq and the LRU stats"); 1: they grow, and
+ * decode_freq[key] += 1 for every key of the query.
+ * Device status: OES_DEV_BAD_ID (id out of range or not ascending) or
+ * OES_DEV_CAPACITY (more misses than non-hit slots): nothing changes and
+ * *n_miss = 0.  A query with no valid id is a no-op. */
+int slot_cache_ensure(oes_slot_cache *cache, int layer, const int32_t *experts, int n,
+                      int record_stats, int32_t *miss, int32_t *n_miss, int32_t *status,
+                      oes_stream_t stream);
+
+/* Where the experts live on the host: L layers of E rows of row_bytes each;
+ * layer l's rows start at the mapped address layer_base[l] (several layers
+ * may share one buffer).  row_bytes is a multiple of 16; bases are 16-byte
+ * aligned.  Create/destroy allocate/free a small device table. */
+typedef struct oes_expert_source oes_expert_source;
+int oes_expert_source_create(const void *const *layer_base, int L, int E, int64_t row_bytes,
+                             oes_expert_source **out);
+int oes_expert_source_destroy(oes_expert_source *src);
+
+/* Copies each miss of one query from the host source into its slot
+ * (FreeToken PR #676, Solution: "copies each query's misses before the next
+ * query evicts"; vLLM fork PR #48, What: "row copies are fixed-grid kernels
+ * from the host source's accelerator view").  For i < *n_miss (read on the
+ * device; at most max_misses): pool[slot] <- source row of key, the whole
+ * row (weights, scales and per-expert scalars).  pool: device [S, row_bytes]
+ * with the source's row_bytes.  Rows not named by the miss list are not
+ * written.  Device status OES_DEV_BAD_ID for a key or slot out of range. */
+int slot_cache_copy_misses(const oes_expert_source *src, void *pool, int S, const int32_t *miss,
+                           const int32_t *n_miss, int max_misses, int32_t *status,
+                           oes_stream_t stream);
+
+/* Copies all E rows of one layer into a contiguous device buffer (the
+ * whole-layer stream of FreeToken PR #676, Problem) with one DMA copy.
+ * dst: device [E, row_bytes]. */
+int oes_copy_layer(const oes_expert_source *src, int layer, void *dst, oes_stream_t stream);
+
+/* ------------------------------------------------------------------ align */
+
+/* moe_align_block_size (FreeToken PR #676, Solution and Tests: correct past
+ * 1024 experts, "every route lands once, in a block of its expert"; vLLM
+ * fork PR #48, What: logical alignment, ignore_invalid_experts).  A stable
+ * counting sort of routes r = 0..R-1 by expert ids[r]:
+ *   sorted_ids: device [OES_ALIGN_CAPACITY(R, E, B)] int32: experts in
+ *     ascending order, each expert's routes in ascending r, padded to a
+ *     multiple of B with the value R; every entry past the last block = R;
+ *   block_expert: device [OES_ALIGN_CAPACITY / B] int32: expert of each
+ *     block, -1 past the last block;
+ *   n_post_pad: device [1] int32: used entries (a multiple of B).
+ * Experts with no route get no block.  ids outside [0, E) are skipped; with
+ * ignore_invalid = 0 they also set OES_DEV_BAD_ID.
+ * workspace: device scratch of moe_align_workspace_size(R, E, B) bytes.
+ * 0 <= R < 2^30, 1 <= E <= OES_MAX_EXPERTS, 1 <= B <= 1024. */
+size_t moe_align_workspace_size(int R, int E, int B);
+int moe_align_block_size(const int32_t *ids, int R, int E, int B, int ignore_invalid,
+                         int32_t *sorted_ids, int32_t *block_expert, int32_t *n_post_pad,
+                         int32_t *status, void *workspace, size_t workspace_bytes,
+                         oes_stream_t stream);
+
+/* ------------------------------------------------------------ expert GEMM */
+
+/* The experts a chunk routes to, as the grouped GEMM sees them (FreeToken
+ * PR #676, Solution: "RoutedExperts" carries the layer's expert count and
+ * input scales beside the slot range).  E is the LAYER's expert count and
+ * alone sizes the tiles; S is only the pool's extent.
+ * Expert row layout (row_bytes each, one per slot):
+ *   bf16:  w13 [2I, H] bf16 (rows 0..I-1 gate, I..2I-1 up), w2 [H, I] bf16;
+ *   nvfp4: w13 values [2I, H/2] u8 (e2m1 pairs, element 2i in the low
+ *          nibble), w13 scales [H/64, 2I, 4] e4m3 (K-chunk-major), w2 values
+ *          [H, I/2], w2 scales [I/64, H, 4], then fp32 gs13, gs2, in13, in2
+ *          (global scales and input scales), each section 16-byte aligned.
+ * Weights decode as e2m1 * e4m3 * gs. */
+typedef struct {
+  int layer;                  /* the layer, for the record */
+  int E;                      /* the layer's expert count (sizes the tiles) */
+  const int32_t *e2s;         /* device [E]: slot of each expert, -1 = not resident */
+  int wfmt;                   /* OES_WFMT_BF16 or OES_WFMT_NVFP4 */
+  const void *pool;           /* device base of the slot pool [S, row_bytes] */
+  int64_t row_bytes;          /* bytes per slot row */
+  int S;                      /* slots in the pool */
+  int H, I;                   /* hidden and expert intermediate sizes */
+  const float *input_scale13; /* device [E] or NULL: the layer's w13 input scales */
+  const float *input_scale2;  /* device [E] or NULL: the layer's w2 input scales */
+} oes_routed_experts;
+
+/* Tile plan (FreeToken PR #676, Solution: tiles from tokens per expert of
+ * the layer, nvfp4_moe.prefill_config): the block size B shared by
+ * moe_align_block_size and the GEMM, a function of R and the layer's E only:
+ * 16, 32, 64 or 128, the smallest not below ceil(R / E). */
+int oes_tile_plan(int R, int E, int *block);
+
+/* Workspace bytes of moe_grouped_gemm_slots for T tokens at top-k. */
+size_t moe_grouped_gemm_workspace_size(const oes_routed_experts *view, int T, int k);
+
+/* The grouped SwiGLU expert GEMM over the slot pool (FreeToken PR #676,
+ * Solution: "runs the same grouped GEMM over its layer's slot pool at their
+ * slots, so its output is bit-identical to the streamed layer's").  For
+ * every block b < n_post_pad / B of expert e = block_expert[b], with
+ * weights at slot e2s[e]:
+ *   h = silu(x_r @ gate^T) * (x_r @ up^T), y_r = h @ w2^T    (fp32 sums)
+ * for the routes r in sorted_ids[b*B .. b*B+B) (padding skipped), then
+ *   out[t] = sum_{j=0..k-1} weights[t, j] * y_{t*k+j}         (j in order)
+ * rounded to bf16; h and y are held as 16-bit values in the workspace.
+ * NVFP4 weights are decoded exactly and the global scales applied to the
+ * fp32 sums.  Every reduction order depends only on the routing, never on
+ * the slots, so the result over the pool equals the result over a
+ * contiguous layer buffer (e2s = identity) bit for bit.
+ * x: device [T, H] bf16; ids / weights: the router's [T, k] int32 / fp32
+ * (a route whose id is outside [0, E) contributes nothing); sorted_ids,
+ * block_expert, n_post_pad: moe_align_block_size with B from oes_tile_plan
+ * (anything else is OES_ERR_INVALID_ARG); out: device [T, H] bf16.
+ * A routed expert with e2s < 0 sets OES_DEV_BAD_ID and its routes give 0.
+ * H, I multiples of 64 in [64, 16384]. */
+int moe_grouped_gemm_slots(const oes_routed_experts *view, const uint16_t *x, int T, int k,
+                           const int32_t *ids, const float *weights, const int32_t *sorted_ids,
+                           const int32_t *block_expert, const int32_t *n_post_pad, int B,
+                           void *workspace, size_t workspace_bytes, uint16_t *out,
+                           int32_t *status, oes_stream_t stream);
+
+/* --------------------------------------------------------- whole layer */
+
+/* One chunk of one layer, as the composite calls see it. */
+typedef struct {
+  const float *logits;    /* device [T, E] fp32, or NULL to compute them from x and gate */
+  const uint16_t *gate;   /* device [H, E] bf16 when logits is NULL */
+  const uint16_t *x;      /* device [T, H] bf16 */
+  int T, k;
+  uint16_t *out;          /* device [T, H] bf16 */
+  int32_t *status;        /* device [1] int32, OR-ed */
+  void *workspace;        /* device scratch of moe_layer_workspace_size() bytes, 256-aligned */
+  size_t workspace_bytes;
+} oes_chunk;
+
+/* The layer as stored: expert count, sizes, weight format and the layer's
+ * input scales (device [E] each, or NULL). */
+typedef struct {
+  int E, H, I, wfmt;
+  const float *input_scale13;
+  const float *input_scale2;
+} oes_layer_desc;
+
+size_t moe_layer_workspace_size(const oes_layer_desc *layer, int T, int k);
+
+/* Device pointers to the router's outputs and the align outputs inside a
+ * layer workspace (for checking the steps of a composite call): ids [T*k],
+ * weights [T*k], distinct [min(T*k, E)] and its count, sorted_ids, block_expert,
+ * n_post_pad.  Any output pointer may be NULL. */
+int moe_layer_workspace_views(const oes_layer_desc *layer, int T, int k, void *workspace,
+                              int32_t **ids, float **weights, int32_t **distinct,
+                              int32_t **d_count, int32_t **sorted_ids, int32_t **block_expert,
+                              int32_t **n_post_pad);
+
+/* The slot path, stream-ordered on `stream` with no host synchronisation
+ * (FreeToken PR #676, Solution): route (or gate logits + route) -> distinct
+ * experts -> for each query of OES_QUERY_MAX distinct experts: ensure
+ * (record_stats as given) then copy its misses -> align -> grouped GEMM
+ * over `pool` through the layer's remap.  The number of queries is
+ * ceil(min(T*k, E) / OES_QUERY_MAX), known on the host.
+ * A layer must never route to more experts than the cache holds (the
+ * author's reply on FreeToken PR #676): with min(T*k, E) > S this returns
+ * OES_ERR_CAPACITY and launches nothing; the caller streams the layer. */
+int moe_layer_forward_slots(oes_slot_cache *cache, const oes_expert_source *src, void *pool,
+                            int layer, const oes_layer_desc *desc, const oes_chunk *chunk,
+                            int record_stats, oes_stream_t stream);
+
+/* The whole-layer streamed path, the baseline the slot path must equal
+ * (FreeToken PR #676, Problem: every expert of the layer is streamed for the
+ * chunk): copy all E rows of `layer` into layer_buf (device [E, row_bytes])
+ * on copy_stream, route and align on compute_stream meanwhile, then run the
+ * same grouped GEMM over layer_buf with the identity remap once the copy is
+ * done.  copy_stream may equal compute_stream. */
+int moe_layer_forward_stream(const oes_expert_source *src, void *layer_buf, int layer,
+                             const oes_layer_desc *desc, const oes_chunk *chunk,
+                             oes_stream_t copy_stream, oes_stream_t compute_stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OES_H */

@@ -1,0 +1,709 @@
+// The grouped SwiGLU expert GEMM over the slot pool, on tcgen05 / TMEM / TMA.
+//
+// FreeToken PR #676, Solution: the chunk "runs the same grouped GEMM over
+// its layer's slot pool at their slots, so its output is bit-identical to
+// the streamed layer's"; the expert view carries the layer's expert count
+// and the NVFP4 prefill sizes its tiles by tokens per expert of the layer.
+// vLLM fork PR #48, What: logical alignment plus a physical-row remap.
+//
+// Design (swap-AB): the weight rows of an expert are the MMA's M side (128
+// rows per tile) and the routes of one align block are its N side (the
+// block's routes, rounded up to 16), both operands K-major.  One persistent
+// kernel template runs both GEMMs:
+//   GEMM1 (MODE 1): per (block, 128 intermediate rows): gate and up tiles
+//     into two TMEM accumulators, epilogue h = silu(g) * u -> 16-bit h;
+//     the block's token rows are gathered from x by TMA (tile::gather4).
+//   GEMM2 (MODE 2): per (block, 128 output rows): y = h @ w2^T -> bf16 y
+//     at each route's row.
+// Warp roles: 0 weight producer (TMA), 1 MMA issuer (one thread), 2 TMEM
+// allocator, 3 token/h producer (TMA), 4-7 epilogue, 8-11 NVFP4 converters
+// (NVFP4 only: e2m1 x e4m3 decoded exactly into f16 tiles in shared memory;
+// the per-expert fp32 global scale is applied to the fp32 sums).
+// The weights of a slot are addressed through a 3-D tensor map over the
+// pool [S][rows][K]; the slot coordinate comes from the remap, so the same
+// kernel over a contiguous layer buffer (remap = identity) runs the same
+// instructions on the same data in the same order: bit-identical output.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace oes {
+namespace {
+
+constexpr int kTileM = 128;  // weight rows per MMA
+constexpr int kChunkK = 64;  // K elements per pipeline stage (128 bytes of 16-bit)
+
+struct GemmMaps {
+  CUtensorMap a;   // 16-bit weights [S][rows][K] (bf16 path)
+  CUtensorMap q;   // NVFP4 values [S][rows][K/2] bytes
+  CUtensorMap sc;  // NVFP4 scales [S][K/64][rows] u32
+  CUtensorMap b;   // GEMM1: x (or f16 x) [T][H]; GEMM2: h [cap][I]
+};
+
+struct GemmParams {
+  const int32_t* sorted_ids;
+  const int32_t* block_expert;
+  const int32_t* n_post_pad;
+  const int32_t* e2s;
+  const uint8_t* pool;
+  int64_t row_bytes;
+  int64_t scal_off;  // NVFP4: byte offset of the fp32 scalars in a row
+  int R, k, BN, H, I, E, S;
+  int n_mtiles, n_kc, up_row0;  // up_row0: first up row of w13 (= I)
+  int NS, NR;                   // pipeline depths
+  uint32_t tmem_cols;
+  uint16_t* h;  // [cap, I]
+  uint16_t* y;  // [R, H] bf16
+  int32_t* status;
+};
+
+struct Unit {
+  int b, m, slot, nvalid;
+  bool skip;
+};
+
+// Which block / tile a unit is, the slot of its expert, and how many of the
+// block's entries are real routes (padding, value R, only at the end).
+__device__ __forceinline__ Unit unit_info(const GemmParams& p, int u, int nb) {
+  Unit t;
+  t.b = u % nb;
+  t.m = u / nb;
+  const int e = p.block_expert[t.b];
+  t.slot = (e >= 0 && e < p.E) ? p.e2s[e] : -1;
+  const int32_t* s = p.sorted_ids + (int64_t)t.b * p.BN;
+  if (s[p.BN - 1] < p.R) {
+    t.nvalid = p.BN;
+  } else {
+    int lo = 0, hi = p.BN - 1;  // first index holding padding
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s[mid] < p.R) lo = mid + 1;
+      else hi = mid;
+    }
+    t.nvalid = lo;
+  }
+  t.skip = t.slot < 0 || t.slot >= p.S || t.nvalid == 0;
+  return t;
+}
+
+__device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
+
+__device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(r) : "r"(byte));
+  return r;
+}
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(r) : "r"(two));
+  return r;
+}
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// One weight row of one K chunk: 32 bytes of e2m1 pairs and a 32-bit word of
+// four e4m3 scales (one per 16 elements) -> 64 f16 = 8 x 16 bytes, stored at
+// the 128-byte-swizzled position of row `row` of a K-major tile.  Every
+// product e2m1 * e4m3 has at most 6 significant bits and lies in
+// [2^-10, 2688], so it is exact in f16.
+__device__ __forceinline__ void convert_row(const uint8_t* q, uint32_t scales, uint8_t* tile,
+                                            int row) {
+  const uint4 q0 = *reinterpret_cast<const uint4*>(q);
+  const uint4 q1 = *reinterpret_cast<const uint4*>(q + 16);
+  const uint32_t s01 = cvt_e4m3x2_f16x2(scales & 0xFFFFu);
+  const uint32_t s23 = cvt_e4m3x2_f16x2(scales >> 16);
+  const uint32_t sc[4] = {__byte_perm(s01, 0, 0x1010), __byte_perm(s01, 0, 0x3232),
+                          __byte_perm(s23, 0, 0x1010), __byte_perm(s23, 0, 0x3232)};
+  const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+  uint8_t* rowp = tile + row * 128;
+  const int sw = row & 7;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t wd = words[c];
+    const uint32_t s = sc[c >> 1];
+    uint4 o;
+    o.x = hmul2_u32(cvt_e2m1x2_f16x2(wd & 0xFFu), s);
+    o.y = hmul2_u32(cvt_e2m1x2_f16x2((wd >> 8) & 0xFFu), s);
+    o.z = hmul2_u32(cvt_e2m1x2_f16x2((wd >> 16) & 0xFFu), s);
+    o.w = hmul2_u32(cvt_e2m1x2_f16x2(wd >> 24), s);
+    *reinterpret_cast<uint4*>(rowp + ((c ^ sw) << 4)) = o;
+  }
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+template <int MODE, int WF>
+__global__ void __launch_bounds__(WF ? 384 : 256, 1)
+    grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  constexpr int kA = (MODE == 1) ? 2 : 1;  // weight tiles per stage (gate + up, or w2)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int a_bytes = kA * kTileM * 128;
+  const int b_bytes = p.BN * 128;
+  const int stage_bytes = a_bytes + b_bytes;
+  const int rq_bytes = kA * kTileM * 32;
+  const int rs_bytes = kA * kTileM * 4;
+  const int raw_stage = ((rq_bytes + rs_bytes) + 1023) & ~1023;
+  uint8_t* stages = smem;
+  uint8_t* raw = stages + p.NS * stage_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + (WF ? p.NR * raw_stage : 0));
+  uint64_t* full = bars;
+  uint64_t* empty = full + p.NS;
+  uint64_t* rfull = empty + p.NS;
+  uint64_t* rempty = rfull + p.NR;
+  uint64_t* tfull = rempty + p.NR;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
+  int32_t* tok = reinterpret_cast<int32_t*>(tmem_holder + 4);  // [BN] token rows of the gather
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.NS; ++s) {
+      mbar_init(&full[s], WF ? 5 : 2);
+      mbar_init(&empty[s], 1);
+    }
+    for (int r = 0; r < p.NR; ++r) {
+      mbar_init(&rfull[r], 1);
+      mbar_init(&rempty[r], 4);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&maps.b);
+    if (WF) {
+      tma_prefetch_desc(&maps.q);
+      tma_prefetch_desc(&maps.sc);
+    } else {
+      tma_prefetch_desc(&maps.a);
+    }
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_holder, p.tmem_cols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int nb = *p.n_post_pad / p.BN;
+  const int total = nb * p.n_mtiles;
+  const uint32_t acc_cols = (MODE == 1) ? 2 * p.BN : p.BN;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------- weight producer
+      int s = 0, ph = 0, r = 0, rph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        const Unit t = unit_info(p, u, nb);
+        if (t.skip) continue;
+        const int row0 = t.m * kTileM;
+        for (int kc = 0; kc < p.n_kc && ok; ++kc) {
+          if (!WF) {
+            ok = mbar_wait(&empty[s], ph ^ 1, p.status);
+            if (!ok) break;
+            uint8_t* A = stages + s * stage_bytes;
+            mbar_arrive_expect_tx(&full[s], a_bytes);
+            tma_load_3d(A, &maps.a, &full[s], kc * kChunkK, row0, t.slot);
+            if (MODE == 1)
+              tma_load_3d(A + kTileM * 128, &maps.a, &full[s], kc * kChunkK, p.up_row0 + row0,
+                          t.slot);
+            if (++s == p.NS) { s = 0; ph ^= 1; }
+          } else {
+            ok = mbar_wait(&rempty[r], rph ^ 1, p.status);
+            if (!ok) break;
+            uint8_t* Q = raw + r * raw_stage;
+            uint8_t* SC = Q + rq_bytes;
+            mbar_arrive_expect_tx(&rfull[r], rq_bytes + rs_bytes);
+            tma_load_3d(Q, &maps.q, &rfull[r], kc * (kChunkK / 2), row0, t.slot);
+            tma_load_3d(SC, &maps.sc, &rfull[r], row0, kc, t.slot);
+            if (MODE == 1) {
+              tma_load_3d(Q + kTileM * 32, &maps.q, &rfull[r], kc * (kChunkK / 2),
+                          p.up_row0 + row0, t.slot);
+              tma_load_3d(SC + kTileM * 4, &maps.sc, &rfull[r], p.up_row0 + row0, kc, t.slot);
+            }
+            if (++r == p.NR) { r = 0; rph ^= 1; }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------- MMA issuer
+      int s = 0, ph = 0;
+      uint32_t use[2] = {0, 0};
+      int a = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        const Unit t = unit_info(p, u, nb);
+        if (t.skip) continue;
+        const uint32_t N = round16(t.nvalid);
+        const uint32_t idesc = idesc_f16(WF ? 0u : 1u, kTileM, N);
+        ok = mbar_wait(&tempty[a], (use[a] & 1) ^ 1, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + a * acc_cols;
+        for (int kc = 0; kc < p.n_kc; ++kc) {
+          ok = mbar_wait(&full[s], ph, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t A = smem_u32(stages + s * stage_bytes);
+          const uint32_t B = A + a_bytes;
+#pragma unroll
+          for (int kk = 0; kk < kChunkK / 16; ++kk) {
+            const uint32_t acc = (kc | kk) ? 1u : 0u;
+            const uint64_t bd = smem_desc_sw128(B + kk * 32);
+            tc_mma_f16(d0, smem_desc_sw128(A + kk * 32), bd, idesc, acc);
+            if (MODE == 1)
+              tc_mma_f16(d0 + p.BN, smem_desc_sw128(A + kTileM * 128 + kk * 32), bd, idesc, acc);
+          }
+          tc_commit(&empty[s]);
+          if (++s == p.NS) { s = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[a]);
+        ++use[a];
+        a ^= 1;
+      }
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------- token / h producer
+    int s = 0, ph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const Unit t = unit_info(p, u, nb);
+      if (t.skip) continue;
+      const int N = round16(t.nvalid);
+      if (MODE == 1) {
+        __syncwarp();
+        for (int n = lane; n < N; n += 32)
+          tok[n] = (n < t.nvalid) ? p.sorted_ids[(int64_t)t.b * p.BN + n] / p.k : 0;
+        __syncwarp();
+      }
+      if (lane == 0) {
+        for (int kc = 0; kc < p.n_kc; ++kc) {
+          ok = mbar_wait(&empty[s], ph ^ 1, p.status);
+          if (!ok) break;
+          uint8_t* B = stages + s * stage_bytes + a_bytes;
+          if (MODE == 1) {
+            mbar_arrive_expect_tx(&full[s], N * 128);
+            for (int g = 0; g < N; g += 4)
+              tma_gather4(B + g * 128, &maps.b, &full[s], kc * kChunkK, tok[g], tok[g + 1],
+                          tok[g + 2], tok[g + 3]);
+          } else {
+            mbar_arrive_expect_tx(&full[s], b_bytes);
+            tma_load_2d(B, &maps.b, &full[s], kc * kChunkK, t.b * p.BN);
+          }
+          if (++s == p.NS) { s = 0; ph ^= 1; }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int row = q * 32 + lane;  // TMEM lane = weight row within the tile
+    uint32_t use[2] = {0, 0};
+    int a = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const Unit t = unit_info(p, u, nb);
+      if (t.skip) {
+        if (MODE == 2 && t.nvalid > 0) {
+          // an expert without a slot: its routes get zeros (and a status bit)
+          const int col = t.m * kTileM + row;
+          if (col < p.H)
+            for (int n = 0; n < t.nvalid; ++n)
+              p.y[(int64_t)p.sorted_ids[(int64_t)t.b * p.BN + n] * p.H + col] = 0;
+          if (row == 0) set_status(p.status, OES_DEV_BAD_ID);
+        }
+        continue;
+      }
+      ok = mbar_wait(&tfull[a], use[a] & 1, p.status);
+      if (!ok) break;
+      tc_fence_after();
+      float gs = 1.0f;
+      if (WF)
+        gs = *reinterpret_cast<const float*>(p.pool + (int64_t)t.slot * p.row_bytes + p.scal_off +
+                                             (MODE == 1 ? 0 : 4));
+      const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16) + a * acc_cols;
+      const int N = round16(t.nvalid);
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        uint32_t g[16];
+        tmem_ld_16(tl + c0, g);
+        if (MODE == 1) {
+          uint32_t v[16];
+          tmem_ld_16(tl + p.BN + c0, v);
+          tc_wait_ld();
+          const int i = t.m * kTileM + row;
+          if (i < p.I) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int n = c0 + j;
+              if (n < t.nvalid) {
+                const float gv = __uint_as_float(g[j]) * gs;
+                const float uv = __uint_as_float(v[j]) * gs;
+                const float hv = silu(gv) * uv;
+                uint16_t hb;
+                if (WF) hb = __half_as_ushort(__float2half_rn(hv));
+                else hb = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+                p.h[((int64_t)t.b * p.BN + n) * p.I + i] = hb;
+              }
+            }
+          }
+        } else {
+          tc_wait_ld();
+          const int col = t.m * kTileM + row;
+          if (col < p.H) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int n = c0 + j;
+              if (n < t.nvalid) {
+                const int r = p.sorted_ids[(int64_t)t.b * p.BN + n];
+                const float yv = __uint_as_float(g[j]) * gs;
+                p.y[(int64_t)r * p.H + col] = __bfloat16_as_ushort(__float2bfloat16_rn(yv));
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[a]);
+      ++use[a];
+      a ^= 1;
+    }
+  } else if (WF && warp >= 8) {
+    // --------------------------------------------------- NVFP4 converters
+    const int ct = threadIdx.x - 256;  // 0..127: one weight row of each tile
+    int s = 0, ph = 0, r = 0, rph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const Unit t = unit_info(p, u, nb);
+      if (t.skip) continue;
+      for (int kc = 0; kc < p.n_kc; ++kc) {
+        ok = mbar_wait(&rfull[r], rph, p.status) && mbar_wait(&empty[s], ph ^ 1, p.status);
+        if (!ok) break;
+        const uint8_t* Q = raw + r * raw_stage;
+        const uint32_t* SC = reinterpret_cast<const uint32_t*>(Q + rq_bytes);
+        uint8_t* A = stages + s * stage_bytes;
+#pragma unroll
+        for (int h2 = 0; h2 < kA; ++h2) {
+          const int rr = h2 * kTileM + ct;
+          convert_row(Q + rr * 32, SC[rr], A + h2 * kTileM * 128, ct);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&rempty[r]);
+          mbar_arrive(&full[s]);
+        }
+        if (++r == p.NR) { r = 0; rph ^= 1; }
+        if (++s == p.NS) { s = 0; ph ^= 1; }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+// f16 copy of x for the NVFP4 path (its MMAs run on f16 operands).
+__global__ void x_to_f16_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ x16,
+                                int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float f = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
+    x16[i] = __half_as_ushort(__float2half_rn(f));
+  }
+}
+
+// out[t, :] = sum_{j=0..k-1} w[t, j] * y[t*k + j, :], fp32 in j order -> bf16.
+__global__ void combine_kernel(const uint16_t* __restrict__ y, const float* __restrict__ w,
+                               const int32_t* __restrict__ ids, int T, int k, int H, int E,
+                               uint16_t* __restrict__ out) {
+  const int vec = H / 8;
+  const int64_t n = (int64_t)T * vec;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = static_cast<int>(i / vec);
+    const int c = static_cast<int>(i % vec);
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int j = 0; j < k; ++j) {
+      const int e = ids[(int64_t)t * k + j];
+      if (e < 0 || e >= E) continue;
+      const float wj = w[(int64_t)t * k + j];
+      const uint4 v = *reinterpret_cast<const uint4*>(y + ((int64_t)t * k + j) * H + c * 8);
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] = fmaf(wj, __uint_as_float(u[q] << 16), acc[2 * q]);
+        acc[2 * q + 1] = fmaf(wj, __uint_as_float(u[q] & 0xFFFF0000u), acc[2 * q + 1]);
+      }
+    }
+    uint4 o;
+    uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * q]));
+      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * q + 1]));
+      op[q] = lo | (hi << 16);
+    }
+    *reinterpret_cast<uint4*>(out + (int64_t)t * H + c * 8) = o;
+  }
+}
+
+struct Sections {
+  int64_t w13, w2, w13q, w13s, w2q, w2s, scal;
+};
+
+Sections sections(int wfmt, int H, int I) {
+  Sections s{};
+  if (wfmt == OES_WFMT_BF16) {
+    s.w13 = 0;
+    s.w2 = (int64_t)2 * I * H * 2;
+  } else {
+    s.w13q = 0;
+    s.w13s = s.w13q + (int64_t)2 * I * H / 2;
+    s.w2q = s.w13s + (int64_t)2 * I * H / 16;
+    s.w2s = s.w2q + (int64_t)H * I / 2;
+    s.scal = s.w2s + (int64_t)H * I / 16;
+  }
+  return s;
+}
+
+int64_t expected_row_bytes(int wfmt, int H, int I) {
+  if (wfmt == OES_WFMT_BF16) return (int64_t)6 * H * I;
+  return sections(wfmt, H, I).scal + 16;
+}
+
+struct Ws {
+  uint16_t* h;
+  uint16_t* y;
+  uint16_t* x16;
+  size_t bytes;
+};
+
+Ws carve(void* base, int T, int k, int E, int H, int I, int B, int wfmt) {
+  Ws w{};
+  const int64_t R = (int64_t)T * k;
+  const int64_t cap = OES_ALIGN_CAPACITY(R, E, B);
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  size_t off = 0;
+  uint8_t* p = static_cast<uint8_t*>(base);
+  w.h = reinterpret_cast<uint16_t*>(p + off);
+  off += up((size_t)cap * I * 2);
+  w.y = reinterpret_cast<uint16_t*>(p + off);
+  off += up((size_t)R * H * 2);
+  w.x16 = reinterpret_cast<uint16_t*>(p + off);
+  if (wfmt == OES_WFMT_NVFP4) off += up((size_t)T * H * 2);
+  w.bytes = off + 256;
+  return w;
+}
+
+int smem_plan(int MODE, int wf, int BN, int* NS, int* NR, size_t* bytes) {
+  const int kA = MODE == 1 ? 2 : 1;
+  const int stage = kA * kTileM * 128 + BN * 128;
+  const int raw_stage = ((kA * kTileM * 36) + 1023) / 1024 * 1024;
+  const int budget = 200 * 1024;
+  const int nr = wf ? (MODE == 1 ? 6 : 8) : 0;
+  const int ns = std::min(8, (budget - nr * raw_stage) / stage);
+  if (ns < 2) return OES_ERR_UNSUPPORTED;
+  *NS = ns;
+  *NR = wf ? nr : 1;
+  *bytes = 1024 + (size_t)ns * stage + (size_t)nr * raw_stage +
+           (size_t)(2 * ns + 2 * (*NR) + 4) * 8 + 16 + (size_t)BN * 4 + 64;
+  return OES_OK;
+}
+
+template <int MODE, int WF>
+int launch_gemm(const GemmMaps& maps, const GemmParams& p0, int BN, cudaStream_t stream) {
+  GemmParams p = p0;
+  size_t smem;
+  int rc = smem_plan(MODE, WF, BN, &p.NS, &p.NR, &smem);
+  if (rc) {
+    set_error("grouped GEMM: no pipeline fits BN=%d", BN);
+    return rc;
+  }
+  p.tmem_cols = (MODE == 1) ? 4 * BN : 2 * BN;
+  if (p.tmem_cols < 32) p.tmem_cols = 32;
+  static bool configured = false;
+  if (!configured) {
+    OES_TRY_CUDA(cudaFuncSetAttribute(grouped_gemm_kernel<MODE, WF>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024));
+    configured = true;
+  }
+  grouped_gemm_kernel<MODE, WF><<<num_sms(), WF ? 384 : 256, smem, stream>>>(maps, p);
+  OES_CHECK_LAUNCH("grouped_gemm_kernel");
+  return OES_OK;
+}
+
+}  // namespace
+
+int tile_plan(int R, int E) {
+  const int per = (R + E - 1) / std::max(E, 1);
+  if (per <= 16) return 16;
+  if (per <= 32) return 32;
+  if (per <= 64) return 64;
+  return 128;
+}
+
+}  // namespace oes
+
+using namespace oes;
+
+extern "C" int oes_tile_plan(int R, int E, int* block) {
+  OES_REQUIRE(block && R >= 0 && E >= 1, "oes_tile_plan: bad arguments");
+  *block = tile_plan(R, E);
+  return OES_OK;
+}
+
+extern "C" size_t moe_grouped_gemm_workspace_size(const oes_routed_experts* v, int T, int k) {
+  if (!v || T < 0 || k < 1 || v->E < 1) return 0;
+  const int B = tile_plan(T * k, v->E);
+  return carve(nullptr, T, k, v->E, v->H, v->I, B, v->wfmt).bytes;
+}
+
+extern "C" int moe_grouped_gemm_slots(const oes_routed_experts* v, const uint16_t* x, int T, int k,
+                                      const int32_t* ids, const float* weights,
+                                      const int32_t* sorted_ids, const int32_t* block_expert,
+                                      const int32_t* n_post_pad, int B, void* workspace,
+                                      size_t workspace_bytes, uint16_t* out, int32_t* status,
+                                      oes_stream_t stream) {
+  OES_REQUIRE(v && x && ids && weights && sorted_ids && block_expert && n_post_pad && out &&
+                  workspace && v->pool && v->e2s,
+              "moe_grouped_gemm_slots: null pointer");
+  const int E = v->E, H = v->H, I = v->I, S = v->S;
+  OES_REQUIRE(E >= 1 && E <= OES_MAX_EXPERTS && S >= 1, "moe_grouped_gemm_slots: bad E=%d S=%d", E, S);
+  OES_REQUIRE(H >= 64 && I >= 64 && H % 64 == 0 && I % 64 == 0 && H <= 16384 && I <= 16384,
+              "moe_grouped_gemm_slots: H=%d I=%d must be multiples of 64 in [64, 16384]", H, I);
+  OES_REQUIRE(v->wfmt == OES_WFMT_BF16 || v->wfmt == OES_WFMT_NVFP4, "moe_grouped_gemm_slots: bad wfmt");
+  OES_REQUIRE(T >= 0 && T <= (1 << 24) && k >= 1 && k <= OES_MAX_TOPK,
+              "moe_grouped_gemm_slots: bad T=%d k=%d", T, k);
+  const int64_t need_row = expected_row_bytes(v->wfmt, H, I);
+  OES_REQUIRE(v->row_bytes >= need_row && v->row_bytes % 16 == 0,
+              "moe_grouped_gemm_slots: row_bytes %lld (layout needs %lld, multiple of 16)",
+              (long long)v->row_bytes, (long long)need_row);
+  OES_REQUIRE(((uintptr_t)v->pool & 15) == 0 && ((uintptr_t)x & 15) == 0 && ((uintptr_t)out & 15) == 0,
+              "moe_grouped_gemm_slots: pool, x and out must be 16-byte aligned");
+  const int R = T * k;
+  const int plan = tile_plan(R, E);
+  OES_REQUIRE(B == plan, "moe_grouped_gemm_slots: block %d differs from the tile plan %d (R=%d, E=%d)",
+              B, plan, R, E);
+  if (T == 0) return OES_OK;
+  OES_REQUIRE(((uintptr_t)workspace & 255) == 0, "moe_grouped_gemm_slots: workspace not 256-byte aligned");
+  const Ws ws = carve(workspace, T, k, E, H, I, B, v->wfmt);
+  OES_REQUIRE(workspace_bytes >= ws.bytes, "moe_grouped_gemm_slots: workspace %zu < %zu bytes",
+              workspace_bytes, ws.bytes);
+  const int64_t cap = OES_ALIGN_CAPACITY(R, E, B);
+  const Sections sec = sections(v->wfmt, H, I);
+  const uint8_t* pool = static_cast<const uint8_t*>(v->pool);
+  const int wf = v->wfmt == OES_WFMT_NVFP4;
+
+  GemmMaps m1{}, m2{};
+  int rc;
+  const uint16_t* xb = x;
+  if (wf) {
+    const int blocks = (int)std::min<int64_t>(ceil_div64((int64_t)T * H, 256), (int64_t)num_sms() * 8);
+    x_to_f16_kernel<<<blocks, 256, 0, stream>>>(x, ws.x16, (int64_t)T * H);
+    OES_CHECK_LAUNCH("x_to_f16_kernel");
+    xb = ws.x16;
+  }
+  const CUtensorMapDataType t16 = wf ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  {
+    const uint64_t dims[2] = {(uint64_t)H, (uint64_t)T};
+    const uint64_t str[1] = {(uint64_t)H * 2};
+    const uint32_t box[2] = {64, 1};
+    if ((rc = encode_tiled(&m1.b, t16, 2, xb, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)I, (uint64_t)cap};
+    const uint64_t str[1] = {(uint64_t)I * 2};
+    const uint32_t box[2] = {64, (uint32_t)B};
+    if ((rc = encode_tiled(&m2.b, t16, 2, ws.h, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
+  }
+  const uint64_t rb = (uint64_t)v->row_bytes;
+  if (!wf) {
+    const uint32_t box[3] = {64, 128, 1};
+    const uint64_t d1[3] = {(uint64_t)H, (uint64_t)2 * I, (uint64_t)S}, s1[2] = {(uint64_t)H * 2, rb};
+    if ((rc = encode_tiled(&m1.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pool + sec.w13, d1, s1, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B)))
+      return rc;
+    const uint64_t d2[3] = {(uint64_t)I, (uint64_t)H, (uint64_t)S}, s2[2] = {(uint64_t)I * 2, rb};
+    if ((rc = encode_tiled(&m2.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pool + sec.w2, d2, s2, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B)))
+      return rc;
+  } else {
+    const uint32_t qbox[3] = {32, 128, 1}, sbox[3] = {128, 1, 1};
+    const uint64_t dq1[3] = {(uint64_t)H / 2, (uint64_t)2 * I, (uint64_t)S}, sq1[2] = {(uint64_t)H / 2, rb};
+    if ((rc = encode_tiled(&m1.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, pool + sec.w13q, dq1, sq1, qbox,
+                           CU_TENSOR_MAP_SWIZZLE_NONE)))
+      return rc;
+    const uint64_t ds1[3] = {(uint64_t)2 * I, (uint64_t)H / 64, (uint64_t)S},
+                   ss1[2] = {(uint64_t)2 * I * 4, rb};
+    if ((rc = encode_tiled(&m1.sc, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, pool + sec.w13s, ds1, ss1, sbox,
+                           CU_TENSOR_MAP_SWIZZLE_NONE)))
+      return rc;
+    const uint64_t dq2[3] = {(uint64_t)I / 2, (uint64_t)H, (uint64_t)S}, sq2[2] = {(uint64_t)I / 2, rb};
+    if ((rc = encode_tiled(&m2.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, pool + sec.w2q, dq2, sq2, qbox,
+                           CU_TENSOR_MAP_SWIZZLE_NONE)))
+      return rc;
+    const uint64_t ds2[3] = {(uint64_t)H, (uint64_t)I / 64, (uint64_t)S}, ss2[2] = {(uint64_t)H * 4, rb};
+    if ((rc = encode_tiled(&m2.sc, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, pool + sec.w2s, ds2, ss2, sbox,
+                           CU_TENSOR_MAP_SWIZZLE_NONE)))
+      return rc;
+  }
+
+  GemmParams p{};
+  p.sorted_ids = sorted_ids;
+  p.block_expert = block_expert;
+  p.n_post_pad = n_post_pad;
+  p.e2s = v->e2s;
+  p.pool = pool;
+  p.row_bytes = v->row_bytes;
+  p.scal_off = sec.scal;
+  p.R = R;
+  p.k = k;
+  p.BN = B;
+  p.H = H;
+  p.I = I;
+  p.E = E;
+  p.S = S;
+  p.up_row0 = I;
+  p.h = ws.h;
+  p.y = ws.y;
+  p.status = status;
+
+  GemmParams p1 = p;
+  p1.n_mtiles = ceil_div(I, kTileM);
+  p1.n_kc = H / kChunkK;
+  rc = wf ? launch_gemm<1, 1>(m1, p1, B, stream) : launch_gemm<1, 0>(m1, p1, B, stream);
+  if (rc) return rc;
+  GemmParams p2 = p;
+  p2.n_mtiles = ceil_div(H, kTileM);
+  p2.n_kc = I / kChunkK;
+  rc = wf ? launch_gemm<2, 1>(m2, p2, B, stream) : launch_gemm<2, 0>(m2, p2, B, stream);
+  if (rc) return rc;
+  const int64_t nvec = (int64_t)T * (H / 8);
+  combine_kernel<<<(int)std::min<int64_t>(ceil_div64(nvec, 256), (int64_t)num_sms() * 8), 256, 0,
+                   stream>>>(ws.y, weights, ids, T, k, H, E, out);
+  OES_CHECK_LAUNCH("combine_kernel");
+  return OES_OK;
+}

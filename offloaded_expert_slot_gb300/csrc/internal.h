@@ -1,0 +1,29 @@
+// Library-private definitions shared by the .cu files of liboes.
+#pragma once
+
+#include <stdint.h>
+
+#include <vector>
+
+#include "oes.h"
+
+struct oes_slot_cache {
+  int S, L, E, device;
+  void* block;           // one allocation for every table
+  int32_t* map;          // [L*E] slot of each key, -1 if absent
+  int32_t* slot_key;     // [S] key held by each slot, -1 if empty
+  int64_t* slot_ts;      // [S] timestamp of the last query that touched the slot, 0 if empty
+  int64_t* ctr;          // [4] clock, hits, misses, evictions
+  int64_t* decode_freq;  // [L*E]
+};
+
+struct oes_expert_source {
+  int L, E;
+  int64_t row_bytes;
+  std::vector<const void*> host_bases;  // [L] mapped addresses
+  const uint8_t** dev_bases;            // device copy of host_bases
+};
+
+namespace oes {
+int tile_plan(int R, int E);
+}  // namespace oes

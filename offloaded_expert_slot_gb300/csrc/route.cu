@@ -1,0 +1,184 @@
+// Routing: gate logits (tiny workload), warp-per-token top-k with softmax
+// renormalisation, and the chunk's distinct experts as a fixed-length
+// sorted list (FreeToken PR #676, Solution).
+#include <math.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace oes {
+namespace {
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// logits[t, e] = sum_h x[t, h] * gate[h, e]; one thread per (t, e), h in order.
+__global__ void gate_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gate,
+                                   int T, int H, int E, float* __restrict__ logits) {
+  const int t = blockIdx.y;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x) {
+    float acc = 0.f;
+    const uint16_t* xr = x + (size_t)t * H;
+    for (int h = 0; h < H; ++h)
+      acc = fmaf(bf16_to_f32(xr[h]), bf16_to_f32(gate[(size_t)h * E + e]), acc);
+    logits[(size_t)t * E + e] = acc;
+  }
+}
+
+// One warp per token.  Lane l holds logits l, l+32, ...; k rounds of a
+// warp-wide arg-max (larger value first, ties to the lower id); a selected
+// entry is replaced by NaN, which loses every comparison.
+template <int EPL>
+__global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                            int32_t* __restrict__ ids, float* __restrict__ weights) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+    const float* row = logits + (size_t)t * E;
+    float v[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+      const int e = lane + 32 * j;
+      v[j] = (e < E) ? __ldg(row + e) : -INFINITY;
+    }
+    float my_v = 0.f;  // lane j keeps round j's winner
+    int my_e = 0;
+    float top = 0.f;
+    for (int r = 0; r < k; ++r) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) {
+        const int e = lane + 32 * j;
+        if (v[j] > bv || (v[j] == bv && e < be)) {
+          bv = v[j];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        if (ov > bv || (ov == bv && oe < be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < EPL; ++j)
+        if (lane + 32 * j == be) v[j] = __int_as_float(0x7fffffff);
+      if (r == 0) top = bv;
+      if (lane == r) {
+        my_v = bv;
+        my_e = be;
+      }
+    }
+    const float ex = (lane < k) ? expf(my_v - top) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane < k) {
+      ids[(size_t)t * k + lane] = my_e;
+      weights[(size_t)t * k + lane] = ex / sum;
+    }
+  }
+}
+
+// Single CTA: presence flags over the E experts, then a block-wide exclusive
+// scan turns flags into output positions.
+__global__ void __launch_bounds__(1024)
+    distinct_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ distinct,
+                    int32_t* __restrict__ d_count) {
+  extern __shared__ uint8_t flag[];
+  __shared__ int warp_tot[32];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  for (int i = tid; i < E; i += nt) flag[i] = 0;
+  __syncthreads();
+  for (int r = tid; r < R; r += nt) {
+    const int v = __ldg(ids + r);
+    if (v >= 0 && v < E) flag[v] = 1;
+  }
+  __syncthreads();
+  const int per = (E + nt - 1) / nt;
+  const int b0 = min(E, tid * per), b1 = min(E, b0 + per);
+  int cnt = 0;
+  for (int i = b0; i < b1; ++i) cnt += flag[i];
+  const int lane = tid & 31, w = tid >> 5;
+  int incl = cnt;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    const int nw = nt >> 5;
+    int s = (lane < nw) ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, s, off);
+      if (lane >= off) s += o;
+    }
+    if (lane < nw) warp_tot[lane] = s;  // inclusive per warp
+  }
+  __syncthreads();
+  int pos = incl - cnt + (w ? warp_tot[w - 1] : 0);
+  for (int i = b0; i < b1; ++i)
+    if (flag[i]) distinct[pos++] = i;
+  const int D = warp_tot[(nt >> 5) - 1];
+  const int Lq = min(R, E);
+  for (int i = D + tid; i < Lq; i += nt) distinct[i] = -1;
+  if (tid == 0) *d_count = D;
+}
+
+}  // namespace
+}  // namespace oes
+
+using namespace oes;
+
+extern "C" int moe_gate_logits(const uint16_t* x, const uint16_t* gate, int T, int H, int E,
+                               float* logits, oes_stream_t stream) {
+  OES_REQUIRE(x && gate && logits, "moe_gate_logits: null pointer");
+  OES_REQUIRE(T >= 1 && T <= 65535 && H >= 1 && E >= 1 && E <= OES_MAX_EXPERTS,
+              "moe_gate_logits: bad sizes T=%d H=%d E=%d", T, H, E);
+  const int threads = E < 256 ? ((E + 31) / 32) * 32 : 256;
+  dim3 grid(ceil_div(E, threads), T);
+  gate_logits_kernel<<<grid, threads, 0, stream>>>(x, gate, T, H, E, logits);
+  OES_CHECK_LAUNCH("gate_logits_kernel");
+  return OES_OK;
+}
+
+extern "C" int moe_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* weights,
+                              oes_stream_t stream) {
+  OES_REQUIRE(logits && ids && weights, "moe_route_topk: null pointer");
+  OES_REQUIRE(T >= 0 && E >= 1 && E <= OES_MAX_EXPERTS, "moe_route_topk: bad T=%d E=%d", T, E);
+  OES_REQUIRE(k >= 1 && k <= E && k <= OES_MAX_TOPK, "moe_route_topk: bad k=%d (E=%d)", k, E);
+  if (T == 0) return OES_OK;
+  const int threads = 128;
+  const int blocks = (int)std::min<int64_t>(ceil_div64((int64_t)T * 32, threads), (int64_t)num_sms() * 16);
+  const int epl = ceil_div(E, 32);
+#define OES_TOPK(N) topk_kernel<N><<<blocks, threads, 0, stream>>>(logits, T, E, k, ids, weights)
+  if (epl <= 1) OES_TOPK(1);
+  else if (epl <= 2) OES_TOPK(2);
+  else if (epl <= 4) OES_TOPK(4);
+  else if (epl <= 8) OES_TOPK(8);
+  else if (epl <= 16) OES_TOPK(16);
+  else if (epl <= 32) OES_TOPK(32);
+  else if (epl <= 64) OES_TOPK(64);
+  else OES_TOPK(128);
+#undef OES_TOPK
+  OES_CHECK_LAUNCH("topk_kernel");
+  return OES_OK;
+}
+
+extern "C" int moe_distinct_experts(const int32_t* ids, int R, int E, int32_t* distinct,
+                                    int32_t* d_count, oes_stream_t stream) {
+  OES_REQUIRE(d_count && (R == 0 || (ids && distinct)), "moe_distinct_experts: null pointer");
+  OES_REQUIRE(R >= 0 && E >= 1 && E <= OES_MAX_EXPERTS, "moe_distinct_experts: bad R=%d E=%d", R, E);
+  distinct_kernel<<<1, 1024, E, stream>>>(ids, R, E, distinct, d_count);
+  OES_CHECK_LAUNCH("distinct_kernel");
+  return OES_OK;
+}

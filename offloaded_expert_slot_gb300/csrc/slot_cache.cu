@@ -1,0 +1,433 @@
+// The LRU slot cache (tables in GPU memory, updated without a host sync),
+// the pinned-host expert source, and the miss-row copies.
+//
+// FreeToken PR #676, Solution: lru_ensure is handed the chunk's distinct
+// experts 128 at a time and each query's misses are copied before the next
+// query evicts; the admissions stay out of collect_decode_freq and the LRU
+// statistics.  The author's reply on that page: the cache is LRU only.
+// vLLM fork PR #48, What: one bank shared by all MoE layers, keyed by
+// (layer, expert); row copies are fixed-grid kernels reading the host
+// source through its accelerator view.
+#include <algorithm>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace oes {
+namespace {
+
+struct CacheView {
+  int S, L, E;
+  int32_t* map;
+  int32_t* slot_key;
+  int64_t* slot_ts;
+  int64_t* ctr;
+  int64_t* decode_freq;
+};
+
+CacheView view_of(oes_slot_cache* c) {
+  return CacheView{c->S, c->L, c->E, c->map, c->slot_key, c->slot_ts, c->ctr, c->decode_freq};
+}
+
+constexpr int kEnsureThreads = 1024;
+
+// One ensure query in one CTA.  Victims: the non-hit slots ordered by the
+// 64-bit key (timestamp << 16 | slot) -- empty slots have timestamp 0 and so
+// come first, in slot order -- sorted with a shared-memory bitonic network.
+__global__ void __launch_bounds__(kEnsureThreads)
+    ensure_kernel(CacheView c, int layer, const int32_t* __restrict__ experts, int n,
+                  int record_stats, int spad, int32_t* __restrict__ miss,
+                  int32_t* __restrict__ n_miss, int32_t* __restrict__ status) {
+  extern __shared__ uint64_t skey[];  // [spad]
+  __shared__ int32_t qkey[OES_QUERY_MAX];
+  __shared__ int32_t qslot[OES_QUERY_MAX];
+  __shared__ int32_t qrank[OES_QUERY_MAX];
+  __shared__ int32_t wvalid[4], wmiss[4];
+  __shared__ uint32_t hitmask[OES_MAX_SLOTS / 32];
+  __shared__ int32_t s_bad, s_nvalid, s_nmiss, s_nhit, s_evict;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int LE = c.L * c.E;
+
+  if (tid == 0) {
+    s_bad = 0;
+    s_evict = 0;
+  }
+  for (int i = tid; i < (c.S + 31) / 32; i += blockDim.x) hitmask[i] = 0;
+  __syncthreads();
+
+  // 1. compact the valid ids of the query into keys
+  int key = -1;
+  bool valid = false;
+  if (tid < OES_QUERY_MAX) {
+    const int e = (tid < n) ? experts[tid] : -1;
+    if (e != -1) {
+      if (e < 0 || e >= c.E) {
+        s_bad = 1;
+      } else {
+        valid = true;
+        key = layer * c.E + e;
+      }
+    }
+    const unsigned b = __ballot_sync(0xffffffffu, valid);
+    if (lane == 0) wvalid[w] = __popc(b);
+  }
+  __syncthreads();
+  if (tid < OES_QUERY_MAX) {
+    const unsigned b = __ballot_sync(0xffffffffu, valid);
+    int off = 0;
+    for (int i = 0; i < w; ++i) off += wvalid[i];
+    if (valid) qkey[off + __popc(b & ((1u << lane) - 1u))] = key;
+  }
+  if (tid == 0) s_nvalid = wvalid[0] + wvalid[1] + wvalid[2] + wvalid[3];
+  __syncthreads();
+  const int nvalid = s_nvalid;
+  if (tid + 1 < nvalid && qkey[tid] >= qkey[tid + 1]) s_bad = 1;
+  __syncthreads();
+  if (s_bad || nvalid == 0) {
+    if (tid == 0) {
+      if (s_bad) set_status(status, OES_DEV_BAD_ID);
+      *n_miss = 0;
+    }
+    return;
+  }
+
+  // 2. look the keys up; rank the misses in key order; mark hit slots
+  bool is_miss = false;
+  if (tid < OES_QUERY_MAX) {
+    int slot = -1;
+    if (tid < nvalid) {
+      slot = c.map[qkey[tid]];
+      if (slot >= c.S) {  // a corrupt table entry: treat as a miss and report
+        set_status(status, OES_DEV_BAD_ID);
+        slot = -1;
+      }
+      qslot[tid] = slot;
+      if (slot >= 0) atomicOr(&hitmask[slot >> 5], 1u << (slot & 31));
+      is_miss = slot < 0;
+    }
+    const unsigned b = __ballot_sync(0xffffffffu, is_miss);
+    if (lane == 0) wmiss[w] = __popc(b);
+  }
+  __syncthreads();
+  if (tid < OES_QUERY_MAX) {
+    const unsigned b = __ballot_sync(0xffffffffu, is_miss);
+    int off = 0;
+    for (int i = 0; i < w; ++i) off += wmiss[i];
+    qrank[tid] = is_miss ? off + __popc(b & ((1u << lane) - 1u)) : -1;
+  }
+  if (tid == 0) {
+    s_nmiss = wmiss[0] + wmiss[1] + wmiss[2] + wmiss[3];
+    s_nhit = nvalid - s_nmiss;
+  }
+  __syncthreads();
+  const int nmiss = s_nmiss, nhit = s_nhit;
+  if (nmiss > c.S - nhit) {
+    if (tid == 0) {
+      set_status(status, OES_DEV_CAPACITY);
+      *n_miss = 0;
+    }
+    return;
+  }
+  const int64_t clock_new = c.ctr[0] + 1;
+
+  // 3. order the evictable slots: (timestamp, slot) ascending
+  if (nmiss > 0) {
+    for (int s = tid; s < spad; s += blockDim.x) {
+      uint64_t k = ~0ull;
+      if (s < c.S && !(hitmask[s >> 5] & (1u << (s & 31)))) {
+        const int64_t ts = c.slot_key[s] < 0 ? 0 : c.slot_ts[s];
+        k = (static_cast<uint64_t>(ts) << 16) | static_cast<uint64_t>(s);
+      }
+      skey[s] = k;
+    }
+    __syncthreads();
+    for (int kk = 2; kk <= spad; kk <<= 1) {
+      for (int j = kk >> 1; j > 0; j >>= 1) {
+        for (int i = tid; i < spad; i += blockDim.x) {
+          const int ixj = i ^ j;
+          if (ixj > i) {
+            const uint64_t a = skey[i], b = skey[ixj];
+            const bool up = (i & kk) == 0;
+            if ((a > b) == up) {
+              skey[i] = b;
+              skey[ixj] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+  }
+
+  // 4. fills, evictions and recency
+  if (tid < nvalid) {
+    const int k = qkey[tid];
+    const int r = qrank[tid];
+    if (r >= 0) {
+      const int v = static_cast<int>(skey[r] & 0xFFFFu);
+      const int old = c.slot_key[v];
+      if (old >= 0 && old < LE) {
+        c.map[old] = -1;
+        atomicAdd(&s_evict, 1);
+      }
+      c.map[k] = v;
+      c.slot_key[v] = k;
+      c.slot_ts[v] = clock_new;
+      miss[3 * r + 0] = k;
+      miss[3 * r + 1] = v;
+      miss[3 * r + 2] = old;
+    } else {
+      c.slot_ts[qslot[tid]] = clock_new;
+    }
+    if (record_stats) c.decode_freq[k] += 1;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    c.ctr[0] = clock_new;
+    if (record_stats) {
+      c.ctr[1] += nhit;
+      c.ctr[2] += nmiss;
+      c.ctr[3] += s_evict;
+    }
+    *n_miss = nmiss;
+  }
+}
+
+constexpr int kCopyThreads = 512;
+constexpr int kCopyUnroll = 4;
+
+// Fixed grid: work item = (miss i, 32 KB chunk of its row).  Each thread
+// moves 4 x 16 bytes per item: all four loads are issued before the stores.
+__global__ void __launch_bounds__(kCopyThreads)
+    copy_misses_kernel(const uint8_t* const* __restrict__ bases, int L, int E, int64_t row_bytes,
+                       uint8_t* __restrict__ pool, int S, const int32_t* __restrict__ miss,
+                       const int32_t* __restrict__ n_miss_p, int max_misses,
+                       int32_t* __restrict__ status) {
+  const int nm = min(*n_miss_p, max_misses);
+  const int64_t vecs = row_bytes >> 4;
+  const int64_t chunk = (int64_t)kCopyThreads * kCopyUnroll;
+  const int64_t per_row = (vecs + chunk - 1) / chunk;
+  const int64_t total = (int64_t)nm * per_row;
+  for (int64_t it = blockIdx.x; it < total; it += gridDim.x) {
+    const int i = static_cast<int>(it / per_row);
+    const int64_t c0 = (it % per_row) * chunk;
+    const int key = miss[3 * i], slot = miss[3 * i + 1];
+    if (key < 0 || key >= L * E || slot < 0 || slot >= S) {
+      if (threadIdx.x == 0 && c0 == 0) set_status(status, OES_DEV_BAD_ID);
+      continue;
+    }
+    const uint4* src =
+        reinterpret_cast<const uint4*>(bases[key / E] + (int64_t)(key % E) * row_bytes);
+    uint4* dst = reinterpret_cast<uint4*>(pool + (int64_t)slot * row_bytes);
+    uint4 buf[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t v = c0 + u * kCopyThreads + threadIdx.x;
+      if (v < vecs) buf[u] = __ldcs(src + v);
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t v = c0 + u * kCopyThreads + threadIdx.x;
+      if (v < vecs) dst[v] = buf[u];
+    }
+  }
+}
+
+}  // namespace
+}  // namespace oes
+
+using namespace oes;
+
+extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
+  OES_REQUIRE(out, "slot_cache_create: null out");
+  OES_REQUIRE(S >= 1 && S <= OES_MAX_SLOTS, "slot_cache_create: S=%d out of [1, %d]", S,
+              OES_MAX_SLOTS);
+  OES_REQUIRE(E >= 1 && E <= OES_MAX_EXPERTS && L >= 1 && (int64_t)L * E < (1ll << 31),
+              "slot_cache_create: bad L=%d E=%d", L, E);
+  auto* c = new oes_slot_cache();
+  c->S = S;
+  c->L = L;
+  c->E = E;
+  cudaGetDevice(&c->device);
+  const size_t LE = (size_t)L * E;
+  const size_t bytes = LE * 4 + (size_t)S * 4 + (size_t)S * 8 + 4 * 8 + LE * 8 + 64;
+  cudaError_t e = cudaMalloc(&c->block, bytes);
+  if (e != cudaSuccess) {
+    delete c;
+    return cuda_fail(e, "cudaMalloc(slot cache tables)");
+  }
+  uint8_t* p = static_cast<uint8_t*>(c->block);
+  c->slot_ts = reinterpret_cast<int64_t*>(p);
+  p += (size_t)S * 8;
+  c->ctr = reinterpret_cast<int64_t*>(p);
+  p += 4 * 8;
+  c->decode_freq = reinterpret_cast<int64_t*>(p);
+  p += LE * 8;
+  c->map = reinterpret_cast<int32_t*>(p);
+  p += LE * 4;
+  c->slot_key = reinterpret_cast<int32_t*>(p);
+  std::vector<int32_t> key(S, -1);
+  std::vector<int64_t> ts(S, 0);
+  int rc = slot_cache_load_state(c, key.data(), ts.data(), 0);
+  if (rc != OES_OK) {
+    cudaFree(c->block);
+    delete c;
+    return rc;
+  }
+  *out = c;
+  return OES_OK;
+}
+
+extern "C" int slot_cache_destroy(oes_slot_cache* c) {
+  if (!c) return OES_OK;
+  cudaError_t e = cudaFree(c->block);
+  delete c;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFree(slot cache tables)");
+  return OES_OK;
+}
+
+extern "C" int slot_cache_load_state(oes_slot_cache* c, const int32_t* slot_key,
+                                     const int64_t* slot_ts, int64_t clock) {
+  OES_REQUIRE(c && slot_key && slot_ts, "slot_cache_load_state: null pointer");
+  OES_REQUIRE(clock >= 0 && clock < (1ll << 47), "slot_cache_load_state: bad clock %lld",
+              (long long)clock);
+  const int S = c->S;
+  const int64_t LE = (int64_t)c->L * c->E;
+  std::vector<int32_t> map(LE, -1);
+  for (int s = 0; s < S; ++s) {
+    const int32_t k = slot_key[s];
+    OES_REQUIRE(k >= -1 && k < LE, "slot_cache_load_state: slot %d holds key %d out of range", s, k);
+    if (k >= 0) {
+      OES_REQUIRE(map[k] < 0, "slot_cache_load_state: key %d held by two slots", k);
+      OES_REQUIRE(slot_ts[s] >= 1 && slot_ts[s] <= clock,
+                  "slot_cache_load_state: slot %d timestamp %lld out of [1, clock]", s,
+                  (long long)slot_ts[s]);
+      map[k] = s;
+    }
+  }
+  std::vector<int64_t> ts(S);
+  for (int s = 0; s < S; ++s) ts[s] = slot_key[s] < 0 ? 0 : slot_ts[s];
+  int64_t ctr[4] = {clock, 0, 0, 0};
+  OES_TRY_CUDA(cudaMemcpy(c->map, map.data(), LE * 4, cudaMemcpyHostToDevice));
+  OES_TRY_CUDA(cudaMemcpy(c->slot_key, slot_key, (size_t)S * 4, cudaMemcpyHostToDevice));
+  OES_TRY_CUDA(cudaMemcpy(c->slot_ts, ts.data(), (size_t)S * 8, cudaMemcpyHostToDevice));
+  OES_TRY_CUDA(cudaMemcpy(c->ctr, ctr, sizeof(ctr), cudaMemcpyHostToDevice));
+  OES_TRY_CUDA(cudaMemset(c->decode_freq, 0, LE * 8));
+  return OES_OK;
+}
+
+extern "C" int slot_cache_read_state(const oes_slot_cache* c, int32_t* map, int32_t* slot_key,
+                                     int64_t* slot_ts, int64_t* clock, int64_t* counters,
+                                     int64_t* decode_freq, oes_stream_t stream) {
+  OES_REQUIRE(c, "slot_cache_read_state: null cache");
+  OES_TRY_CUDA(cudaStreamSynchronize(stream));
+  const size_t LE = (size_t)c->L * c->E;
+  if (map) OES_TRY_CUDA(cudaMemcpy(map, c->map, LE * 4, cudaMemcpyDeviceToHost));
+  if (slot_key)
+    OES_TRY_CUDA(cudaMemcpy(slot_key, c->slot_key, (size_t)c->S * 4, cudaMemcpyDeviceToHost));
+  if (slot_ts)
+    OES_TRY_CUDA(cudaMemcpy(slot_ts, c->slot_ts, (size_t)c->S * 8, cudaMemcpyDeviceToHost));
+  int64_t ctr[4];
+  OES_TRY_CUDA(cudaMemcpy(ctr, c->ctr, sizeof(ctr), cudaMemcpyDeviceToHost));
+  if (clock) *clock = ctr[0];
+  if (counters) {
+    counters[0] = ctr[1];
+    counters[1] = ctr[2];
+    counters[2] = ctr[3];
+  }
+  if (decode_freq)
+    OES_TRY_CUDA(cudaMemcpy(decode_freq, c->decode_freq, LE * 8, cudaMemcpyDeviceToHost));
+  return OES_OK;
+}
+
+extern "C" int slot_cache_layer_map(const oes_slot_cache* c, int layer, const int32_t** e2s) {
+  OES_REQUIRE(c && e2s, "slot_cache_layer_map: null pointer");
+  OES_REQUIRE(layer >= 0 && layer < c->L, "slot_cache_layer_map: layer %d out of [0, %d)", layer,
+              c->L);
+  *e2s = c->map + (size_t)layer * c->E;
+  return OES_OK;
+}
+
+extern "C" int slot_cache_ensure(oes_slot_cache* c, int layer, const int32_t* experts, int n,
+                                 int record_stats, int32_t* miss, int32_t* n_miss, int32_t* status,
+                                 oes_stream_t stream) {
+  OES_REQUIRE(c && miss && n_miss && (n == 0 || experts), "slot_cache_ensure: null pointer");
+  OES_REQUIRE(layer >= 0 && layer < c->L, "slot_cache_ensure: layer %d out of [0, %d)", layer, c->L);
+  OES_REQUIRE(n >= 0 && n <= OES_QUERY_MAX, "slot_cache_ensure: n=%d out of [0, %d]", n,
+              OES_QUERY_MAX);
+  int spad = 2;
+  while (spad < c->S) spad <<= 1;
+  const size_t smem = (size_t)spad * 8;
+  static size_t configured_smem = 0;
+  if (smem > 48 * 1024 && smem > configured_smem) {
+    OES_TRY_CUDA(cudaFuncSetAttribute(ensure_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem));
+    configured_smem = smem;
+  }
+  ensure_kernel<<<1, kEnsureThreads, smem, stream>>>(view_of(c), layer, experts, n, record_stats,
+                                                     spad, miss, n_miss, status);
+  OES_CHECK_LAUNCH("ensure_kernel");
+  return OES_OK;
+}
+
+extern "C" int oes_expert_source_create(const void* const* layer_base, int L, int E,
+                                        int64_t row_bytes, oes_expert_source** out) {
+  OES_REQUIRE(out && layer_base, "oes_expert_source_create: null pointer");
+  OES_REQUIRE(L >= 1 && E >= 1 && (int64_t)L * E < (1ll << 31), "oes_expert_source_create: bad L/E");
+  OES_REQUIRE(row_bytes > 0 && row_bytes % 16 == 0,
+              "oes_expert_source_create: row_bytes %lld is not a positive multiple of 16",
+              (long long)row_bytes);
+  for (int l = 0; l < L; ++l)
+    OES_REQUIRE(layer_base[l] && ((uintptr_t)layer_base[l] & 15) == 0,
+                "oes_expert_source_create: layer %d base is null or not 16-byte aligned", l);
+  auto* s = new oes_expert_source();
+  s->L = L;
+  s->E = E;
+  s->row_bytes = row_bytes;
+  s->host_bases.assign(layer_base, layer_base + L);
+  s->dev_bases = nullptr;
+  cudaError_t e = cudaMalloc(&s->dev_bases, sizeof(void*) * L);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(s->dev_bases, s->host_bases.data(), sizeof(void*) * L, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(s->dev_bases);
+    delete s;
+    return cuda_fail(e, "oes_expert_source_create");
+  }
+  *out = s;
+  return OES_OK;
+}
+
+extern "C" int oes_expert_source_destroy(oes_expert_source* s) {
+  if (!s) return OES_OK;
+  cudaError_t e = cudaFree(s->dev_bases);
+  delete s;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFree(source bases)");
+  return OES_OK;
+}
+
+extern "C" int slot_cache_copy_misses(const oes_expert_source* src, void* pool, int S,
+                                      const int32_t* miss, const int32_t* n_miss, int max_misses,
+                                      int32_t* status, oes_stream_t stream) {
+  OES_REQUIRE(src && pool && miss && n_miss, "slot_cache_copy_misses: null pointer");
+  OES_REQUIRE(S >= 1 && max_misses >= 0 && max_misses <= OES_QUERY_MAX,
+              "slot_cache_copy_misses: bad S=%d max_misses=%d", S, max_misses);
+  OES_REQUIRE(((uintptr_t)pool & 15) == 0, "slot_cache_copy_misses: pool not 16-byte aligned");
+  if (max_misses == 0) return OES_OK;
+  const int grid = num_sms() * 2;
+  copy_misses_kernel<<<grid, kCopyThreads, 0, stream>>>(
+      src->dev_bases, src->L, src->E, src->row_bytes, static_cast<uint8_t*>(pool), S, miss, n_miss,
+      max_misses, status);
+  OES_CHECK_LAUNCH("copy_misses_kernel");
+  return OES_OK;
+}
+
+extern "C" int oes_copy_layer(const oes_expert_source* src, int layer, void* dst,
+                              oes_stream_t stream) {
+  OES_REQUIRE(src && dst, "oes_copy_layer: null pointer");
+  OES_REQUIRE(layer >= 0 && layer < src->L, "oes_copy_layer: layer %d out of range", layer);
+  OES_TRY_CUDA(cudaMemcpyAsync(dst, src->host_bases[layer], (size_t)src->E * src->row_bytes,
+                               cudaMemcpyDefault, stream));
+  return OES_OK;
+}
