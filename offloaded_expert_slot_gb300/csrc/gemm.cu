@@ -12,7 +12,8 @@
 // kernel template runs both GEMMs:
 //   GEMM1 (MODE 1): per (block, 128 intermediate rows): gate and up tiles
 //     into two TMEM accumulators, epilogue h = silu(g) * u -> 16-bit h;
-//     the block's token rows are gathered from x by TMA (tile::gather4).
+//     the block's token rows are gathered from x with 16-byte cp.async
+//     copies into the 128-byte-swizzled layout the MMA reads.
 //   GEMM2 (MODE 2): per (block, 128 output rows): y = h @ w2^T -> bf16 y
 //     at each route's row.
 // Warp roles: 0 weight producer (TMA), 1 MMA issuer (one thread), 2 TMEM
@@ -41,7 +42,7 @@ struct GemmMaps {
   CUtensorMap a;   // 16-bit weights [S][rows][K] (bf16 path)
   CUtensorMap q;   // NVFP4 values [S][rows][K/2] bytes
   CUtensorMap sc;  // NVFP4 scales [S][K/64][rows] u32
-  CUtensorMap b;   // GEMM1: x (or f16 x) [T][H]; GEMM2: h [cap][I]
+  CUtensorMap b;   // GEMM2: h [cap][I]
 };
 
 struct GemmParams {
@@ -56,6 +57,7 @@ struct GemmParams {
   int n_mtiles, n_kc, up_row0;  // up_row0: first up row of w13 (= I)
   int NS, NR;                   // pipeline depths
   uint32_t tmem_cols;
+  const uint16_t* xg;  // GEMM1: token rows to gather, [T, H] (bf16, or f16 for NVFP4)
   uint16_t* h;  // [cap, I]
   uint16_t* y;  // [R, H] bf16
   int32_t* status;
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(WF ? 384 : 256, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&maps.b);
+    if (MODE == 2) tma_prefetch_desc(&maps.b);
     if (WF) {
       tma_prefetch_desc(&maps.q);
       tma_prefetch_desc(&maps.sc);
@@ -281,7 +283,11 @@ __global__ void __launch_bounds__(WF ? 384 : 256, 1)
     }
   } else if (warp == 3) {
     // ------------------------------------------------- token / h producer
-    int s = 0, ph = 0;
+    // GEMM1: all 32 lanes gather the block's token rows with cp.async; a
+    // stage is signalled one stage later, once its copies have completed
+    // (wait_group) and been made visible to the tensor core (proxy fence).
+    // GEMM2: one TMA tile of h per stage.
+    int s = 0, ph = 0, pend = -1;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       const Unit t = unit_info(p, u, nb);
@@ -293,24 +299,39 @@ __global__ void __launch_bounds__(WF ? 384 : 256, 1)
           tok[n] = (n < t.nvalid) ? p.sorted_ids[(int64_t)t.b * p.BN + n] / p.k : 0;
         __syncwarp();
       }
-      if (lane == 0) {
-        for (int kc = 0; kc < p.n_kc; ++kc) {
-          ok = mbar_wait(&empty[s], ph ^ 1, p.status);
-          if (!ok) break;
-          uint8_t* B = stages + s * stage_bytes + a_bytes;
-          if (MODE == 1) {
-            mbar_arrive_expect_tx(&full[s], N * 128);
-            for (int g = 0; g < N; g += 4)
-              tma_gather4(B + g * 128, &maps.b, &full[s], kc * kChunkK, tok[g], tok[g + 1],
-                          tok[g + 2], tok[g + 3]);
-          } else {
-            mbar_arrive_expect_tx(&full[s], b_bytes);
-            tma_load_2d(B, &maps.b, &full[s], kc * kChunkK, t.b * p.BN);
+      for (int kc = 0; kc < p.n_kc; ++kc) {
+        if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, p.status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        uint8_t* B = stages + s * stage_bytes + a_bytes;
+        if (MODE == 1) {
+          const uint32_t b_s = smem_u32(B);
+          const uint8_t* xg = reinterpret_cast<const uint8_t*>(p.xg) + kc * (kChunkK * 2);
+          for (int i = lane; i < N * 8; i += 32) {
+            const int n = i >> 3, c = i & 7;
+            cp_async16(b_s + n * 128 + ((c ^ (n & 7)) << 4),
+                       xg + (int64_t)tok[n] * p.H * 2 + c * 16);
           }
-          if (++s == p.NS) { s = 0; ph ^= 1; }
+          cp_async_commit();
+          if (pend >= 0) {
+            cp_async_wait_1();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[pend]);
+          }
+          pend = s;
+        } else if (lane == 0) {
+          mbar_arrive_expect_tx(&full[s], b_bytes);
+          tma_load_2d(B, &maps.b, &full[s], kc * kChunkK, t.b * p.BN);
         }
+        if (++s == p.NS) { s = 0; ph ^= 1; }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    if (MODE == 1 && pend >= 0) {
+      cp_async_wait_0();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && ok) mbar_arrive(&full[pend]);
     }
   } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------- epilogue
@@ -628,12 +649,6 @@ extern "C" int moe_grouped_gemm_slots(const oes_routed_experts* v, const uint16_
   }
   const CUtensorMapDataType t16 = wf ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   {
-    const uint64_t dims[2] = {(uint64_t)H, (uint64_t)T};
-    const uint64_t str[1] = {(uint64_t)H * 2};
-    const uint32_t box[2] = {64, 1};
-    if ((rc = encode_tiled(&m1.b, t16, 2, xb, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))) return rc;
-  }
-  {
     const uint64_t dims[2] = {(uint64_t)I, (uint64_t)cap};
     const uint64_t str[1] = {(uint64_t)I * 2};
     const uint32_t box[2] = {64, (uint32_t)B};
@@ -687,6 +702,7 @@ extern "C" int moe_grouped_gemm_slots(const oes_routed_experts* v, const uint16_
   p.E = E;
   p.S = S;
   p.up_row0 = I;
+  p.xg = xb;
   p.h = ws.h;
   p.y = ws.y;
   p.status = status;

@@ -1,0 +1,72 @@
+"""The C-ABI library builds, loads and exports every call include/oes.h
+declares; host-side argument checks work without a GPU (CPU only)."""
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+from offloaded_expert_slot_gb300 import build, oes
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return oes.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "oes.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while", "for")))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(oes._SIGS)
+
+
+def test_host_argument_checks(lib):
+    with pytest.raises(oes.OesError) as e:
+        oes.moe_route_topk(0, 4, 8, 2, 0, 0, stream=0)
+    assert e.value.code == oes.OES_ERR_INVALID_ARG
+    with pytest.raises(oes.OesError) as e:
+        oes.moe_route_topk(16, 4, 8, 9, 16, 16, stream=0)     # k > E
+    assert e.value.code == oes.OES_ERR_INVALID_ARG
+    with pytest.raises(oes.OesError) as e:
+        oes.slot_cache_create(0, 1, 8)
+    assert e.value.code == oes.OES_ERR_INVALID_ARG
+    with pytest.raises(oes.OesError) as e:
+        oes.slot_cache_create(oes.OES_MAX_SLOTS + 1, 1, 8)
+    assert e.value.code == oes.OES_ERR_INVALID_ARG
+    with pytest.raises(oes.OesError) as e:
+        oes.moe_align_block_size(16, 4, 0, 16, 1, 16, 16, 16, 0, 16, 1 << 20, stream=0)   # E = 0
+    assert e.value.code == oes.OES_ERR_INVALID_ARG
+    with pytest.raises(oes.OesError) as e:
+        oes.slot_cache_ensure(0, 0, 16, 4, 0, 16, 16, 16, stream=0)   # null cache
+    assert e.value.code == oes.OES_ERR_INVALID_ARG
+
+
+def test_tile_plan_uses_the_layers_expert_count(lib):
+    """FreeToken PR #676, Solution: the prefill picks its tiles from tokens
+    per expert of the layer, not of the slot pool.  At 4096 tokens x top-10
+    the layer's 512 experts give 80 routes per expert (block 128); sizing by
+    1650 slots would give 25 (block 32)."""
+    assert oes.oes_tile_plan(4096 * 10, 512) == 128
+    assert oes.oes_tile_plan(4096 * 10, 1650) == 32
+    assert oes.oes_tile_plan(32 * 10, 512) == 16
+    assert oes.oes_tile_plan(600 * 10, 512) == 16
+    assert oes.oes_tile_plan(16 * 2, 8) == 16
+    for R, E, want in [(16 * 512, 512, 16), (17 * 512, 512, 32), (33 * 512, 512, 64),
+                       (65 * 512, 512, 128), (0, 5, 16)]:
+        assert oes.oes_tile_plan(R, E) == want
+
+
+def test_align_capacity_macro_matches_the_oracle():
+    from oracle.align import align_capacity
+    for R, E, B in [(0, 5, 4), (1, 1, 1), (10, 3, 8), (40960, 512, 128), (65536, 2100, 64)]:
+        assert oes.align_capacity(R, E, B) == align_capacity(R, E, B)

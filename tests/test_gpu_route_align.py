@@ -1,0 +1,134 @@
+"""GPU parity: routing, distinct experts and moe_align_block_size against the
+oracle, bit-exact for ids, distinct lists and align outputs; router
+weights within 2e-6 relative (expf in fp32 against fp64)."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import bits16, cuda, f32, i32, lib, scratch, status
+from offloaded_expert_slot_gb300 import oes
+from offloaded_expert_slot_gb300.configs import C1, C2, C3, C4, C5, C5B
+from offloaded_expert_slot_gb300.inputs import router_inputs, uniform_routes
+from oracle.align import moe_align_block_size as oracle_align
+from oracle.distinct import distinct_experts
+from oracle.router import gate_logits, route_topk
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_route(logits: np.ndarray, k: int):
+    T, E = logits.shape
+    ids, w = i32(T * k), f32(T * k)
+    oes.moe_route_topk(cuda(logits), T, E, k, ids, w)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy().reshape(T, k), w.cpu().numpy().reshape(T, k)
+
+
+@pytest.mark.parametrize("cfg", [C2, C3, C4, C5], ids=lambda c: c.name)
+def test_topk_matches_oracle(cfg):
+    lib()
+    logits = router_inputs(cfg)["logits"]
+    ids, w = gpu_route(logits, cfg.k)
+    rows = np.arange(cfg.T) if cfg.T <= 600 else np.random.default_rng(0).choice(cfg.T, 600, False)
+    oids, ow = route_topk(logits[rows], cfg.k)
+    assert np.array_equal(ids[rows], oids)
+    np.testing.assert_allclose(w[rows], ow, rtol=2e-6, atol=1e-7)
+
+
+def test_topk_ties_and_wide_experts():
+    lib()
+    g = np.random.default_rng(11)
+    for E, k in [(8, 2), (64, 8), (512, 10), (2100, 32), (4096, 16)]:
+        logits = (g.integers(-4, 5, size=(33, E)) * 0.25).astype(np.float32)   # many ties
+        ids, w = gpu_route(logits, k)
+        oids, ow = route_topk(logits, k)
+        assert np.array_equal(ids, oids), E
+        np.testing.assert_allclose(w, ow, rtol=2e-6, atol=1e-7)
+
+
+def test_gate_logits_tiny_workload():
+    """The tiny workload's router: bf16 gate, fp32 sums; the top-2 decision
+    is compared where its margin exceeds the fp32 rounding of the sums."""
+    lib()
+    rin = router_inputs(C1)
+    logits = torch.zeros(C1.T * C1.E, dtype=torch.float32, device="cuda")
+    oes.moe_gate_logits(bits16(rin["x"]), bits16(rin["gate"]), C1.T, C1.H, C1.E, logits)
+    torch.cuda.synchronize()
+    got = logits.cpu().numpy().reshape(C1.T, C1.E)
+    want = gate_logits(rin["x"], rin["gate"])
+    np.testing.assert_allclose(got, want, rtol=1e-5, atol=1e-6)
+    srt = np.sort(want, axis=1)
+    assert (srt[:, -C1.k] - srt[:, -C1.k - 1]).min() > 1e-4
+    ids, _ = gpu_route(got, C1.k)
+    oids, _ = route_topk(want, C1.k)
+    assert np.array_equal(ids, oids)
+
+
+@pytest.mark.parametrize("R,E", [(0, 8), (1, 1), (32, 8), (320, 512), (2000, 512), (40960, 512),
+                                 (65536, 2100), (5000, 4096)])
+def test_distinct_matches_oracle(R, E):
+    lib()
+    g = np.random.default_rng(R + E)
+    ids = g.integers(-1, E, size=R).astype(np.int32)
+    n = min(R, E)
+    d, cnt = i32(n, 7), i32(1, 7)
+    oes.moe_distinct_experts(cuda(ids) if R else 0, R, E, d if n else 0, cnt)
+    torch.cuda.synchronize()
+    od, oD = distinct_experts(ids, E)
+    assert int(cnt.item()) == oD
+    assert np.array_equal(d.cpu().numpy()[:n], od)
+
+
+def gpu_align(ids: np.ndarray, E: int, B: int, ignore_invalid=True):
+    R = ids.size
+    cap = oes.align_capacity(R, E, B)
+    s, b, n, st = i32(cap, -7), i32(cap // B, -7), i32(1, -7), status()
+    wsb = oes.moe_align_workspace_size(R, E, B)
+    ws = scratch(wsb)
+    oes.moe_align_block_size(cuda(ids.astype(np.int32)) if R else 0, R, E, B, ignore_invalid,
+                             s if cap else 0, b if cap else 0, n, st, ws, ws.numel())
+    torch.cuda.synchronize()
+    return s.cpu().numpy()[:cap], b.cpu().numpy()[:cap // B], int(n.item()), int(st.item())
+
+
+def _routes_of(cfg):
+    ids, _ = route_topk(router_inputs(cfg)["logits"], cfg.k)    # the oracle's routing
+    return ids.reshape(-1)
+
+
+@pytest.mark.parametrize("cfg", [C2, C3, C4, C5], ids=lambda c: c.name)
+def test_align_workload_sizes(cfg):
+    lib()
+    ids = _routes_of(cfg)
+    B = oes.oes_tile_plan(ids.size, cfg.E)
+    s, b, n, st = gpu_align(ids, cfg.E, B)
+    os_, ob, on, _ = oracle_align(ids, cfg.E, B)
+    assert n == on and st == 0
+    assert np.array_equal(s, os_) and np.array_equal(b, ob)
+
+
+@pytest.mark.parametrize("E", list(C5B.Es) + [1024, 4096])
+def test_align_past_1024_experts(E):
+    """FreeToken PR #676, Tests: 8192 tokens x top-8 uniformly routed at 1023
+    and 2100 experts, block 64: every route lands once, in a block of its
+    expert -- here bit-exact against the oracle."""
+    lib()
+    ids = uniform_routes(C5B.T, C5B.k, E, C5B.seed)
+    s, b, n, st = gpu_align(ids, E, C5B.block)
+    os_, ob, on, _ = oracle_align(ids, E, C5B.block)
+    assert n == on and st == 0
+    assert np.array_equal(s, os_) and np.array_equal(b, ob)
+
+
+@pytest.mark.parametrize("R,E,B", [(0, 5, 4), (1, 1, 1), (7, 3, 1), (100, 7, 3), (999, 64, 16),
+                                   (3000, 1, 128), (4099, 4096, 16)])
+def test_align_edges_and_invalid_ids(R, E, B):
+    lib()
+    g = np.random.default_rng(R * 7 + E)
+    ids = g.integers(-2, E + 2, size=R)
+    for ignore in (True, False):
+        s, b, n, st = gpu_align(ids, E, B, ignore_invalid=ignore)
+        os_, ob, on, bad = oracle_align(ids, E, B, ignore_invalid=ignore)
+        assert n == on
+        assert np.array_equal(s, os_) and np.array_equal(b, ob)
+        assert (st == oes.OES_DEV_BAD_ID) == bad

@@ -1,0 +1,214 @@
+"""GPU parity: the LRU ensure and the miss-row copies against the oracle.
+
+Bit-exact: every miss list, n_miss, map, slot_key, slot_ts, clock, the
+counters and decode_freq, and the status word.  Copies: miss slots hold the
+source rows byte for byte, every other slot is untouched (vLLM fork PR #51,
+Tests: "resident rows untouched").
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from conftest import GOLDEN
+from gpu_util import Workload, cuda, i32, lib, status
+from offloaded_expert_slot_gb300 import oes
+from offloaded_expert_slot_gb300.configs import C2, C5, scaled
+from offloaded_expert_slot_gb300.inputs import pool_prefill, router_inputs
+from oracle.distinct import distinct_experts
+from oracle.router import route_topk
+from oracle.slot_cache import SlotCache
+
+pytestmark = pytest.mark.gpu
+
+
+class GpuCache:
+    def __init__(self, S, L, E):
+        lib()
+        self.S, self.L, self.E = S, L, E
+        self.h = oes.slot_cache_create(S, L, E)
+        self.miss = i32(3 * oes.OES_QUERY_MAX, -9)
+        self.n_miss = i32(1, -9)
+        self.status = status()
+
+    def load(self, slot_key, slot_ts, clock):
+        oes.slot_cache_load_state(self.h, slot_key, slot_ts, clock)
+
+    def ensure(self, layer, experts, record_stats=False):
+        n = len(experts)
+        dev = cuda(np.asarray(experts, dtype=np.int32)) if n else None
+        self.status.zero_()
+        oes.slot_cache_ensure(self.h, layer, dev if n else 0, n, record_stats, self.miss, self.n_miss,
+                              self.status)
+        torch.cuda.synchronize()
+        nm = int(self.n_miss.item())
+        m = self.miss.cpu().numpy()[: 3 * nm].reshape(nm, 3)
+        return int(self.status.item()), [tuple(int(v) for v in r) for r in m]
+
+    def state(self):
+        return oes.slot_cache_read_state(self.h, self.S, self.L, self.E)
+
+    def close(self):
+        oes.slot_cache_destroy(self.h)
+
+
+STATUS = {0: 0, 1: oes.OES_DEV_CAPACITY, 2: oes.OES_DEV_BAD_ID}
+
+
+def assert_same(g: GpuCache, o: SlotCache):
+    st = g.state()
+    assert np.array_equal(st["map"], o.map)
+    assert np.array_equal(st["slot_key"], o.slot_key)
+    assert np.array_equal(st["slot_ts"], o.slot_ts)
+    assert st["clock"] == o.clock
+    assert (st["hits"], st["misses"], st["evictions"]) == (o.hits, o.misses, o.evictions)
+    assert np.array_equal(st["decode_freq"], o.decode_freq)
+
+
+def test_hand_trace_on_gpu():
+    g = json.load(open(os.path.join(GOLDEN, "lru_hand_trace.json")))
+    ini = g["initial"]
+    c = GpuCache(g["S"], g["L"], g["E"])
+    c.load(ini["slot_key"], ini["slot_ts"], ini["clock"])
+    for st in g["steps"]:
+        s, m = c.ensure(0, st["query"])
+        assert s == STATUS[st["status"]]
+        assert [list(x) for x in m] == st["misses"]
+        now = c.state()
+        assert now["slot_key"].tolist() == st["slot_key"]
+        assert now["slot_ts"].tolist() == st["slot_ts"]
+        assert now["clock"] == st["clock"]
+    assert c.state()["map"].tolist() == g["final_map"]
+    c.close()
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_sequences_against_oracle(seed):
+    g = np.random.default_rng(500 + seed)
+    S = int(g.choice([1, 3, 8, 33, 257, 1100]))
+    L = int(g.integers(1, 4))
+    E = int(g.choice([4, 16, 200]))
+    c = GpuCache(S, L, E)
+    n = int(g.integers(0, min(S, L * E) + 1))
+    key = np.full(S, -1, np.int32)
+    ts = np.zeros(S, np.int64)
+    slots = g.permutation(S)[:n]
+    key[slots] = g.choice(L * E, size=n, replace=False)
+    ts[slots] = g.permutation(n) + 1
+    c.load(key, ts, n)
+    o = SlotCache.from_state(S, L, E, key, ts, n)
+    for step in range(25):
+        layer = int(g.integers(0, L))
+        w = int(g.integers(0, min(E, oes.OES_QUERY_MAX) + 1))
+        q = sorted(g.choice(E, size=w, replace=False).tolist())
+        if g.random() < 0.1 and len(q) > 1:
+            q = q[::-1]                                     # not ascending
+        if g.random() < 0.05:
+            q = q + [E + 3]                                 # out of range
+        q = q + [-1] * int(g.integers(0, 3))
+        q = q[: oes.OES_QUERY_MAX]
+        rs = bool(g.random() < 0.5)
+        s, m = c.ensure(layer, q, record_stats=rs)
+        os_, om = o.ensure([layer * E + e if e >= 0 and e < E else (-1 if e == -1 else 10 ** 9)
+                            for e in q], record_stats=rs)
+        assert s == STATUS[os_], (seed, step)
+        assert m == [tuple(x) for x in om]
+        assert_same(c, o)
+    c.close()
+
+
+def test_decode_width_queries_on_prefilled_pool():
+    """The decode-width workload: 1100 slots shared by 2 layers, 800
+    pre-filled; the chunk's distinct experts of layer 0 in queries of 128,
+    no statistics recorded (a demand admission)."""
+    cfg = C2
+    st = pool_prefill(cfg)
+    c = GpuCache(cfg.S, cfg.L, cfg.E)
+    c.load(st["slot_key"], st["slot_ts"], st["clock"])
+    o = SlotCache.from_state(cfg.S, cfg.L, cfg.E, st["slot_key"], st["slot_ts"], st["clock"])
+    ids, _ = route_topk(router_inputs(cfg)["logits"], cfg.k)
+    d, D = distinct_experts(ids, cfg.E)
+    assert d.size == 320 and 150 < D < 320
+    for q0 in range(0, d.size, 128):
+        q = d[q0:q0 + 128].tolist()
+        s, m = c.ensure(0, q)
+        os_, om = o.ensure([e if e < 0 else e for e in q])
+        assert s == 0 and m == [tuple(x) for x in om]
+        assert_same(c, o)
+    assert c.state()["hits"] == 0 and not c.state()["decode_freq"].any()
+    c.close()
+
+
+def test_wide_pool_many_queries_with_stats():
+    """1650 slots (the long-prefill pool), 48 layers, four layers admitted in
+    full (512 experts each, four queries per layer), with statistics."""
+    cfg = C5
+    c = GpuCache(cfg.S, cfg.L, cfg.E)
+    o = SlotCache(cfg.S, cfg.L, cfg.E)
+    g = np.random.default_rng(9)
+    for layer in (0, 1, 2, 3, 0, 7):
+        experts = sorted(g.choice(cfg.E, size=int(g.integers(300, 513)), replace=False).tolist())
+        for q0 in range(0, len(experts), 128):
+            q = experts[q0:q0 + 128]
+            s, m = c.ensure(layer, q, record_stats=True)
+            os_, om = o.ensure([layer * cfg.E + e for e in q], record_stats=True)
+            assert s == 0 and m == [tuple(x) for x in om]
+        assert_same(c, o)
+    c.close()
+
+
+def test_copy_misses_moves_exactly_the_miss_rows():
+    cfg = scaled(C2, E=40, H=128, I=64, S=50, L=3, prefill=30, wfmt="bf16")
+    w = Workload(cfg, gen_device="cpu")
+    c_ref = SlotCache.from_state(cfg.S, cfg.L, cfg.E, w.prefill["slot_key"], w.prefill["slot_ts"],
+                                 w.prefill["clock"])
+    opool = w.oracle_pool()
+    miss, n_miss, st = i32(3 * 128), i32(1), status()
+    for layer, experts in [(0, list(range(0, 40, 3))), (2, list(range(5, 25))), (1, [0, 39])]:
+        dev = cuda(np.array(experts, np.int32))
+        oes.slot_cache_ensure(w.cache, layer, dev, len(experts), 0, miss, n_miss, st)
+        oes.slot_cache_copy_misses(w.src, w.pool, cfg.S, miss, n_miss, len(experts), st)
+        _, om = c_ref.ensure([layer * cfg.E + e for e in experts])
+        for key, slot, _ in om:
+            opool[slot] = w.source_row(key // cfg.E, key % cfg.E)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    pool = w.pool.cpu().numpy()
+    for s in range(cfg.S):
+        assert np.array_equal(pool[s], opool[s]), s
+    w.close()
+
+
+def test_copy_misses_large_rows_and_offsets_past_2gib():
+    """Full-size bf16 rows (9 MiB) copied into slots whose byte offsets exceed
+    2^31 (vLLM fork PR #51: a 32-bit offset overflows past 8192 rows x 4 MiB).
+    Slots below the top six hold other layers' keys, so the six misses take
+    the six empty slots at the top of a 2.8 GB pool."""
+    L = 60
+    cfg = scaled(C2, E=6, S=300, L=1, prefill=0)
+    w = Workload(cfg, with_pool=False)
+    pool = torch.zeros((cfg.S, cfg.row_bytes), dtype=torch.uint8, device="cuda")
+    assert (cfg.S - 6) * cfg.row_bytes > 2 ** 31
+    cache = oes.slot_cache_create(cfg.S, L, cfg.E)
+    key = np.full(cfg.S, -1, np.int32)
+    ts = np.zeros(cfg.S, np.int64)
+    key[: cfg.S - 6] = np.arange(cfg.E, cfg.E + cfg.S - 6)      # keys of layers >= 1
+    ts[: cfg.S - 6] = np.arange(1, cfg.S - 5)
+    oes.slot_cache_load_state(cache, key, ts, cfg.S)
+    src = oes.oes_expert_source_create([w.src_bufs[0]] * L, cfg.E, cfg.row_bytes)
+    miss, n_miss, st = i32(3 * 128), i32(1), status()
+    oes.slot_cache_ensure(cache, 0, cuda(np.arange(6, dtype=np.int32)), 6, 0, miss, n_miss, st)
+    oes.slot_cache_copy_misses(src, pool, cfg.S, miss, n_miss, 6, st)
+    torch.cuda.synchronize()
+    m = miss.cpu().numpy()[:18].reshape(6, 3)
+    assert int(st.item()) == 0 and int(n_miss.item()) == 6
+    assert m[:, 1].tolist() == list(range(cfg.S - 6, cfg.S))
+    for key_, slot, old in m:
+        assert old == -1 and int(slot) * cfg.row_bytes >= 2 ** 31
+        assert torch.equal(pool[int(slot)].cpu(), w.src_bufs[0][int(key_)])
+    assert int(pool[: cfg.S - 6].count_nonzero().item()) == 0
+    oes.oes_expert_source_destroy(src)
+    oes.slot_cache_destroy(cache)
+    w.close()
