@@ -1,0 +1,510 @@
+"""Benchmark: routed tokens/s of one offloaded-MoE layer forward over the GPU
+slot cache, on one GB300 (or N independent replicas, one per GPU).
+
+A step is one pass of the whole slot path over one chunk: route -> distinct
+experts -> queries of 128 (ensure + miss copies from pinned host memory) ->
+align -> grouped SwiGLU GEMM -> combine.  Before each step the cache tables
+are restored on the device to the workload's seeded pre-fill (a 25 KB
+device-to-device copy inside the timed region), so every step admits the same
+misses and copies the same rows.  Workload: the decode-width step (32 tokens,
+top-10, 512 experts, hidden 2048, intermediate 768, bf16 experts, 1100-slot
+pool shared by 2 layers with 800 slots pre-filled).
+
+Output: one JSON line (rank 0).  `value` = tokens of all ranks / max step time
+over ranks; `e2e` = the same through the C ABI with the chunk's inputs copied
+from pinned host memory and the output read back inside every timed step;
+`roofline` = the step with the largest share of the step time, against its
+bound; `cpu_baseline` = the CPU oracle timed on the host cores on a bounded
+sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from offloaded_expert_slot_gb300.configs import CONFIGS  # noqa: E402
+
+DEFAULT_CONFIG = "c2_decode_width"
+METRIC = "routed tokens/s per MoE layer (1xGB300)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        d["source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["source"] = "fallback"
+    return d
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- oracle
+def oracle_sample(cfg, rin, source_row, prefill, n_tokens, seed):
+    """One bounded sample of the oracle's slot path: routing, distinct
+    experts, every LRU query and the align for the whole chunk; the expert
+    MLP and combine for n_tokens sampled tokens.  Returns seconds."""
+    from oracle.layer import forward_slots
+    from oracle.slot_cache import SlotCache
+    from offloaded_expert_slot_gb300.inputs import empty_slot_row
+    empty = empty_slot_row(cfg)
+    pool = {s: (source_row(int(k) // cfg.E, int(k) % cfg.E) if k >= 0 else empty)
+            for s, k in enumerate(prefill["slot_key"])}
+    cache = SlotCache.from_state(cfg.S, cfg.L, cfg.E, prefill["slot_key"], prefill["slot_ts"],
+                                 prefill["clock"])
+    toks = np.random.default_rng(seed).choice(cfg.T, n_tokens, replace=False)
+    block = 16 if cfg.T * cfg.k <= 16 * cfg.E else 128
+    t0 = time.perf_counter()
+    forward_slots(cfg, rin, source_row, cache, pool, block=block, tokens=toks)
+    return time.perf_counter() - t0
+
+
+def lazy_source(cfg, needed):
+    """Host rows of the (layer, expert) pairs in `needed`, generated on the CPU."""
+    from offloaded_expert_slot_gb300.inputs import expert_rows
+    rows = {}
+    by_layer = {}
+    for l, e in needed:
+        by_layer.setdefault(l, []).append(e)
+    for l, es in by_layer.items():
+        es = sorted(set(es))
+        r = expert_rows(cfg, l, es).numpy()
+        for i, e in enumerate(es):
+            rows[(l, e)] = r[i]
+    return lambda l, e: rows[(l, e)]
+
+
+def reference_arm(args, cfg):
+    """The CPU oracle as the reference implementation, on the host cores."""
+    from offloaded_expert_slot_gb300.inputs import pool_prefill, router_inputs
+    from oracle.distinct import distinct_experts
+    from oracle.router import route_topk
+    rin = router_inputs(cfg)
+    prefill = pool_prefill(cfg)
+    ids, _ = route_topk(rin["logits"], cfg.k)
+    n_tok = min(cfg.T, 8)
+    needed = {(cfg.layer, int(e)) for e in np.unique(ids)}
+    src = lazy_source(cfg, needed)
+    src_row = lambda l, e: src(l, e) if (l, e) in needed else np.zeros(cfg.row_bytes, np.uint8)
+    for i in range(args.warmup):
+        oracle_sample(cfg, rin, src_row, prefill, n_tok, i)
+    times = [oracle_sample(cfg, rin, src_row, prefill, n_tok, 100 + i) for i in range(args.steps)]
+    s = float(np.sum(times))
+    value = n_tok * args.steps / s
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"oracle slot path on the full chunk (routing, distinct, LRU queries, align) with "
+              f"the expert MLP and combine for {n_tok} of {cfg.T} tokens per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000 * s / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "T": cfg.T, "k": cfg.k, "E": cfg.E, "H": cfg.H,
+                       "I": cfg.I, "wfmt": cfg.wfmt, "slots": cfg.S, "layers_in_pool": cfg.L},
+            "cpu_baseline": {"kind": "oracle", "value": value, "unit": "tokens/s", "cores": cores,
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ----------------------------------------------------------------- GPU arm
+class Bench:
+    def __init__(self, cfg, rank):
+        import torch
+
+        from offloaded_expert_slot_gb300 import oes
+        from offloaded_expert_slot_gb300.inputs import (empty_slot_row, expert_layer_rows,
+                                                        n_source_buffers, pool_prefill,
+                                                        router_inputs, source_layer_index)
+        self.torch, self.oes, self.cfg = torch, oes, cfg
+        oes.load()
+        rb = cfg.row_bytes
+        self.rin = router_inputs(cfg)
+        self.src_bufs = []
+        for l in range(n_source_buffers(cfg)):
+            buf = torch.empty((cfg.E, rb), dtype=torch.uint8, pin_memory=True)
+            expert_layer_rows(cfg, l, device="cuda", out=buf)
+            self.src_bufs.append(buf)
+        self.source_index = lambda l: source_layer_index(cfg, l)
+        bases = [self.src_bufs[source_layer_index(cfg, l)] for l in range(cfg.L)]
+        self.src = oes.oes_expert_source_create(bases, cfg.E, rb)
+        self.pool = torch.empty((cfg.S, rb), dtype=torch.uint8, device="cuda")
+        self.cache = oes.slot_cache_create(cfg.S, cfg.L, cfg.E)
+        st = pool_prefill(cfg)
+        self.prefill = st
+        oes.slot_cache_load_state(self.cache, st["slot_key"], st["slot_ts"], st["clock"])
+        self.pool[:] = torch.from_numpy(empty_slot_row(cfg)).cuda()
+        for s in np.nonzero(st["slot_key"] >= 0)[0]:
+            k = int(st["slot_key"][s])
+            self.pool[int(s)].copy_(self.src_bufs[source_layer_index(cfg, k // cfg.E)][k % cfg.E])
+        self.snap = torch.empty(oes.slot_cache_state_bytes(self.cache), dtype=torch.uint8,
+                                device="cuda")
+        oes.slot_cache_snapshot(self.cache, self.snap)
+        self.x = torch.from_numpy(self.rin["x"].view(np.int16)).cuda()
+        self.logits = torch.from_numpy(self.rin["logits"]).cuda()
+        self.wfmt = oes.OES_WFMT_BF16 if cfg.wfmt == "bf16" else oes.OES_WFMT_NVFP4
+        self.desc = oes.layer_desc(cfg.E, cfg.H, cfg.I, self.wfmt)
+        self.wsb = oes.moe_layer_workspace_size(self.desc, cfg.T, cfg.k)
+        self.ws = torch.empty(self.wsb, dtype=torch.uint8, device="cuda")
+        self.out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device="cuda")
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.chunk = oes.chunk(self.x, cfg.T, cfg.k, self.out, self.status, self.ws, self.wsb,
+                               logits=self.logits)
+        torch.cuda.synchronize()
+
+    def step(self):
+        oes = self.oes
+        oes.slot_cache_restore(self.cache, self.snap)
+        oes.moe_layer_forward_slots(self.cache, self.src, self.pool, self.cfg.layer, self.desc,
+                                    self.chunk, 0)
+
+    def timed(self, fn, steps):
+        torch = self.torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    # -- end to end through the C ABI with host buffers
+    def e2e(self, steps, warmup):
+        torch, oes, cfg = self.torch, self.oes, self.cfg
+        xh = torch.from_numpy(self.rin["x"].view(np.int16)).pin_memory()
+        lh = torch.from_numpy(self.rin["logits"]).pin_memory()
+        oh = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
+
+        def one():
+            self.x.copy_(xh, non_blocking=True)
+            self.logits.copy_(lh, non_blocking=True)
+            self.step()
+            oh.copy_(self.out, non_blocking=True)
+
+        for _ in range(warmup):
+            one()
+        ms = self.timed(one, steps)
+        bi = xh.numel() * 2 + lh.numel() * 4
+        bo = oh.numel() * 2
+        return ms, bi, bo
+
+    # -- per-step breakdown: the same calls, one by one, with events between
+    def breakdown(self, steps):
+        torch, oes, cfg = self.torch, self.oes, self.cfg
+        T, k, E = cfg.T, cfg.k, cfg.E
+        R = T * k
+        B = oes.oes_tile_plan(R, E)
+        cap = oes.align_capacity(R, E, B)
+        ids = torch.empty(R, dtype=torch.int32, device="cuda")
+        w = torch.empty(R, dtype=torch.float32, device="cuda")
+        Lq = min(R, E)
+        dist = torch.empty(Lq, dtype=torch.int32, device="cuda")
+        dcnt = torch.empty(1, dtype=torch.int32, device="cuda")
+        miss = torch.empty(3 * 128, dtype=torch.int32, device="cuda")
+        nmiss = torch.empty(1, dtype=torch.int32, device="cuda")
+        nmiss_tot = torch.zeros(1, dtype=torch.int32, device="cuda")
+        srt = torch.empty(cap, dtype=torch.int32, device="cuda")
+        bexp = torch.empty(cap // B, dtype=torch.int32, device="cuda")
+        npp = torch.empty(1, dtype=torch.int32, device="cuda")
+        awsb = oes.moe_align_workspace_size(R, E, B)
+        aws = torch.empty(max(awsb, 256), dtype=torch.uint8, device="cuda")
+        e2s = oes.slot_cache_layer_map(self.cache, cfg.layer)
+        view = oes.routed_experts(cfg.layer, E, e2s, self.wfmt, self.pool, cfg.row_bytes, cfg.S,
+                                  cfg.H, cfg.I)
+        gwsb = oes.moe_grouped_gemm_workspace_size(view, T, k)
+        gws = torch.empty(gwsb, dtype=torch.uint8, device="cuda")
+        names = ["restore", "route", "distinct", "ensure", "copy", "align", "gemm"]
+        tot = {n: 0.0 for n in names}
+        Q = (Lq + 127) // 128
+        for it in range(steps + 1):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3 + 2 * Q + 3)]
+            i = 0
+            ev[i].record(); i += 1
+            oes.slot_cache_restore(self.cache, self.snap)
+            ev[i].record(); i += 1
+            oes.moe_route_topk(self.logits, T, E, k, ids, w)
+            ev[i].record(); i += 1
+            oes.moe_distinct_experts(ids, R, E, dist, dcnt)
+            marks = []
+            for q in range(Q):
+                n = min(128, Lq - q * 128)
+                ev[i].record(); i += 1
+                oes.slot_cache_ensure(self.cache, cfg.layer, dist.data_ptr() + 4 * q * 128, n, 0,
+                                      miss, nmiss, self.status)
+                if it == 0:
+                    nmiss_tot.add_(nmiss)
+                ev[i].record(); i += 1
+                oes.slot_cache_copy_misses(self.src, self.pool, cfg.S, miss, nmiss, n, self.status)
+                marks.append(i)
+            ev[i].record(); i += 1
+            oes.moe_align_block_size(ids, R, E, B, 1, srt, bexp, npp, self.status, aws, awsb)
+            ev[i].record(); i += 1
+            oes.moe_grouped_gemm_slots(view, self.x, T, k, ids, w, srt, bexp, npp, B, gws, gwsb,
+                                       self.out, self.status)
+            ev[i].record(); i += 1
+            torch.cuda.synchronize()
+            if it == 0:
+                continue     # warm-up pass (also counts the misses)
+            el = [ev[j].elapsed_time(ev[j + 1]) for j in range(i - 1)]
+            tot["restore"] += el[0]
+            tot["route"] += el[1]
+            tot["distinct"] += el[2]
+            for q in range(Q):
+                tot["ensure"] += el[3 + 2 * q]
+                tot["copy"] += el[4 + 2 * q]
+            tot["align"] += el[3 + 2 * Q]
+            tot["gemm"] += el[4 + 2 * Q]
+        ms = {n: v / steps for n, v in tot.items()}
+        n_miss = int(nmiss_tot.item())
+        n_blocks = int(npp.item()) // B
+        D = int(dcnt.item())
+        return ms, {"misses": n_miss, "distinct": D, "blocks": n_blocks, "queries": Q, "block": B,
+                    "status": int(self.status.item())}
+
+    def link_probe(self):
+        torch = self.torch
+        n = 1 << 30
+        h = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        d = torch.empty(n, dtype=torch.uint8, device="cuda")
+        for _ in range(2):
+            d.copy_(h, non_blocking=True)
+        ms = self.timed(lambda: d.copy_(h, non_blocking=True), 4)
+        del h, d
+        return n / (ms / 1e3) / 1e9
+
+    def close(self):
+        self.oes.slot_cache_destroy(self.cache)
+        self.oes.oes_expert_source_destroy(self.src)
+
+
+def gpu_launches(cfg, with_restore=True):
+    """Kernels of liboes launched per step of the slot path."""
+    R = cfg.T * cfg.k
+    Q = (min(R, cfg.E) + 127) // 128
+    n = 1 + 1 + 2 * Q + 3 + 3          # topk, distinct, Q x (ensure, copy), align x3, gemm1/2 + combine
+    if cfg.logits == "gate":
+        n += 1
+    if cfg.wfmt == "nvfp4":
+        n += 1                          # x -> f16
+    return n
+
+
+def gpu_arm(args, cfg):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    from offloaded_expert_slot_gb300 import build
+    if rank == 0:
+        build.build()
+    if dist:
+        dist.barrier()
+    b = Bench(cfg, rank)
+    for _ in range(args.warmup):
+        b.step()
+    torch.cuda.synchronize()
+    st = int(b.status.item())
+    if st:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    ms = b.timed(b.step, args.steps)
+    clocks = sampler.stop()
+    barrier()
+    ms_max = ms
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    value = cfg.T * world / (ms_max / 1e3)
+
+    e2e_ms, bi, bo = b.e2e(args.steps, args.warmup)
+    if dist:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = cfg.T * world / (e2e_ms / 1e3)
+
+    bd, info = b.breakdown(max(3, args.steps // 2))
+    link = b.link_probe()
+    pk = peaks()
+    hbm = float(pk["hbm_gbs"])
+    bf16 = float(pk["bf16_tflops"])
+    R = cfg.T * cfg.k
+    H, I, E = cfg.H, cfg.I, cfg.E
+    step_bytes = {
+        "route": cfg.T * E * 4 + R * 8,
+        "distinct": R * 4 + min(R, E) * 4,
+        "align": R * 4 * 2 + info["blocks"] * info["block"] * 4 + info["blocks"] * 4,
+        "copy": info["misses"] * cfg.row_bytes,
+        "gemm": info["distinct"] * cfg.row_bytes + cfg.T * H * 2 * 2,
+    }
+    flops = R * 6 * H * I
+    kernels = {}
+    for n, b_ in step_bytes.items():
+        t_ms = bd[n]
+        gbs = b_ / (t_ms / 1e3) / 1e9 if t_ms > 0 else None
+        bound_peak = link if n == "copy" else hbm
+        kernels[n] = {"ms": round(t_ms, 5), "bytes": b_, "GB/s": gbs,
+                      "bound": "host_link" if n == "copy" else "hbm",
+                      "frac": (gbs / bound_peak) if gbs else None}
+    kernels["gemm"]["TFLOP/s"] = flops / (bd["gemm"] / 1e3) / 1e12
+    kernels["gemm"]["tensor_frac"] = kernels["gemm"]["TFLOP/s"] / bf16
+    kernels["ensure"] = {"ms": round(bd["ensure"], 5), "queries": info["queries"],
+                         "us_per_query": 1e3 * bd["ensure"] / info["queries"], "bound": "latency"}
+    kernels["restore"] = {"ms": round(bd["restore"], 5)}
+    dom = max(("route", "distinct", "ensure", "copy", "align", "gemm"), key=lambda n: bd[n])
+    # the GEMM is the dominant HBM/tensor kernel of the path; the miss copies are
+    # bound by the host link, whose peak is probed in this run.
+    g = kernels["gemm"]
+    gemm_hbm = g["GB/s"]
+    roof_gemm = {"kernel": "grouped_gemm (gemm1 + gemm2 + combine)", "bound": "hbm",
+                 "achieved": gemm_hbm, "peak": hbm, "unit": "GB/s", "frac": gemm_hbm / hbm,
+                 "traffic": None, "peak_source": pk["source"],
+                 "algorithmic_bytes": step_bytes["gemm"], "launch_ms": bd["gemm"]}
+    if dom == "copy":
+        c = kernels["copy"]
+        roofline = {"kernel": "copy_misses_kernel", "bound": "host_link", "achieved": c["GB/s"],
+                    "peak": link, "unit": "GB/s", "frac": c["frac"], "traffic": None,
+                    "peak_source": "measured in this run: 1 GiB pinned host->device cudaMemcpyAsync",
+                    "algorithmic_bytes": step_bytes["copy"], "launch_ms": bd["copy"]}
+    else:
+        roofline = roof_gemm
+    if rank == 0:
+        cpu = cpu_baseline(cfg, b)
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if cfg.wfmt == "bf16" else "nvfp4-w/f16", "data": "synthetic",
+                "config": {"workload": cfg.name, "T": cfg.T, "k": cfg.k, "E": E, "H": H, "I": I,
+                           "wfmt": cfg.wfmt, "slots": cfg.S, "layers_in_pool": cfg.L,
+                           "prefilled": cfg.prefill, "queries": info["queries"],
+                           "misses_per_step": info["misses"], "distinct": info["distinct"],
+                           "block": info["block"], "parallelism": f"replicas x{world}",
+                           "l2": "inputs larger than L2 (expert rows read per step "
+                                 f"{(info['distinct'] * cfg.row_bytes) / 1e9:.2f} GB)"},
+                "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": bi,
+                        "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms},
+                "gpu_launches": gpu_launches(cfg) * args.steps,
+                "clocks": clocks, "roofline": roofline, "roofline_gemm": roof_gemm,
+                "steps_breakdown": kernels, "host_link_gbs": link, "cpu_baseline": cpu}
+        print(json.dumps(line))
+    b.close()
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def cpu_baseline(cfg, b):
+    """The oracle on the host cores over bounded samples (about 10 s)."""
+    srcs = [x.numpy() for x in b.src_bufs]
+    row = lambda l, e: srcs[b.source_index(l)][e]
+    n_tok = min(cfg.T, 8)
+    total, tokens, i = 0.0, 0, 0
+    while total < 10.0 and i < 20:
+        total += oracle_sample(cfg, b.rin, row, b.prefill, n_tok, 1000 + i)
+        tokens += n_tok
+        i += 1
+    return {"kind": "oracle", "value": tokens / total, "unit": "tokens/s",
+            "cores": len(os.sched_getaffinity(0)),
+            "sample": f"{i} samples of the oracle slot path (full routing, LRU queries and align; "
+                      f"expert MLP and combine for {n_tok} of {cfg.T} tokens each), {total:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="oes", choices=["oes", "reference"])
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(CONFIGS))
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    cfg = CONFIGS[args.config]
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        reference_arm(args, cfg)
+        return
+    gpu_arm(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

@@ -134,6 +134,15 @@ int slot_cache_read_state(const oes_slot_cache *cache, int32_t *map, int32_t *sl
                           int64_t *slot_ts, int64_t *clock, int64_t *counters,
                           int64_t *decode_freq, oes_stream_t stream);
 
+/* Bytes of the cache's device tables, and asynchronous device-to-device
+ * copies of them: snapshot saves every table (map, slots, timestamps,
+ * clock, counters, decode_freq) into dst, restore puts such a snapshot
+ * back.  dst / src: device buffers of slot_cache_state_bytes() bytes.  Used
+ * to replay a query sequence from a known state without a host sync. */
+size_t slot_cache_state_bytes(const oes_slot_cache *cache);
+int slot_cache_snapshot(const oes_slot_cache *cache, void *dst, oes_stream_t stream);
+int slot_cache_restore(oes_slot_cache *cache, const void *src, oes_stream_t stream);
+
 /* Device pointer to the layer's expert->slot remap: map + layer * E, [E]
  * int32, the slot of each of the layer's experts or -1 (vLLM fork PR #48,
  * What: "physical-row remap").  Valid until slot_cache_destroy. */

@@ -10,6 +10,7 @@
 struct oes_slot_cache {
   int S, L, E, device;
   void* block;           // one allocation for every table
+  size_t block_bytes;
   int32_t* map;          // [L*E] slot of each key, -1 if absent
   int32_t* slot_key;     // [S] key held by each slot, -1 if empty
   int64_t* slot_ts;      // [S] timestamp of the last query that touched the slot, 0 if empty

@@ -252,6 +252,7 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   cudaGetDevice(&c->device);
   const size_t LE = (size_t)L * E;
   const size_t bytes = LE * 4 + (size_t)S * 4 + (size_t)S * 8 + 4 * 8 + LE * 8 + 64;
+  c->block_bytes = bytes;
   cudaError_t e = cudaMalloc(&c->block, bytes);
   if (e != cudaSuccess) {
     delete c;
@@ -338,6 +339,20 @@ extern "C" int slot_cache_read_state(const oes_slot_cache* c, int32_t* map, int3
   }
   if (decode_freq)
     OES_TRY_CUDA(cudaMemcpy(decode_freq, c->decode_freq, LE * 8, cudaMemcpyDeviceToHost));
+  return OES_OK;
+}
+
+extern "C" size_t slot_cache_state_bytes(const oes_slot_cache* c) { return c ? c->block_bytes : 0; }
+
+extern "C" int slot_cache_snapshot(const oes_slot_cache* c, void* dst, oes_stream_t stream) {
+  OES_REQUIRE(c && dst, "slot_cache_snapshot: null pointer");
+  OES_TRY_CUDA(cudaMemcpyAsync(dst, c->block, c->block_bytes, cudaMemcpyDeviceToDevice, stream));
+  return OES_OK;
+}
+
+extern "C" int slot_cache_restore(oes_slot_cache* c, const void* src, oes_stream_t stream) {
+  OES_REQUIRE(c && src, "slot_cache_restore: null pointer");
+  OES_TRY_CUDA(cudaMemcpyAsync(c->block, src, c->block_bytes, cudaMemcpyDeviceToDevice, stream));
   return OES_OK;
 }
 

@@ -144,48 +144,63 @@ def quantize_nvfp4(w: torch.Tensor):
 
 
 # ---------------------------------------------------------------- expert source
-def _layer_generator(cfg: LayerConfig, layer: int, device) -> torch.Generator:
+def _expert_generator(cfg: LayerConfig, layer: int, e: int, device) -> torch.Generator:
     g = torch.Generator(device=device)
-    g.manual_seed(cfg.seed * 1_000_003 + 17 * layer + 1)
+    g.manual_seed(((cfg.seed * 1_000_003 + 17 * layer) * 65_537 + e) & ((1 << 62) - 1))
     return g
+
+
+def expert_rows(cfg: LayerConfig, layer: int, experts, device="cpu") -> torch.Tensor:
+    """Rows of the given experts of one layer in the host-source byte layout,
+    [len(experts), row_bytes] u8 on `device`.  Every expert has its own
+    seeded generator, so any subset can be regenerated on its own.
+
+    Weights ~ N(0, 0.02) drawn as fp32 and rounded to bf16; NVFP4 rows encode
+    those bf16 values (see module docstring).
+    """
+    E, H, I = cfg.E, cfg.H, cfg.I
+    rb = expert_row_bytes(cfg.wfmt, H, I)
+    experts = list(experts)
+    n = len(experts)
+    w13 = torch.empty((n, 2 * I, H), dtype=torch.bfloat16, device=device)
+    w2 = torch.empty((n, H, I), dtype=torch.bfloat16, device=device)
+    for i, e in enumerate(experts):
+        g = _expert_generator(cfg, layer, int(e), device)
+        w13[i] = (torch.randn((2 * I, H), generator=g, device=device) * WEIGHT_STD).to(torch.bfloat16)
+        w2[i] = (torch.randn((H, I), generator=g, device=device) * WEIGHT_STD).to(torch.bfloat16)
+    rows = torch.empty((n, rb), dtype=torch.uint8, device=device)
+    if cfg.wfmt == "bf16":
+        rows[:, : 2 * I * H * 2] = w13.reshape(n, -1).view(torch.uint8)
+        rows[:, 2 * I * H * 2:] = w2.reshape(n, -1).view(torch.uint8)
+    else:
+        scale_in = 0.0
+        if cfg.layer_input_scales:
+            scale_in = float(cfg.layer_input_scales[layer % len(cfg.layer_input_scales)])
+        o = nvfp4_offsets(H, I)
+        q13, s13, gs13 = quantize_nvfp4(w13.to(torch.float32))
+        q2, s2, gs2 = quantize_nvfp4(w2.to(torch.float32))
+        rows[:, o["w13q"]:o["w13s"]] = q13.reshape(n, -1)
+        rows[:, o["w13s"]:o["w2q"]] = s13.reshape(n, -1)
+        rows[:, o["w2q"]:o["w2s"]] = q2.reshape(n, -1)
+        rows[:, o["w2s"]:o["scalars"]] = s2.reshape(n, -1)
+        scal = torch.stack([gs13, gs2, torch.full_like(gs13, scale_in),
+                            torch.full_like(gs13, scale_in)], dim=1).contiguous()
+        rows[:, o["scalars"]:o["end"]] = scal.view(torch.uint8).reshape(n, 16)
+    return rows
 
 
 def expert_layer_rows(cfg: LayerConfig, layer: int, device="cpu", out: torch.Tensor | None = None,
                       chunk: int = 32) -> torch.Tensor:
-    """All E expert rows of one layer in the host-source byte layout: [E, row_bytes] u8.
-
-    Weights ~ N(0, 0.02) drawn as fp32 and rounded to bf16; NVFP4 rows encode
-    those bf16 values (see module docstring).  Generated on `device`; written
-    into `out` (any device, e.g. pinned host memory) when given.
-    """
-    E, H, I = cfg.E, cfg.H, cfg.I
-    rb = expert_row_bytes(cfg.wfmt, H, I)
+    """All E expert rows of one layer, [E, row_bytes] u8, generated on
+    `device` (in chunks) and written into `out` (any device, e.g. pinned host
+    memory) when given.  Row e equals expert_rows(cfg, layer, [e]) made on
+    the same kind of device."""
+    rb = expert_row_bytes(cfg.wfmt, cfg.H, cfg.I)
     if out is None:
-        out = torch.empty((E, rb), dtype=torch.uint8)
-    g = _layer_generator(cfg, layer, device)
-    scale_in = 0.0
-    if cfg.wfmt == "nvfp4" and cfg.layer_input_scales:
-        scale_in = float(cfg.layer_input_scales[layer % len(cfg.layer_input_scales)])
-    for e0 in range(0, E, chunk):
-        n = min(chunk, E - e0)
-        w13 = (torch.randn((n, 2 * I, H), generator=g, device=device) * WEIGHT_STD).to(torch.bfloat16)
-        w2 = (torch.randn((n, H, I), generator=g, device=device) * WEIGHT_STD).to(torch.bfloat16)
-        rows = torch.empty((n, rb), dtype=torch.uint8, device=device)
-        if cfg.wfmt == "bf16":
-            rows[:, : 2 * I * H * 2] = w13.reshape(n, -1).view(torch.uint8)
-            rows[:, 2 * I * H * 2:] = w2.reshape(n, -1).view(torch.uint8)
-        else:
-            o = nvfp4_offsets(H, I)
-            q13, s13, gs13 = quantize_nvfp4(w13.to(torch.float32))
-            q2, s2, gs2 = quantize_nvfp4(w2.to(torch.float32))
-            rows[:, o["w13q"]:o["w13s"]] = q13.reshape(n, -1)
-            rows[:, o["w13s"]:o["w2q"]] = s13.reshape(n, -1)
-            rows[:, o["w2q"]:o["w2s"]] = q2.reshape(n, -1)
-            rows[:, o["w2s"]:o["scalars"]] = s2.reshape(n, -1)
-            scal = torch.stack([gs13, gs2, torch.full_like(gs13, scale_in),
-                                torch.full_like(gs13, scale_in)], dim=1).contiguous()
-            rows[:, o["scalars"]:o["end"]] = scal.view(torch.uint8).reshape(n, 16)
-        out[e0:e0 + n].copy_(rows, non_blocking=False)
+        out = torch.empty((cfg.E, rb), dtype=torch.uint8)
+    for e0 in range(0, cfg.E, chunk):
+        e1 = min(cfg.E, e0 + chunk)
+        out[e0:e1].copy_(expert_rows(cfg, layer, range(e0, e1), device=device))
     return out
 
 

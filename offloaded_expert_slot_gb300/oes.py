@@ -73,6 +73,9 @@ _SIGS = {
     "slot_cache_load_state": (_i, [_vp, _vp, _vp, _i64]),
     "slot_cache_read_state": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "slot_cache_layer_map": (_i, [_vp, _i, C.POINTER(_vp)]),
+    "slot_cache_state_bytes": (_sz, [_vp]),
+    "slot_cache_snapshot": (_i, [_vp, _vp, _vp]),
+    "slot_cache_restore": (_i, [_vp, _vp, _vp]),
     "slot_cache_ensure": (_i, [_vp, _i, _vp, _i, _i, _vp, _vp, _vp, _vp]),
     "oes_expert_source_create": (_i, [_vp, _i, _i, _i64, C.POINTER(_vp)]),
     "oes_expert_source_destroy": (_i, [_vp]),
@@ -188,6 +191,18 @@ def slot_cache_read_state(cache, S, L, E, stream=None) -> dict:
           clock.ctypes.data, ctr.ctypes.data, df.ctypes.data, _stream(stream))
     return {"map": m, "slot_key": sk, "slot_ts": st, "clock": int(clock[0]),
             "hits": int(ctr[0]), "misses": int(ctr[1]), "evictions": int(ctr[2]), "decode_freq": df}
+
+
+def slot_cache_state_bytes(cache) -> int:
+    return int(load().slot_cache_state_bytes(cache))
+
+
+def slot_cache_snapshot(cache, dst, stream=None):
+    _call("slot_cache_snapshot", cache, _ptr(dst), _stream(stream))
+
+
+def slot_cache_restore(cache, src, stream=None):
+    _call("slot_cache_restore", cache, _ptr(src), _stream(stream))
 
 
 def slot_cache_layer_map(cache, layer) -> int:
