@@ -383,8 +383,14 @@ def gpu_arm(args, cfg):
         raise RuntimeError(f"device status {st} after warm-up")
 
     barrier()
+    # clocks: sampled from just before the timed region (GPU already under
+    # load from these extra untimed steps) to its end
     sampler = ClockSampler(local)
     sampler.start()
+    t_end = time.perf_counter() + 0.5
+    while time.perf_counter() < t_end:
+        b.step()
+        torch.cuda.synchronize()
     ms = b.timed(b.step, args.steps)
     clocks = sampler.stop()
     barrier()
@@ -478,7 +484,7 @@ def cpu_baseline(cfg, b):
     row = lambda l, e: srcs[b.source_index(l)][e]
     n_tok = min(cfg.T, 8)
     total, tokens, i = 0.0, 0, 0
-    while total < 10.0 and i < 20:
+    while total < 10.0 and i < 200:
         total += oracle_sample(cfg, b.rin, row, b.prefill, n_tok, 1000 + i)
         tokens += n_tok
         i += 1
