@@ -217,6 +217,30 @@ int moe_align_block_size(const int32_t *ids, int R, int E, int B, int ignore_inv
                          int32_t *status, void *workspace, size_t workspace_bytes,
                          oes_stream_t stream);
 
+/* moe_align_block_size without a workspace argument: the same result, with
+ * its scratch in a fixed buffer inside the library.  The pages have no
+ * counterpart; this is for callers that cannot call cudaMalloc on this path,
+ * such as an engine that has handed all free GPU memory to its own pool, or a
+ * caller that must not risk the device-wide synchronisation cudaMalloc and
+ * cudaFree can cause in the middle of its work.
+ * The buffer is OES_ALIGN_NOALLOC_SCRATCH_BYTES (1 MiB) of device memory on
+ * every GPU that loads the library, held until the process exits.  A call
+ * needing more scratch than that (moe_align_workspace_size(R, E, B)) returns
+ * OES_ERR_INVALID_ARG and launches nothing; e.g. 40960 routes over 512
+ * experts need 41 KB, 65536 routes over 2100 experts 269 KB.
+ * The first call on a device looks the buffer's device address up
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  The call allocates nothing.
+ * Every call on a device shares the one buffer, which keeps the last call's
+ * contents; each call writes all the scratch it reads, so nothing has to
+ * start at zero.  Calls whose kernels overlap on the GPU (other streams, or
+ * other threads) race on the buffer and must be ordered by the caller.
+ * Arguments, outputs and status as for moe_align_block_size. */
+#define OES_ALIGN_NOALLOC_SCRATCH_BYTES (1 << 20)
+int moe_align_block_size_noalloc(const int32_t *ids, int R, int E, int B, int ignore_invalid,
+                                 int32_t *sorted_ids, int32_t *block_expert, int32_t *n_post_pad,
+                                 int32_t *status, oes_stream_t stream);
+
 /* ------------------------------------------------------------ expert GEMM */
 
 /* The experts a chunk routes to, as the grouped GEMM sees them (FreeToken

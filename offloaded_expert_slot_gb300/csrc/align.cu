@@ -13,6 +13,7 @@
 //            of one expert keep ascending route order (bit-exact, stable);
 //            extra CTAs write the padding and block_expert.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -242,4 +243,56 @@ extern "C" int moe_align_block_size(const int32_t* ids, int R, int E, int B, int
       ids, R, E, B, C, G, cap, ws, sorted_ids, block_expert);
   OES_CHECK_LAUNCH("align_scatter_kernel");
   return OES_OK;
+}
+
+// ------------------------------------------------------ no-allocation variant
+// Scratch for moe_align_block_size_noalloc: one fixed buffer per GPU that
+// loads the library, held until the process exits.  Host code must not pass
+// the symbol itself to a kernel (on the host it names a stand-in, not device
+// memory); its device address is looked up once per device below.
+static __device__ __align__(256) uint8_t g_align_scratch[OES_ALIGN_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_align_scratch_mu;
+void* g_align_scratch_ptr[64] = {nullptr};
+
+// Device address of g_align_scratch on the current device (looked up with
+// that device current, on the first call for the device).
+int align_scratch_address(void** out) {
+  int dev = 0;
+  OES_TRY_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) {
+    oes::set_error("moe_align_block_size_noalloc: device ordinal %d out of range", dev);
+    return OES_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lock(g_align_scratch_mu);
+  if (!g_align_scratch_ptr[dev]) {
+    void* p = nullptr;
+    OES_TRY_CUDA(cudaGetSymbolAddress(&p, g_align_scratch));
+    g_align_scratch_ptr[dev] = p;
+  }
+  *out = g_align_scratch_ptr[dev];
+  return OES_OK;
+}
+}  // namespace
+
+extern "C" int moe_align_block_size_noalloc(const int32_t* ids, int R, int E, int B,
+                                            int ignore_invalid, int32_t* sorted_ids,
+                                            int32_t* block_expert, int32_t* n_post_pad,
+                                            int32_t* status, oes_stream_t stream) {
+  OES_REQUIRE(R >= 0 && R < (1 << 30) && E >= 1 && E <= OES_MAX_EXPERTS && B >= 1 && B <= 1024,
+              "moe_align_block_size_noalloc: bad R=%d E=%d B=%d", R, E, B);
+  const size_t need = moe_align_workspace_size(R, E, B);
+  if (need > (size_t)OES_ALIGN_NOALLOC_SCRATCH_BYTES) {
+    oes::set_error(
+        "moe_align_block_size_noalloc: R=%d routes over E=%d experts need %zu bytes of scratch, "
+        "more than its fixed %d-byte buffer; call moe_align_block_size with a workspace instead",
+        R, E, need, (int)OES_ALIGN_NOALLOC_SCRATCH_BYTES);
+    return OES_ERR_INVALID_ARG;
+  }
+  void* scratch = nullptr;
+  const int rc = align_scratch_address(&scratch);
+  if (rc) return rc;
+  return moe_align_block_size(ids, R, E, B, ignore_invalid, sorted_ids, block_expert, n_post_pad,
+                              status, scratch, (size_t)OES_ALIGN_NOALLOC_SCRATCH_BYTES, stream);
 }

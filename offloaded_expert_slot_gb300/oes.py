@@ -83,6 +83,7 @@ _SIGS = {
     "oes_copy_layer": (_i, [_vp, _i, _vp, _vp]),
     "moe_align_workspace_size": (_sz, [_i, _i, _i]),
     "moe_align_block_size": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_align_block_size_noalloc": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "oes_tile_plan": (_i, [_i, _i, C.POINTER(_i)]),
     "moe_grouped_gemm_workspace_size": (_sz, [C.POINTER(RoutedExperts), _i, _i]),
     "moe_grouped_gemm_slots": (_i, [C.POINTER(RoutedExperts), _vp, _i, _i, _vp, _vp, _vp, _vp, _vp,
@@ -246,6 +247,15 @@ def moe_align_block_size(ids, R, E, B, ignore_invalid, sorted_ids, block_expert,
     _call("moe_align_block_size", _ptr(ids), R, E, B, int(bool(ignore_invalid)), _ptr(sorted_ids),
           _ptr(block_expert), _ptr(n_post_pad), _ptr(status), _ptr(workspace), workspace_bytes,
           _stream(stream))
+
+
+OES_ALIGN_NOALLOC_SCRATCH_BYTES = 1 << 20
+
+
+def moe_align_block_size_noalloc(ids, R, E, B, ignore_invalid, sorted_ids, block_expert,
+                                 n_post_pad, status, stream=None):
+    _call("moe_align_block_size_noalloc", _ptr(ids), R, E, B, int(bool(ignore_invalid)),
+          _ptr(sorted_ids), _ptr(block_expert), _ptr(n_post_pad), _ptr(status), _stream(stream))
 
 
 # -------------------------------------------------------------------- GEMM
