@@ -341,6 +341,22 @@ class Bench:
         self.oes.oes_expert_source_destroy(self.src)
 
 
+def reduce_max(x: float, dist, device) -> float:
+    """Max of a per-rank number over all ranks (the slowest rank sets the
+    step time of the job); identity on a single process."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(tokens_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput: tokens of all ranks over the slowest rank's step."""
+    return tokens_per_rank * world / (ms_max / 1e3)
+
+
 def gpu_launches(cfg, with_restore=True):
     """Kernels of liboes launched per step of the slot path."""
     R = cfg.T * cfg.k
@@ -394,19 +410,12 @@ def gpu_arm(args, cfg):
     ms = b.timed(b.step, args.steps)
     clocks = sampler.stop()
     barrier()
-    ms_max = ms
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    value = cfg.T * world / (ms_max / 1e3)
+    ms_max = reduce_max(ms, dist, "cuda")
+    value = job_value(cfg.T, world, ms_max)
 
     e2e_ms, bi, bo = b.e2e(args.steps, args.warmup)
-    if dist:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = cfg.T * world / (e2e_ms / 1e3)
+    e2e_ms = reduce_max(e2e_ms, dist, "cuda")
+    e2e_value = job_value(cfg.T, world, e2e_ms)
 
     bd, info = b.breakdown(max(3, args.steps // 2))
     link = b.link_probe()

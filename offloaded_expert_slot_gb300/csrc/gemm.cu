@@ -17,7 +17,7 @@
 //   GEMM2 (MODE 2): per (block, 128 output rows): y = h @ w2^T -> bf16 y
 //     at each route's row.
 // Warp roles: 0 weight producer (TMA), 1 MMA issuer (one thread), 2 TMEM
-// allocator, 3 token/h producer (TMA), 4-7 epilogue, 8-11 NVFP4 converters
+// allocator, 3 token/h producer, 4-7 epilogue, 8-15 NVFP4 converters
 // (NVFP4 only: e2m1 x e4m3 decoded exactly into f16 tiles in shared memory;
 // the per-expert fp32 global scale is applied to the fp32 sums).
 // The weights of a slot are addressed through a 3-D tensor map over the
@@ -37,6 +37,7 @@ namespace {
 
 constexpr int kTileM = 128;  // weight rows per MMA
 constexpr int kChunkK = 64;  // K elements per pipeline stage (128 bytes of 16-bit)
+constexpr int kConvWarps = 8;  // NVFP4 converter warps
 
 struct GemmMaps {
   CUtensorMap a;   // 16-bit weights [S][rows][K] (bf16 path)
@@ -116,7 +117,7 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
 // product e2m1 * e4m3 has at most 6 significant bits and lies in
 // [2^-10, 2688], so it is exact in f16.
 __device__ __forceinline__ void convert_row(const uint8_t* q, uint32_t scales, uint8_t* tile,
-                                            int row) {
+                                            int row, int c_begin, int c_end) {
   const uint4 q0 = *reinterpret_cast<const uint4*>(q);
   const uint4 q1 = *reinterpret_cast<const uint4*>(q + 16);
   const uint32_t s01 = cvt_e4m3x2_f16x2(scales & 0xFFFFu);
@@ -128,6 +129,7 @@ __device__ __forceinline__ void convert_row(const uint8_t* q, uint32_t scales, u
   const int sw = row & 7;
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
+    if (c < c_begin || c >= c_end) continue;
     const uint32_t wd = words[c];
     const uint32_t s = sc[c >> 1];
     uint4 o;
@@ -142,7 +144,7 @@ __device__ __forceinline__ void convert_row(const uint8_t* q, uint32_t scales, u
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
 template <int MODE, int WF>
-__global__ void __launch_bounds__(WF ? 384 : 256, 1)
+__global__ void __launch_bounds__(WF ? 512 : 256, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   constexpr int kA = (MODE == 1) ? 2 : 1;  // weight tiles per stage (gate + up, or w2)
   extern __shared__ uint8_t smem_raw[];
@@ -169,12 +171,12 @@ __global__ void __launch_bounds__(WF ? 384 : 256, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
-      mbar_init(&full[s], WF ? 5 : 2);
+      mbar_init(&full[s], WF ? 1 + kConvWarps : 2);
       mbar_init(&empty[s], 1);
     }
     for (int r = 0; r < p.NR; ++r) {
       mbar_init(&rfull[r], 1);
-      mbar_init(&rempty[r], 4);
+      mbar_init(&rempty[r], kConvWarps);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -287,7 +289,10 @@ __global__ void __launch_bounds__(WF ? 384 : 256, 1)
     // stage is signalled one stage later, once its copies have completed
     // (wait_group) and been made visible to the tensor core (proxy fence).
     // GEMM2: one TMA tile of h per stage.
-    int s = 0, ph = 0, pend = -1;
+    // Up to `lag` = NS - 1 stages of copies are in flight before the oldest
+    // is waited for and signalled, so L2 latency overlaps the MMAs.
+    int s = 0, ph = 0, issued = 0, signalled = 0;
+    const int lag = p.NS - 1 < 7 ? p.NS - 1 : 7;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       const Unit t = unit_info(p, u, nb);
@@ -313,13 +318,14 @@ __global__ void __launch_bounds__(WF ? 384 : 256, 1)
                        xg + (int64_t)tok[n] * p.H * 2 + c * 16);
           }
           cp_async_commit();
-          if (pend >= 0) {
-            cp_async_wait_1();
+          ++issued;
+          if (issued - signalled > lag) {
+            cp_async_wait(lag);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&full[pend]);
+            if (lane == 0) mbar_arrive(&full[signalled % p.NS]);
+            ++signalled;
           }
-          pend = s;
         } else if (lane == 0) {
           mbar_arrive_expect_tx(&full[s], b_bytes);
           tma_load_2d(B, &maps.b, &full[s], kc * kChunkK, t.b * p.BN);
@@ -327,11 +333,12 @@ __global__ void __launch_bounds__(WF ? 384 : 256, 1)
         if (++s == p.NS) { s = 0; ph ^= 1; }
       }
     }
-    if (MODE == 1 && pend >= 0) {
-      cp_async_wait_0();
+    if (MODE == 1 && issued > signalled) {
+      cp_async_wait(0);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0 && ok) mbar_arrive(&full[pend]);
+      if (lane == 0 && ok)
+        for (; signalled < issued; ++signalled) mbar_arrive(&full[signalled % p.NS]);
     }
   } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------- epilogue
@@ -409,9 +416,14 @@ __global__ void __launch_bounds__(WF ? 384 : 256, 1)
     }
   } else if (WF && warp >= 8) {
     // --------------------------------------------------- NVFP4 converters
-    const int ct = threadIdx.x - 256;  // 0..127: one weight row of each tile
+    // 256 threads: GEMM1 (256 weight rows per stage) one row each; GEMM2
+    // (128 rows) half a row each.
+    const int ct = threadIdx.x - 256;
     int s = 0, ph = 0, r = 0, rph = 0;
     bool ok = true;
+    const int rr = (MODE == 1) ? ct : (ct & (kTileM - 1));
+    const int c_begin = (MODE == 1) ? 0 : (ct >> 7) * 4;
+    const int c_end = (MODE == 1) ? 8 : c_begin + 4;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       const Unit t = unit_info(p, u, nb);
       if (t.skip) continue;
@@ -421,11 +433,8 @@ __global__ void __launch_bounds__(WF ? 384 : 256, 1)
         const uint8_t* Q = raw + r * raw_stage;
         const uint32_t* SC = reinterpret_cast<const uint32_t*>(Q + rq_bytes);
         uint8_t* A = stages + s * stage_bytes;
-#pragma unroll
-        for (int h2 = 0; h2 < kA; ++h2) {
-          const int rr = h2 * kTileM + ct;
-          convert_row(Q + rr * 32, SC[rr], A + h2 * kTileM * 128, ct);
-        }
+        convert_row(Q + rr * 32, SC[rr], A + (rr / kTileM) * kTileM * 128, rr & (kTileM - 1),
+                    c_begin, c_end);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -571,7 +580,7 @@ int launch_gemm(const GemmMaps& maps, const GemmParams& p0, int BN, cudaStream_t
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024));
     configured = true;
   }
-  grouped_gemm_kernel<MODE, WF><<<num_sms(), WF ? 384 : 256, smem, stream>>>(maps, p);
+  grouped_gemm_kernel<MODE, WF><<<num_sms(), WF ? 512 : 256, smem, stream>>>(maps, p);
   OES_CHECK_LAUNCH("grouped_gemm_kernel");
   return OES_OK;
 }
