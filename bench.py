@@ -503,6 +503,55 @@ def cpu_baseline(cfg, b):
                       f"expert MLP and combine for {n_tok} of {cfg.T} tokens each), {total:.1f} s"}
 
 
+def sweep(args):
+    """Bandwidth sweep of the bookkeeping kernels at sizes where HBM time is
+    measurable (beyond the workloads, which are latency-bound): routing of
+    65,536 tokens over 512 experts (134 MB of logits) and align of 2^24
+    routes.  One JSON line per kernel; not the headline."""
+    import torch
+    from offloaded_expert_slot_gb300 import build, oes
+    build.build()
+    oes.load()
+    hbm = float(peaks()["hbm_gbs"])
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+
+    def timed(fn, steps=20):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    for T, E, k in [(65536, 512, 10), (262144, 512, 8)]:
+        logits = torch.randn((T, E), generator=g, device="cuda")
+        ids = torch.empty(T * k, dtype=torch.int32, device="cuda")
+        w = torch.empty(T * k, dtype=torch.float32, device="cuda")
+        ms = timed(lambda: oes.moe_route_topk(logits, T, E, k, ids, w))
+        b = T * E * 4 + T * k * 8
+        print(json.dumps({"sweep": "moe_route_topk", "T": T, "E": E, "k": k, "ms": ms,
+                          "bytes": b, "GB/s": b / ms / 1e6, "hbm_frac": b / ms / 1e6 / hbm}))
+        del logits
+    for R, E, B in [(1 << 24, 512, 64), (1 << 24, 2100, 64), (65536, 2100, 64), (40960, 512, 128)]:
+        ids = torch.randint(0, E, (R,), generator=g, device="cuda", dtype=torch.int32)
+        cap = oes.align_capacity(R, E, B)
+        srt = torch.empty(cap, dtype=torch.int32, device="cuda")
+        be = torch.empty(cap // B, dtype=torch.int32, device="cuda")
+        npp = torch.empty(1, dtype=torch.int32, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        wsb = oes.moe_align_workspace_size(R, E, B)
+        ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        ms = timed(lambda: oes.moe_align_block_size(ids, R, E, B, 1, srt, be, npp, st, ws, wsb))
+        b = R * 4 * 2 + cap * 4 + (cap // B) * 4
+        print(json.dumps({"sweep": "moe_align_block_size", "R": R, "E": E, "B": B, "ms": ms,
+                          "bytes": b, "GB/s": b / ms / 1e6, "hbm_frac": b / ms / 1e6 / hbm}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -510,7 +559,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="oes", choices=["oes", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(CONFIGS))
+    ap.add_argument("--sweep", action="store_true",
+                    help="bandwidth sweep of the routing and align kernels (not the headline)")
     args = ap.parse_args()
+    if args.sweep:
+        sweep(args)
+        return
     args.warmup = max(args.warmup, 3)
     cfg = CONFIGS[args.config]
     if args.impl == "reference":

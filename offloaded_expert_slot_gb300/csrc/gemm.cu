@@ -13,7 +13,9 @@
 //   GEMM1 (MODE 1): per (block, 128 intermediate rows): gate and up tiles
 //     into two TMEM accumulators, epilogue h = silu(g) * u -> 16-bit h;
 //     the block's token rows are gathered from x with 16-byte cp.async
-//     copies into the 128-byte-swizzled layout the MMA reads.
+//     copies into the 128-byte-swizzled layout the MMA reads; each lane's
+//     copies arrive on the stage's mbarrier when they complete, and the MMA
+//     thread orders them before its tensor-core reads with a proxy fence.
 //   GEMM2 (MODE 2): per (block, 128 output rows): y = h @ w2^T -> bf16 y
 //     at each route's row.
 // Warp roles: 0 weight producer (TMA), 1 MMA issuer (one thread), 2 TMEM
@@ -171,7 +173,9 @@ __global__ void __launch_bounds__(WF ? 512 : 256, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
-      mbar_init(&full[s], WF ? 1 + kConvWarps : 2);
+      // arrivals per stage: the weight side (TMA producer, or the converter
+      // warps) and the token side (32 gather lanes, or the h TMA producer)
+      mbar_init(&full[s], (WF ? kConvWarps : 1) + (MODE == 1 ? 32 : 1));
       mbar_init(&empty[s], 1);
     }
     for (int r = 0; r < p.NR; ++r) {
@@ -264,6 +268,7 @@ __global__ void __launch_bounds__(WF ? 512 : 256, 1)
           ok = mbar_wait(&full[s], ph, p.status);
           if (!ok) break;
           tc_fence_after();
+          if (MODE == 1) fence_proxy_async_smem();  // cp.async-written tokens -> tensor core
           const uint32_t A = smem_u32(stages + s * stage_bytes);
           const uint32_t B = A + a_bytes;
 #pragma unroll
@@ -285,14 +290,10 @@ __global__ void __launch_bounds__(WF ? 512 : 256, 1)
     }
   } else if (warp == 3) {
     // ------------------------------------------------- token / h producer
-    // GEMM1: all 32 lanes gather the block's token rows with cp.async; a
-    // stage is signalled one stage later, once its copies have completed
-    // (wait_group) and been made visible to the tensor core (proxy fence).
+    // GEMM1: all 32 lanes gather the block's token rows with cp.async; each
+    // lane's copies arrive on the stage's full barrier when they complete.
     // GEMM2: one TMA tile of h per stage.
-    // Up to `lag` = NS - 1 stages of copies are in flight before the oldest
-    // is waited for and signalled, so L2 latency overlaps the MMAs.
-    int s = 0, ph = 0, issued = 0, signalled = 0;
-    const int lag = p.NS - 1 < 7 ? p.NS - 1 : 7;
+    int s = 0, ph = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       const Unit t = unit_info(p, u, nb);
@@ -317,15 +318,7 @@ __global__ void __launch_bounds__(WF ? 512 : 256, 1)
             cp_async16(b_s + n * 128 + ((c ^ (n & 7)) << 4),
                        xg + (int64_t)tok[n] * p.H * 2 + c * 16);
           }
-          cp_async_commit();
-          ++issued;
-          if (issued - signalled > lag) {
-            cp_async_wait(lag);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full[signalled % p.NS]);
-            ++signalled;
-          }
+          cp_async_mbar_arrive(&full[s]);
         } else if (lane == 0) {
           mbar_arrive_expect_tx(&full[s], b_bytes);
           tma_load_2d(B, &maps.b, &full[s], kc * kChunkK, t.b * p.BN);
@@ -333,13 +326,7 @@ __global__ void __launch_bounds__(WF ? 512 : 256, 1)
         if (++s == p.NS) { s = 0; ph ^= 1; }
       }
     }
-    if (MODE == 1 && issued > signalled) {
-      cp_async_wait(0);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0 && ok)
-        for (; signalled < issued; ++signalled) mbar_arrive(&full[signalled % p.NS]);
-    }
+    if (MODE == 1) cp_async_wait_all();  // no copy of this warp outlives the CTA
   } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;
