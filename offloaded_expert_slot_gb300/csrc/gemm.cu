@@ -19,7 +19,8 @@
 //   GEMM2 (MODE 2): per (block, 128 output rows): y = h @ w2^T -> bf16 y
 //     at each route's row.
 // Warp roles: 0 weight producer (TMA), 1 MMA issuer (one thread), 2 TMEM
-// allocator, 3 token/h producer, 4-7 epilogue, 8-15 NVFP4 converters
+// allocator, 3 h producer (GEMM2, TMA), 4-7 epilogue, 8-11 token gather
+// (GEMM1, cp.async), 12-19 NVFP4 converters
 // (NVFP4 only: e2m1 x e4m3 decoded exactly into f16 tiles in shared memory;
 // the per-expert fp32 global scale is applied to the fp32 sums).
 // The weights of a slot are addressed through a 3-D tensor map over the
@@ -39,7 +40,13 @@ namespace {
 
 constexpr int kTileM = 128;  // weight rows per MMA
 constexpr int kChunkK = 64;  // K elements per pipeline stage (128 bytes of 16-bit)
-constexpr int kConvWarps = 8;  // NVFP4 converter warps
+constexpr int kConvWarps = 8;    // NVFP4 converter warps
+constexpr int kGatherWarps = 4;  // GEMM1 token-gather warps
+constexpr int kGatherW0 = 8;     // first gather warp
+constexpr int kConvW0 = kGatherW0 + kGatherWarps;
+constexpr int kMaxUnitsPerCta = 512;  // units whose info is tabled in shared memory
+
+__host__ __device__ constexpr int gemm_threads(int wf) { return 32 * (wf ? kConvW0 + kConvWarps : kConvW0); }
 
 struct GemmMaps {
   CUtensorMap a;   // 16-bit weights [S][rows][K] (bf16 path)
@@ -97,6 +104,26 @@ __device__ __forceinline__ Unit unit_info(const GemmParams& p, int u, int nb) {
 
 __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
 
+struct UnitRec {  // shared-memory copy of a Unit
+  int b, m, slot, nvalid;
+};
+
+// The CTA's u-th unit (u counted in this CTA's sequence), from the table
+// filled at kernel start, or computed directly past the table's end.
+__device__ __forceinline__ Unit my_unit(const GemmParams& p, const UnitRec* tab, int idx, int u, int nb) {
+  if (idx < kMaxUnitsPerCta) {
+    const UnitRec r = tab[idx];
+    Unit t;
+    t.b = r.b;
+    t.m = r.m;
+    t.slot = r.slot;
+    t.nvalid = r.nvalid;
+    t.skip = t.slot < 0 || t.slot >= p.S || t.nvalid == 0;
+    return t;
+  }
+  return unit_info(p, u, nb);
+}
+
 __device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
   uint32_t r;
   asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(r) : "r"(byte));
@@ -146,7 +173,7 @@ __device__ __forceinline__ void convert_row(const uint8_t* q, uint32_t scales, u
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
 template <int MODE, int WF>
-__global__ void __launch_bounds__(WF ? 512 : 256, 1)
+__global__ void __launch_bounds__(gemm_threads(WF), 1)
     grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   constexpr int kA = (MODE == 1) ? 2 : 1;  // weight tiles per stage (gate + up, or w2)
   extern __shared__ uint8_t smem_raw[];
@@ -168,14 +195,14 @@ __global__ void __launch_bounds__(WF ? 512 : 256, 1)
   uint64_t* tfull = rempty + p.NR;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
-  int32_t* tok = reinterpret_cast<int32_t*>(tmem_holder + 4);  // [BN] token rows of the gather
+  UnitRec* utab = reinterpret_cast<UnitRec*>(tmem_holder + 4);  // [kMaxUnitsPerCta]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
       // arrivals per stage: the weight side (TMA producer, or the converter
       // warps) and the token side (32 gather lanes, or the h TMA producer)
-      mbar_init(&full[s], (WF ? kConvWarps : 1) + (MODE == 1 ? 32 : 1));
+      mbar_init(&full[s], (WF ? kConvWarps : 1) + (MODE == 1 ? 32 * kGatherWarps : 1));
       mbar_init(&empty[s], 1);
     }
     for (int r = 0; r < p.NR; ++r) {
@@ -209,14 +236,23 @@ __global__ void __launch_bounds__(WF ? 512 : 256, 1)
   const int nb = *p.n_post_pad / p.BN;
   const int total = nb * p.n_mtiles;
   const uint32_t acc_cols = (MODE == 1) ? 2 * p.BN : p.BN;
+  // every thread looks up one of this CTA's units (independent loads in
+  // parallel), so the roles below never wait on global memory for them
+  for (int i = threadIdx.x; i < kMaxUnitsPerCta; i += blockDim.x) {
+    const int u = blockIdx.x + i * gridDim.x;
+    if (u >= total) break;
+    const Unit t = unit_info(p, u, nb);
+    utab[i] = UnitRec{t.b, t.m, t.slot, t.nvalid};
+  }
+  __syncthreads();
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------- weight producer
       int s = 0, ph = 0, r = 0, rph = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit t = unit_info(p, u, nb);
+      for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+        const Unit t = my_unit(p, utab, ui, u, nb);
         if (t.skip) continue;
         const int row0 = t.m * kTileM;
         for (int kc = 0; kc < p.n_kc && ok; ++kc) {
@@ -255,8 +291,8 @@ __global__ void __launch_bounds__(WF ? 512 : 256, 1)
       uint32_t use[2] = {0, 0};
       int a = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit t = unit_info(p, u, nb);
+      for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+        const Unit t = my_unit(p, utab, ui, u, nb);
         if (t.skip) continue;
         const uint32_t N = round16(t.nvalid);
         const uint32_t idesc = idesc_f16(WF ? 0u : 1u, kTileM, N);
@@ -289,44 +325,61 @@ __global__ void __launch_bounds__(WF ? 512 : 256, 1)
       }
     }
   } else if (warp == 3) {
-    // ------------------------------------------------- token / h producer
-    // GEMM1: all 32 lanes gather the block's token rows with cp.async; each
-    // lane's copies arrive on the stage's full barrier when they complete.
-    // GEMM2: one TMA tile of h per stage.
-    int s = 0, ph = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit t = unit_info(p, u, nb);
-      if (t.skip) continue;
-      const int N = round16(t.nvalid);
-      if (MODE == 1) {
-        __syncwarp();
-        for (int n = lane; n < N; n += 32)
-          tok[n] = (n < t.nvalid) ? p.sorted_ids[(int64_t)t.b * p.BN + n] / p.k : 0;
-        __syncwarp();
-      }
-      for (int kc = 0; kc < p.n_kc; ++kc) {
-        if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, p.status);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        uint8_t* B = stages + s * stage_bytes + a_bytes;
-        if (MODE == 1) {
-          const uint32_t b_s = smem_u32(B);
-          const uint8_t* xg = reinterpret_cast<const uint8_t*>(p.xg) + kc * (kChunkK * 2);
-          for (int i = lane; i < N * 8; i += 32) {
-            const int n = i >> 3, c = i & 7;
-            cp_async16(b_s + n * 128 + ((c ^ (n & 7)) << 4),
-                       xg + (int64_t)tok[n] * p.H * 2 + c * 16);
-          }
-          cp_async_mbar_arrive(&full[s]);
-        } else if (lane == 0) {
+    // ------------------------------------------------ h producer (GEMM2)
+    if (MODE == 2 && lane == 0) {
+      int s = 0, ph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+        const Unit t = my_unit(p, utab, ui, u, nb);
+        if (t.skip) continue;
+        for (int kc = 0; kc < p.n_kc; ++kc) {
+          ok = mbar_wait(&empty[s], ph ^ 1, p.status);
+          if (!ok) break;
+          uint8_t* B = stages + s * stage_bytes + a_bytes;
           mbar_arrive_expect_tx(&full[s], b_bytes);
           tma_load_2d(B, &maps.b, &full[s], kc * kChunkK, t.b * p.BN);
+          if (++s == p.NS) { s = 0; ph ^= 1; }
         }
-        if (++s == p.NS) { s = 0; ph ^= 1; }
       }
     }
-    if (MODE == 1) cp_async_wait_all();  // no copy of this warp outlives the CTA
+  } else if (warp >= kGatherW0 && warp < kGatherW0 + kGatherWarps) {
+    // ----------------------------------------------- token gather (GEMM1)
+    // 128 threads; thread g copies 16-byte chunk (g & 7) of rows
+    // (g >> 3) + 16 j of the block's tokens.  Each thread's copies arrive on
+    // the stage's full barrier when they complete (no thread waits for them).
+    if (MODE == 1) {
+      const int g = threadIdx.x - kGatherW0 * 32;
+      const int c = g & 7, r0 = g >> 3;
+      int s = 0, ph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+        const Unit t = my_unit(p, utab, ui, u, nb);
+        if (t.skip) continue;
+        const int N = round16(t.nvalid);
+        int64_t src_off[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int n = r0 + 16 * j;
+          const int tk = (n < t.nvalid) ? p.sorted_ids[(int64_t)t.b * p.BN + n] / p.k : 0;
+          src_off[j] = (int64_t)tk * p.H * 2 + c * 16;
+        }
+        for (int kc = 0; kc < p.n_kc; ++kc) {
+          if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, p.status);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          const uint32_t b_s = smem_u32(stages + s * stage_bytes + a_bytes);
+          const uint8_t* xg = reinterpret_cast<const uint8_t*>(p.xg) + kc * (kChunkK * 2);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int n = r0 + 16 * j;
+            if (n < N) cp_async16(b_s + n * 128 + ((c ^ (n & 7)) << 4), xg + src_off[j]);
+          }
+          cp_async_mbar_arrive(&full[s]);
+          if (++s == p.NS) { s = 0; ph ^= 1; }
+        }
+      }
+      cp_async_wait_all();  // no copy of this thread outlives the CTA
+    }
   } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;
@@ -334,8 +387,8 @@ __global__ void __launch_bounds__(WF ? 512 : 256, 1)
     uint32_t use[2] = {0, 0};
     int a = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit t = unit_info(p, u, nb);
+    for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+      const Unit t = my_unit(p, utab, ui, u, nb);
       if (t.skip) {
         if (MODE == 2 && t.nvalid > 0) {
           // an expert without a slot: its routes get zeros (and a status bit)
@@ -401,18 +454,18 @@ __global__ void __launch_bounds__(WF ? 512 : 256, 1)
       ++use[a];
       a ^= 1;
     }
-  } else if (WF && warp >= 8) {
+  } else if (WF && warp >= kConvW0) {
     // --------------------------------------------------- NVFP4 converters
     // 256 threads: GEMM1 (256 weight rows per stage) one row each; GEMM2
     // (128 rows) half a row each.
-    const int ct = threadIdx.x - 256;
+    const int ct = threadIdx.x - kConvW0 * 32;
     int s = 0, ph = 0, r = 0, rph = 0;
     bool ok = true;
     const int rr = (MODE == 1) ? ct : (ct & (kTileM - 1));
     const int c_begin = (MODE == 1) ? 0 : (ct >> 7) * 4;
     const int c_end = (MODE == 1) ? 8 : c_begin + 4;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit t = unit_info(p, u, nb);
+    for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+      const Unit t = my_unit(p, utab, ui, u, nb);
       if (t.skip) continue;
       for (int kc = 0; kc < p.n_kc; ++kc) {
         ok = mbar_wait(&rfull[r], rph, p.status) && mbar_wait(&empty[s], ph ^ 1, p.status);
@@ -539,14 +592,14 @@ int smem_plan(int MODE, int wf, int BN, int* NS, int* NR, size_t* bytes) {
   const int kA = MODE == 1 ? 2 : 1;
   const int stage = kA * kTileM * 128 + BN * 128;
   const int raw_stage = ((kA * kTileM * 36) + 1023) / 1024 * 1024;
-  const int budget = 200 * 1024;
-  const int nr = wf ? (MODE == 1 ? 6 : 8) : 0;
+  const int budget = 200 * 1024 - kMaxUnitsPerCta * (int)sizeof(UnitRec);
+  const int nr = wf ? (MODE == 1 ? 5 : 8) : 0;
   const int ns = std::min(8, (budget - nr * raw_stage) / stage);
   if (ns < 2) return OES_ERR_UNSUPPORTED;
   *NS = ns;
   *NR = wf ? nr : 1;
   *bytes = 1024 + (size_t)ns * stage + (size_t)nr * raw_stage +
-           (size_t)(2 * ns + 2 * (*NR) + 4) * 8 + 16 + (size_t)BN * 4 + 64;
+           (size_t)(2 * ns + 2 * (*NR) + 4) * 8 + 16 + (size_t)kMaxUnitsPerCta * sizeof(UnitRec) + 64;
   return OES_OK;
 }
 
@@ -567,7 +620,7 @@ int launch_gemm(const GemmMaps& maps, const GemmParams& p0, int BN, cudaStream_t
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024));
     configured = true;
   }
-  grouped_gemm_kernel<MODE, WF><<<num_sms(), WF ? 512 : 256, smem, stream>>>(maps, p);
+  grouped_gemm_kernel<MODE, WF><<<num_sms(), gemm_threads(WF), smem, stream>>>(maps, p);
   OES_CHECK_LAUNCH("grouped_gemm_kernel");
   return OES_OK;
 }
