@@ -20,7 +20,9 @@
 //     at each route's row.
 // Warp roles: 0 weight producer (TMA), 1 MMA issuer (one thread), 2 TMEM
 // allocator, 3 h producer (GEMM2, TMA), 4-7 epilogue, 8-11 token gather
-// (GEMM1, cp.async), 12-19 NVFP4 converters
+// (GEMM1, cp.async), and for NVFP4 eight converter warps placed on
+// schedulers 0, 2 and 3 (warp id mod 4), so that the scheduler of the MMA
+// issuer carries no ALU-heavy warp.
 // (NVFP4 only: e2m1 x e4m3 decoded exactly into f16 tiles in shared memory;
 // the per-expert fp32 global scale is applied to the fp32 sums).
 // The weights of a slot are addressed through a 3-D tensor map over the
@@ -43,10 +45,25 @@ constexpr int kChunkK = 64;  // K elements per pipeline stage (128 bytes of 16-b
 constexpr int kConvWarps = 8;    // NVFP4 converter warps
 constexpr int kGatherWarps = 4;  // GEMM1 token-gather warps
 constexpr int kGatherW0 = 8;     // first gather warp
-constexpr int kConvW0 = kGatherW0 + kGatherWarps;
 constexpr int kMaxUnitsPerCta = 512;  // units whose info is tabled in shared memory
 
-__host__ __device__ constexpr int gemm_threads(int wf) { return 32 * (wf ? kConvW0 + kConvWarps : kConvW0); }
+// Converter index (0..7) of a warp, or -1: warps 12, 14, 15, 16, 18, 19, 20,
+// 22; warps 13, 17 and 21 (the MMA issuer's scheduler) stay idle.
+__device__ __forceinline__ int conv_index(int warp) {
+  switch (warp) {
+    case 12: return 0;
+    case 14: return 1;
+    case 15: return 2;
+    case 16: return 3;
+    case 18: return 4;
+    case 19: return 5;
+    case 20: return 6;
+    case 22: return 7;
+    default: return -1;
+  }
+}
+
+__host__ __device__ constexpr int gemm_threads(int wf) { return 32 * (wf ? 23 : 12); }
 
 struct GemmMaps {
   CUtensorMap a;   // 16-bit weights [S][rows][K] (bf16 path)
@@ -81,9 +98,12 @@ struct Unit {
 // Which block / tile a unit is, the slot of its expert, and how many of the
 // block's entries are real routes (padding, value R, only at the end).
 __device__ __forceinline__ Unit unit_info(const GemmParams& p, int u, int nb) {
+  // tile index fastest: the units of one block run on neighbouring CTAs at
+  // the same time, so the block's token rows (GEMM1) or h rows (GEMM2) are
+  // read from DRAM once and then served from L2 for its other tiles
   Unit t;
-  t.b = u % nb;
-  t.m = u / nb;
+  t.b = u / p.n_mtiles;
+  t.m = u % p.n_mtiles;
   const int e = p.block_expert[t.b];
   t.slot = (e >= 0 && e < p.E) ? p.e2s[e] : -1;
   const int32_t* s = p.sorted_ids + (int64_t)t.b * p.BN;
@@ -306,14 +326,15 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
           tc_fence_after();
           if (MODE == 1) fence_proxy_async_smem();  // cp.async-written tokens -> tensor core
           const uint32_t A = smem_u32(stages + s * stage_bytes);
-          const uint32_t B = A + a_bytes;
+          // +32 bytes along K = +2 in the descriptor's start-address field
+          const uint64_t ad = smem_desc_sw128(A);
+          const uint64_t ud = smem_desc_sw128(A + kTileM * 128);
+          const uint64_t bd = smem_desc_sw128(A + a_bytes);
 #pragma unroll
           for (int kk = 0; kk < kChunkK / 16; ++kk) {
             const uint32_t acc = (kc | kk) ? 1u : 0u;
-            const uint64_t bd = smem_desc_sw128(B + kk * 32);
-            tc_mma_f16(d0, smem_desc_sw128(A + kk * 32), bd, idesc, acc);
-            if (MODE == 1)
-              tc_mma_f16(d0 + p.BN, smem_desc_sw128(A + kTileM * 128 + kk * 32), bd, idesc, acc);
+            tc_mma_f16(d0, ad + 2 * kk, bd + 2 * kk, idesc, acc);
+            if (MODE == 1) tc_mma_f16(d0 + p.BN, ud + 2 * kk, bd + 2 * kk, idesc, acc);
           }
           tc_commit(&empty[s]);
           if (++s == p.NS) { s = 0; ph ^= 1; }
@@ -454,11 +475,11 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
       ++use[a];
       a ^= 1;
     }
-  } else if (WF && warp >= kConvW0) {
+  } else if (WF && conv_index(warp) >= 0) {
     // --------------------------------------------------- NVFP4 converters
     // 256 threads: GEMM1 (256 weight rows per stage) one row each; GEMM2
     // (128 rows) half a row each.
-    const int ct = threadIdx.x - kConvW0 * 32;
+    const int ct = conv_index(warp) * 32 + lane;
     int s = 0, ph = 0, r = 0, rph = 0;
     bool ok = true;
     const int rr = (MODE == 1) ? ct : (ct & (kTileM - 1));
@@ -475,6 +496,332 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
         uint8_t* A = stages + s * stage_bytes;
         convert_row(Q + rr * 32, SC[rr], A + (rr / kTileM) * kTileM * 128, rr & (kTileM - 1),
                     c_begin, c_end);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&rempty[r]);
+          mbar_arrive(&full[s]);
+        }
+        if (++r == p.NR) { r = 0; rph ^= 1; }
+        if (++s == p.NS) { s = 0; ph ^= 1; }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+
+// ---------------------------------------------------------------------------
+// Token-major variant, for blocks of 128 routes (many routes per expert): the
+// block's 128 token rows are the MMA's M side and a 256-row weight tile its N
+// side (GEMM1: 128 gate rows + the matching 128 up rows; GEMM2: 256 rows of
+// w2), so one 128 x 256 x 16 MMA per K step replaces two 128 x N x 16 ones.
+// TMEM: two 256-column fp32 accumulators; thread = token row in the
+// epilogue, which stores h / y rows with 16-byte vectors.  Same roles,
+// barriers and shared-memory stage layout as the kernel above (weights at
+// the stage start, 32 KB; tokens after them, 16 KB).
+template <int MODE, int WF>
+__global__ void __launch_bounds__(gemm_threads(WF), 1)
+    grouped_gemm_tm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  constexpr int kN = 256;                  // weight rows per tile
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int w_bytes = kN * 128;            // 32 KB of 16-bit weights per K chunk
+  const int x_bytes = kTileM * 128;        // 16 KB of 16-bit tokens per K chunk
+  const int stage_bytes = w_bytes + x_bytes;
+  const int rq_bytes = kN * 32;
+  const int rs_bytes = kN * 4;
+  const int raw_stage = ((rq_bytes + rs_bytes) + 1023) & ~1023;
+  uint8_t* stages = smem;
+  uint8_t* raw = stages + p.NS * stage_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + (WF ? p.NR * raw_stage : 0));
+  uint64_t* full = bars;
+  uint64_t* empty = full + p.NS;
+  uint64_t* rfull = empty + p.NS;
+  uint64_t* rempty = rfull + p.NR;
+  uint64_t* tfull = rempty + p.NR;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
+  UnitRec* utab = reinterpret_cast<UnitRec*>(tmem_holder + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.NS; ++s) {
+      mbar_init(&full[s], (WF ? kConvWarps : 1) + (MODE == 1 ? 32 * kGatherWarps : 1));
+      mbar_init(&empty[s], 1);
+    }
+    for (int r = 0; r < p.NR; ++r) {
+      mbar_init(&rfull[r], 1);
+      mbar_init(&rempty[r], kConvWarps);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    if (MODE == 2) tma_prefetch_desc(&maps.b);
+    if (WF) {
+      tma_prefetch_desc(&maps.q);
+      tma_prefetch_desc(&maps.sc);
+    } else {
+      tma_prefetch_desc(&maps.a);
+    }
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_holder, p.tmem_cols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int nb = *p.n_post_pad / p.BN;
+  const int total = nb * p.n_mtiles;
+  for (int i = threadIdx.x; i < kMaxUnitsPerCta; i += blockDim.x) {
+    const int u = blockIdx.x + i * gridDim.x;
+    if (u >= total) break;
+    const Unit t = unit_info(p, u, nb);
+    utab[i] = UnitRec{t.b, t.m, t.slot, t.nvalid};
+  }
+  __syncthreads();
+
+  // weight rows of tile j: GEMM1 gate [128j, +128) and up [I + 128j, +128);
+  // GEMM2 w2 rows [256j, +256)
+  auto row_a = [&](int j) { return (MODE == 1) ? j * kTileM : j * kN; };
+  auto row_b = [&](int j) { return (MODE == 1) ? p.up_row0 + j * kTileM : j * kN + kTileM; };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------- weight producer
+      int s = 0, ph = 0, r = 0, rph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+        const Unit t = my_unit(p, utab, ui, u, nb);
+        if (t.skip) continue;
+        const int ra = row_a(t.m), rb = row_b(t.m);
+        for (int kc = 0; kc < p.n_kc && ok; ++kc) {
+          if (!WF) {
+            ok = mbar_wait(&empty[s], ph ^ 1, p.status);
+            if (!ok) break;
+            uint8_t* W = stages + s * stage_bytes;
+            mbar_arrive_expect_tx(&full[s], w_bytes);
+            tma_load_3d(W, &maps.a, &full[s], kc * kChunkK, ra, t.slot);
+            tma_load_3d(W + kTileM * 128, &maps.a, &full[s], kc * kChunkK, rb, t.slot);
+            if (++s == p.NS) { s = 0; ph ^= 1; }
+          } else {
+            ok = mbar_wait(&rempty[r], rph ^ 1, p.status);
+            if (!ok) break;
+            uint8_t* Q = raw + r * raw_stage;
+            uint8_t* SC = Q + rq_bytes;
+            mbar_arrive_expect_tx(&rfull[r], rq_bytes + rs_bytes);
+            tma_load_3d(Q, &maps.q, &rfull[r], kc * (kChunkK / 2), ra, t.slot);
+            tma_load_3d(Q + kTileM * 32, &maps.q, &rfull[r], kc * (kChunkK / 2), rb, t.slot);
+            tma_load_3d(SC, &maps.sc, &rfull[r], ra, kc, t.slot);
+            tma_load_3d(SC + kTileM * 4, &maps.sc, &rfull[r], rb, kc, t.slot);
+            if (++r == p.NR) { r = 0; rph ^= 1; }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------- MMA issuer
+      int s = 0, ph = 0;
+      uint32_t use[2] = {0, 0};
+      int a = 0;
+      bool ok = true;
+      const uint32_t idesc = idesc_f16(WF ? 0u : 1u, kTileM, kN);
+      for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+        const Unit t = my_unit(p, utab, ui, u, nb);
+        if (t.skip) continue;
+        ok = mbar_wait(&tempty[a], (use[a] & 1) ^ 1, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + a * kN;
+        for (int kc = 0; kc < p.n_kc; ++kc) {
+          ok = mbar_wait(&full[s], ph, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          if (MODE == 1) fence_proxy_async_smem();  // cp.async-written tokens -> tensor core
+          const uint32_t W = smem_u32(stages + s * stage_bytes);
+          const uint64_t wd = smem_desc_sw128(W);             // B: 256 weight rows
+          const uint64_t xd = smem_desc_sw128(W + w_bytes);   // A: 128 token rows
+#pragma unroll
+          for (int kk = 0; kk < kChunkK / 16; ++kk)
+            tc_mma_f16(d0, xd + 2 * kk, wd + 2 * kk, idesc, (kc | kk) ? 1u : 0u);
+          tc_commit(&empty[s]);
+          if (++s == p.NS) { s = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[a]);
+        ++use[a];
+        a ^= 1;
+      }
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------ h producer (GEMM2)
+    if (MODE == 2 && lane == 0) {
+      int s = 0, ph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+        const Unit t = my_unit(p, utab, ui, u, nb);
+        if (t.skip) continue;
+        for (int kc = 0; kc < p.n_kc; ++kc) {
+          ok = mbar_wait(&empty[s], ph ^ 1, p.status);
+          if (!ok) break;
+          uint8_t* X = stages + s * stage_bytes + w_bytes;
+          mbar_arrive_expect_tx(&full[s], x_bytes);
+          tma_load_2d(X, &maps.b, &full[s], kc * kChunkK, t.b * p.BN);
+          if (++s == p.NS) { s = 0; ph ^= 1; }
+        }
+      }
+    }
+  } else if (warp >= kGatherW0 && warp < kGatherW0 + kGatherWarps) {
+    // ----------------------------------------------- token gather (GEMM1)
+    if (MODE == 1) {
+      const int g = threadIdx.x - kGatherW0 * 32;
+      const int c = g & 7, r0 = g >> 3;
+      int s = 0, ph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+        const Unit t = my_unit(p, utab, ui, u, nb);
+        if (t.skip) continue;
+        const int N = round16(t.nvalid);
+        int64_t src_off[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int n = r0 + 16 * j;
+          const int tk = (n < t.nvalid) ? p.sorted_ids[(int64_t)t.b * p.BN + n] / p.k : 0;
+          src_off[j] = (int64_t)tk * p.H * 2 + c * 16;
+        }
+        for (int kc = 0; kc < p.n_kc; ++kc) {
+          if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, p.status);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          const uint32_t x_s = smem_u32(stages + s * stage_bytes + w_bytes);
+          const uint8_t* xg = reinterpret_cast<const uint8_t*>(p.xg) + kc * (kChunkK * 2);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int n = r0 + 16 * j;
+            if (n < N) cp_async16(x_s + n * 128 + ((c ^ (n & 7)) << 4), xg + src_off[j]);
+          }
+          cp_async_mbar_arrive(&full[s]);
+          if (++s == p.NS) { s = 0; ph ^= 1; }
+        }
+      }
+      cp_async_wait_all();
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int row = q * 32 + lane;  // TMEM lane = token row of the block
+    uint32_t use[2] = {0, 0};
+    int a = 0;
+    bool ok = true;
+    for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+      const Unit t = my_unit(p, utab, ui, u, nb);
+      const bool live = row < t.nvalid;
+      if (t.skip) {
+        if (MODE == 2 && live) {
+          const int r = p.sorted_ids[(int64_t)t.b * p.BN + row];
+          for (int c = 0; c < kN; c += 8) {
+            const int col = t.m * kN + c;
+            if (col < p.H) *reinterpret_cast<uint4*>(p.y + (int64_t)r * p.H + col) = make_uint4(0, 0, 0, 0);
+          }
+          if (row == 0) set_status(p.status, OES_DEV_BAD_ID);
+        }
+        continue;
+      }
+      ok = mbar_wait(&tfull[a], use[a] & 1, p.status);
+      if (!ok) break;
+      tc_fence_after();
+      float gs = 1.0f;
+      if (WF)
+        gs = *reinterpret_cast<const float*>(p.pool + (int64_t)t.slot * p.row_bytes + p.scal_off +
+                                             (MODE == 1 ? 0 : 4));
+      const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16) + a * kN;
+      if (MODE == 1) {
+        uint16_t* hrow = p.h + ((int64_t)t.b * p.BN + row) * p.I;
+        for (int c0 = 0; c0 < kTileM; c0 += 16) {
+          uint32_t g[16], v[16];
+          tmem_ld_16(tl + c0, g);
+          tmem_ld_16(tl + kTileM + c0, v);
+          tc_wait_ld();
+          const int i0 = t.m * kTileM + c0;
+          if (live && i0 < p.I) {
+            uint32_t packed[8];
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+              float h0 = silu(__uint_as_float(g[j]) * gs) * (__uint_as_float(v[j]) * gs);
+              float h1 = silu(__uint_as_float(g[j + 1]) * gs) * (__uint_as_float(v[j + 1]) * gs);
+              uint32_t lo, hi;
+              if (WF) {
+                lo = __half_as_ushort(__float2half_rn(h0));
+                hi = __half_as_ushort(__float2half_rn(h1));
+              } else {
+                lo = __bfloat16_as_ushort(__float2bfloat16_rn(h0));
+                hi = __bfloat16_as_ushort(__float2bfloat16_rn(h1));
+              }
+              packed[j / 2] = lo | (hi << 16);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(hrow + i0);
+            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          }
+        }
+      } else {
+        const int r = live ? p.sorted_ids[(int64_t)t.b * p.BN + row] : 0;
+        uint16_t* yrow = p.y + (int64_t)r * p.H;
+        for (int c0 = 0; c0 < kN; c0 += 16) {
+          uint32_t g[16];
+          tmem_ld_16(tl + c0, g);
+          tc_wait_ld();
+          const int col = t.m * kN + c0;
+          if (live && col < p.H) {
+            uint32_t packed[8];
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+              const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(g[j]) * gs));
+              const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(g[j + 1]) * gs));
+              packed[j / 2] = lo | (hi << 16);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(yrow + col);
+            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[a]);
+      ++use[a];
+      a ^= 1;
+    }
+  } else if (WF && conv_index(warp) >= 0) {
+    // --------------------------------------------------- NVFP4 converters
+    const int rr = conv_index(warp) * 32 + lane;  // one of the 256 weight rows
+    int s = 0, ph = 0, r = 0, rph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
+      const Unit t = my_unit(p, utab, ui, u, nb);
+      if (t.skip) continue;
+      for (int kc = 0; kc < p.n_kc; ++kc) {
+        ok = mbar_wait(&rfull[r], rph, p.status) && mbar_wait(&empty[s], ph ^ 1, p.status);
+        if (!ok) break;
+        const uint8_t* Q = raw + r * raw_stage;
+        const uint32_t* SC = reinterpret_cast<const uint32_t*>(Q + rq_bytes);
+        uint8_t* W = stages + s * stage_bytes;
+        convert_row(Q + rr * 32, SC[rr], W + (rr / kTileM) * kTileM * 128, rr & (kTileM - 1), 0, 8);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -603,6 +950,41 @@ int smem_plan(int MODE, int wf, int BN, int* NS, int* NR, size_t* bytes) {
   return OES_OK;
 }
 
+int smem_plan_tm(int wf, int* NS, int* NR, size_t* bytes) {
+  const int stage = 256 * 128 + kTileM * 128;
+  const int raw_stage = 9 * 1024;
+  const int budget = 220 * 1024 - kMaxUnitsPerCta * (int)sizeof(UnitRec);
+  const int nr = wf ? 4 : 0;
+  const int ns = std::min(6, (budget - nr * raw_stage) / stage);
+  if (ns < 2) return OES_ERR_UNSUPPORTED;
+  *NS = ns;
+  *NR = wf ? nr : 1;
+  *bytes = 1024 + (size_t)ns * stage + (size_t)nr * raw_stage + (size_t)(2 * ns + 2 * (*NR) + 4) * 8 +
+           16 + (size_t)kMaxUnitsPerCta * sizeof(UnitRec) + 64;
+  return OES_OK;
+}
+
+template <int MODE, int WF>
+int launch_gemm_tm(const GemmMaps& maps, const GemmParams& p0, cudaStream_t stream) {
+  GemmParams p = p0;
+  size_t smem;
+  int rc = smem_plan_tm(WF, &p.NS, &p.NR, &smem);
+  if (rc) {
+    set_error("grouped GEMM (token-major): no pipeline fits");
+    return rc;
+  }
+  p.tmem_cols = 512;
+  static bool configured = false;
+  if (!configured) {
+    OES_TRY_CUDA(cudaFuncSetAttribute(grouped_gemm_tm_kernel<MODE, WF>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024));
+    configured = true;
+  }
+  grouped_gemm_tm_kernel<MODE, WF><<<num_sms(), gemm_threads(WF), smem, stream>>>(maps, p);
+  OES_CHECK_LAUNCH("grouped_gemm_tm_kernel");
+  return OES_OK;
+}
+
 template <int MODE, int WF>
 int launch_gemm(const GemmMaps& maps, const GemmParams& p0, int BN, cudaStream_t stream) {
   GemmParams p = p0;
@@ -628,11 +1010,10 @@ int launch_gemm(const GemmMaps& maps, const GemmParams& p0, int BN, cudaStream_t
 }  // namespace
 
 int tile_plan(int R, int E) {
+  // routes per expert of the LAYER: up to 8, blocks of 16 routes on the
+  // weight-major kernel; more, blocks of 128 routes on the token-major one
   const int per = (R + E - 1) / std::max(E, 1);
-  if (per <= 16) return 16;
-  if (per <= 32) return 32;
-  if (per <= 64) return 64;
-  return 128;
+  return per <= 8 ? 16 : 128;
 }
 
 }  // namespace oes
@@ -756,15 +1137,18 @@ extern "C" int moe_grouped_gemm_slots(const oes_routed_experts* v, const uint16_
   p.y = ws.y;
   p.status = status;
 
+  const bool tm = (B == 128);  // token-major kernel for blocks of 128 routes
   GemmParams p1 = p;
   p1.n_mtiles = ceil_div(I, kTileM);
   p1.n_kc = H / kChunkK;
-  rc = wf ? launch_gemm<1, 1>(m1, p1, B, stream) : launch_gemm<1, 0>(m1, p1, B, stream);
+  if (tm) rc = wf ? launch_gemm_tm<1, 1>(m1, p1, stream) : launch_gemm_tm<1, 0>(m1, p1, stream);
+  else rc = wf ? launch_gemm<1, 1>(m1, p1, B, stream) : launch_gemm<1, 0>(m1, p1, B, stream);
   if (rc) return rc;
   GemmParams p2 = p;
-  p2.n_mtiles = ceil_div(H, kTileM);
+  p2.n_mtiles = tm ? ceil_div(H, 256) : ceil_div(H, kTileM);
   p2.n_kc = I / kChunkK;
-  rc = wf ? launch_gemm<2, 1>(m2, p2, B, stream) : launch_gemm<2, 0>(m2, p2, B, stream);
+  if (tm) rc = wf ? launch_gemm_tm<2, 1>(m2, p2, stream) : launch_gemm_tm<2, 0>(m2, p2, stream);
+  else rc = wf ? launch_gemm<2, 1>(m2, p2, B, stream) : launch_gemm<2, 0>(m2, p2, B, stream);
   if (rc) return rc;
   const int64_t nvec = (int64_t)T * (H / 8);
   combine_kernel<<<(int)std::min<int64_t>(ceil_div64(nvec, 256), (int64_t)num_sms() * 8), 256, 0,

@@ -52,17 +52,18 @@ def test_host_argument_checks(lib):
 
 
 def test_tile_plan_uses_the_layers_expert_count(lib):
-    """FreeToken PR #676, Solution: the prefill picks its tiles from tokens
-    per expert of the layer, not of the slot pool.  At 4096 tokens x top-10
-    the layer's 512 experts give 80 routes per expert (block 128); sizing by
-    1650 slots would give 25 (block 32)."""
+    """FreeToken PR #676, Solution and Tests: the prefill picks its tiles from
+    tokens per expert of the layer, not of the slot pool.  At 600 tokens x
+    top-10 the layer's 512 experts get 11.7 routes each (blocks of 128 routes,
+    token-major kernel); sizing by the 1100 slots would give 5.5 (blocks of
+    16, weight-major kernel)."""
+    assert oes.oes_tile_plan(600 * 10, 512) == 128
+    assert oes.oes_tile_plan(600 * 10, 1100) == 16
     assert oes.oes_tile_plan(4096 * 10, 512) == 128
-    assert oes.oes_tile_plan(4096 * 10, 1650) == 32
     assert oes.oes_tile_plan(32 * 10, 512) == 16
-    assert oes.oes_tile_plan(600 * 10, 512) == 16
+    assert oes.oes_tile_plan(200 * 10, 512) == 16
     assert oes.oes_tile_plan(16 * 2, 8) == 16
-    for R, E, want in [(16 * 512, 512, 16), (17 * 512, 512, 32), (33 * 512, 512, 64),
-                       (65 * 512, 512, 128), (0, 5, 16)]:
+    for R, E, want in [(8 * 512, 512, 16), (8 * 512 + 1, 512, 128), (0, 5, 16)]:
         assert oes.oes_tile_plan(R, E) == want
 
 
