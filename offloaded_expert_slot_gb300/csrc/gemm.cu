@@ -45,7 +45,7 @@ constexpr int kChunkK = 64;  // K elements per pipeline stage (128 bytes of 16-b
 constexpr int kConvWarps = 8;    // NVFP4 converter warps
 constexpr int kGatherWarps = 4;  // GEMM1 token-gather warps
 constexpr int kGatherW0 = 8;     // first gather warp
-constexpr int kMaxUnitsPerCta = 512;  // units whose info is tabled in shared memory
+constexpr int kMaxUnitsPerCta = 256;  // units whose info is tabled in shared memory
 
 // Converter index (0..7) of a warp, or -1: warps 12, 14, 15, 16, 18, 19, 20,
 // 22; warps 13, 17 and 21 (the MMA issuer's scheduler) stay idle.
@@ -64,6 +64,11 @@ __device__ __forceinline__ int conv_index(int warp) {
 }
 
 __host__ __device__ constexpr int gemm_threads(int wf) { return 32 * (wf ? 23 : 12); }
+// token-major kernel: NVFP4 adds 16 converter warps (12..27) in two groups of
+// eight that take alternate pipeline stages
+constexpr int kTmConvW0 = 12;
+constexpr int kTmConvWarps = 16;
+__host__ __device__ constexpr int gemm_threads_tm(int wf) { return 32 * (wf ? kTmConvW0 + kTmConvWarps : 12); }
 
 struct GemmMaps {
   CUtensorMap a;   // 16-bit weights [S][rows][K] (bf16 path)
@@ -527,7 +532,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
 // barriers and shared-memory stage layout as the kernel above (weights at
 // the stage start, 32 KB; tokens after them, 16 KB).
 template <int MODE, int WF>
-__global__ void __launch_bounds__(gemm_threads(WF), 1)
+__global__ void __launch_bounds__(gemm_threads_tm(WF), 1)
     grouped_gemm_tm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   constexpr int kN = 256;                  // weight rows per tile
   extern __shared__ uint8_t smem_raw[];
@@ -807,26 +812,31 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
       ++use[a];
       a ^= 1;
     }
-  } else if (WF && conv_index(warp) >= 0) {
+  } else if (WF && warp >= kTmConvW0) {
     // --------------------------------------------------- NVFP4 converters
-    const int rr = conv_index(warp) * 32 + lane;  // one of the 256 weight rows
-    int s = 0, ph = 0, r = 0, rph = 0;
+    // group 0 converts the even pipeline stages, group 1 the odd ones; in a
+    // group, thread rr converts weight row rr of the 256-row tile
+    const int group = (warp - kTmConvW0) >> 3;
+    const int rr = ((warp - kTmConvW0) & 7) * 32 + lane;
+    int s = 0, ph = 0, r = 0, rph = 0, n = 0;
     bool ok = true;
     for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
       const Unit t = my_unit(p, utab, ui, u, nb);
       if (t.skip) continue;
-      for (int kc = 0; kc < p.n_kc; ++kc) {
-        ok = mbar_wait(&rfull[r], rph, p.status) && mbar_wait(&empty[s], ph ^ 1, p.status);
-        if (!ok) break;
-        const uint8_t* Q = raw + r * raw_stage;
-        const uint32_t* SC = reinterpret_cast<const uint32_t*>(Q + rq_bytes);
-        uint8_t* W = stages + s * stage_bytes;
-        convert_row(Q + rr * 32, SC[rr], W + (rr / kTileM) * kTileM * 128, rr & (kTileM - 1), 0, 8);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&rempty[r]);
-          mbar_arrive(&full[s]);
+      for (int kc = 0; kc < p.n_kc; ++kc, ++n) {
+        if ((n & 1) == group) {
+          ok = mbar_wait(&rfull[r], rph, p.status) && mbar_wait(&empty[s], ph ^ 1, p.status);
+          if (!ok) break;
+          const uint8_t* Q = raw + r * raw_stage;
+          const uint32_t* SC = reinterpret_cast<const uint32_t*>(Q + rq_bytes);
+          uint8_t* W = stages + s * stage_bytes;
+          convert_row(Q + rr * 32, SC[rr], W + (rr / kTileM) * kTileM * 128, rr & (kTileM - 1), 0, 8);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&rempty[r]);
+            mbar_arrive(&full[s]);
+          }
         }
         if (++r == p.NR) { r = 0; rph ^= 1; }
         if (++s == p.NS) { s = 0; ph ^= 1; }
@@ -954,7 +964,7 @@ int smem_plan_tm(int wf, int* NS, int* NR, size_t* bytes) {
   const int stage = 256 * 128 + kTileM * 128;
   const int raw_stage = 9 * 1024;
   const int budget = 220 * 1024 - kMaxUnitsPerCta * (int)sizeof(UnitRec);
-  const int nr = wf ? 4 : 0;
+  const int nr = wf ? 8 : 0;
   const int ns = std::min(6, (budget - nr * raw_stage) / stage);
   if (ns < 2) return OES_ERR_UNSUPPORTED;
   *NS = ns;
@@ -980,7 +990,7 @@ int launch_gemm_tm(const GemmMaps& maps, const GemmParams& p0, cudaStream_t stre
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024));
     configured = true;
   }
-  grouped_gemm_tm_kernel<MODE, WF><<<num_sms(), gemm_threads(WF), smem, stream>>>(maps, p);
+  grouped_gemm_tm_kernel<MODE, WF><<<num_sms(), gemm_threads_tm(WF), smem, stream>>>(maps, p);
   OES_CHECK_LAUNCH("grouped_gemm_tm_kernel");
   return OES_OK;
 }
