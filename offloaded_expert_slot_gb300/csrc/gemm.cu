@@ -35,6 +35,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "gemm_types.h"
 #include "internal.h"
 
 namespace oes {
@@ -70,35 +71,12 @@ constexpr int kTmConvW0 = 12;
 constexpr int kTmConvWarps = 16;
 __host__ __device__ constexpr int gemm_threads_tm(int wf) { return 32 * (wf ? kTmConvW0 + kTmConvWarps : 12); }
 
-struct GemmMaps {
-  CUtensorMap a;   // 16-bit weights [S][rows][K] (bf16 path)
-  CUtensorMap q;   // NVFP4 values [S][rows][K/2] bytes
-  CUtensorMap sc;  // NVFP4 scales [S][K/64][rows] u32
-  CUtensorMap b;   // GEMM2: h [cap][I]
-};
-
-struct GemmParams {
-  const int32_t* sorted_ids;
-  const int32_t* block_expert;
-  const int32_t* n_post_pad;
-  const int32_t* e2s;
-  const uint8_t* pool;
-  int64_t row_bytes;
-  int64_t scal_off;  // NVFP4: byte offset of the fp32 scalars in a row
-  int R, k, BN, H, I, E, S;
-  int n_mtiles, n_kc, up_row0;  // up_row0: first up row of w13 (= I)
-  int NS, NR;                   // pipeline depths
-  uint32_t tmem_cols;
-  const uint16_t* xg;  // GEMM1: token rows to gather, [T, H] (bf16, or f16 for NVFP4)
-  uint16_t* h;  // [cap, I]
-  uint16_t* y;  // [R, H] bf16
-  int32_t* status;
-};
-
 struct Unit {
   int b, m, slot, nvalid;
   bool skip;
 };
+
+constexpr int kFiltered = -2;  // Unit::slot of a block another launch computes
 
 // Which block / tile a unit is, the slot of its expert, and how many of the
 // block's entries are real routes (padding, value R, only at the end).
@@ -110,7 +88,13 @@ __device__ __forceinline__ Unit unit_info(const GemmParams& p, int u, int nb) {
   t.b = u / p.n_mtiles;
   t.m = u % p.n_mtiles;
   const int e = p.block_expert[t.b];
-  t.slot = (e >= 0 && e < p.E) ? p.e2s[e] : -1;
+  const bool valid_e = e >= 0 && e < p.E;
+  bool filtered = false;
+  if (p.filter && valid_e) {
+    const bool resident = p.flags[e] != 0;
+    filtered = (p.filter == 1) ? !resident : resident;
+  }
+  t.slot = filtered ? kFiltered : (valid_e ? p.e2s[e] : -1);
   const int32_t* s = p.sorted_ids + (int64_t)t.b * p.BN;
   if (s[p.BN - 1] < p.R) {
     t.nvalid = p.BN;
@@ -416,7 +400,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
     for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
       const Unit t = my_unit(p, utab, ui, u, nb);
       if (t.skip) {
-        if (MODE == 2 && t.nvalid > 0) {
+        if (MODE == 2 && t.nvalid > 0 && t.slot != kFiltered) {
           // an expert without a slot: its routes get zeros (and a status bit)
           const int col = t.m * kTileM + row;
           if (col < p.H)
@@ -737,7 +721,7 @@ __global__ void __launch_bounds__(gemm_threads_tm(WF), 1)
       const Unit t = my_unit(p, utab, ui, u, nb);
       const bool live = row < t.nvalid;
       if (t.skip) {
-        if (MODE == 2 && live) {
+        if (MODE == 2 && live && t.slot != kFiltered) {
           const int r = p.sorted_ids[(int64_t)t.b * p.BN + row];
           for (int c = 0; c < kN; c += 8) {
             const int col = t.m * kN + c;
@@ -1042,14 +1026,15 @@ extern "C" size_t moe_grouped_gemm_workspace_size(const oes_routed_experts* v, i
   return carve(nullptr, T, k, v->E, v->H, v->I, B, v->wfmt).bytes;
 }
 
-extern "C" int moe_grouped_gemm_slots(const oes_routed_experts* v, const uint16_t* x, int T, int k,
-                                      const int32_t* ids, const float* weights,
-                                      const int32_t* sorted_ids, const int32_t* block_expert,
-                                      const int32_t* n_post_pad, int B, void* workspace,
-                                      size_t workspace_bytes, uint16_t* out, int32_t* status,
-                                      oes_stream_t stream) {
-  OES_REQUIRE(v && x && ids && weights && sorted_ids && block_expert && n_post_pad && out &&
-                  workspace && v->pool && v->e2s,
+namespace oes {
+
+// Validates the call, writes the f16 copy of x (NVFP4), and builds the tensor
+// maps and kernel parameters of both GEMMs.
+int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
+                 const int32_t* sorted_ids, const int32_t* block_expert, const int32_t* n_post_pad,
+                 int B, void* workspace, size_t workspace_bytes, int32_t* status, cudaStream_t stream,
+                 GemmPlan* g) {
+  OES_REQUIRE(v && x && sorted_ids && block_expert && n_post_pad && workspace && v->pool && v->e2s,
               "moe_grouped_gemm_slots: null pointer");
   const int E = v->E, H = v->H, I = v->I, S = v->S;
   OES_REQUIRE(E >= 1 && E <= OES_MAX_EXPERTS && S >= 1, "moe_grouped_gemm_slots: bad E=%d S=%d", E, S);
@@ -1062,13 +1047,14 @@ extern "C" int moe_grouped_gemm_slots(const oes_routed_experts* v, const uint16_
   OES_REQUIRE(v->row_bytes >= need_row && v->row_bytes % 16 == 0,
               "moe_grouped_gemm_slots: row_bytes %lld (layout needs %lld, multiple of 16)",
               (long long)v->row_bytes, (long long)need_row);
-  OES_REQUIRE(((uintptr_t)v->pool & 15) == 0 && ((uintptr_t)x & 15) == 0 && ((uintptr_t)out & 15) == 0,
-              "moe_grouped_gemm_slots: pool, x and out must be 16-byte aligned");
+  OES_REQUIRE(((uintptr_t)v->pool & 15) == 0 && ((uintptr_t)x & 15) == 0,
+              "moe_grouped_gemm_slots: pool and x must be 16-byte aligned");
   const int R = T * k;
   const int plan = tile_plan(R, E);
   OES_REQUIRE(B == plan, "moe_grouped_gemm_slots: block %d differs from the tile plan %d (R=%d, E=%d)",
               B, plan, R, E);
-  if (T == 0) return OES_OK;
+  g->empty = (T == 0);
+  if (g->empty) return OES_OK;
   OES_REQUIRE(((uintptr_t)workspace & 255) == 0, "moe_grouped_gemm_slots: workspace not 256-byte aligned");
   const Ws ws = carve(workspace, T, k, E, H, I, B, v->wfmt);
   OES_REQUIRE(workspace_bytes >= ws.bytes, "moe_grouped_gemm_slots: workspace %zu < %zu bytes",
@@ -1077,6 +1063,13 @@ extern "C" int moe_grouped_gemm_slots(const oes_routed_experts* v, const uint16_
   const Sections sec = sections(v->wfmt, H, I);
   const uint8_t* pool = static_cast<const uint8_t*>(v->pool);
   const int wf = v->wfmt == OES_WFMT_NVFP4;
+  g->wf = wf;
+  g->tm = (B == 128);  // token-major kernel for blocks of 128 routes
+  g->y = ws.y;
+  g->T = T;
+  g->k = k;
+  g->H = H;
+  g->E = E;
 
   GemmMaps m1{}, m2{};
   int rc;
@@ -1131,6 +1124,8 @@ extern "C" int moe_grouped_gemm_slots(const oes_routed_experts* v, const uint16_
   p.block_expert = block_expert;
   p.n_post_pad = n_post_pad;
   p.e2s = v->e2s;
+  p.flags = nullptr;
+  p.filter = 0;
   p.pool = pool;
   p.row_bytes = v->row_bytes;
   p.scal_off = sec.scal;
@@ -1146,23 +1141,58 @@ extern "C" int moe_grouped_gemm_slots(const oes_routed_experts* v, const uint16_
   p.h = ws.h;
   p.y = ws.y;
   p.status = status;
+  g->m1 = m1;
+  g->m2 = m2;
+  g->p1 = p;
+  g->p1.n_mtiles = ceil_div(I, kTileM);
+  g->p1.n_kc = H / kChunkK;
+  g->p2 = p;
+  g->p2.n_mtiles = g->tm ? ceil_div(H, 256) : ceil_div(H, kTileM);
+  g->p2.n_kc = I / kChunkK;
+  return OES_OK;
+}
 
-  const bool tm = (B == 128);  // token-major kernel for blocks of 128 routes
-  GemmParams p1 = p;
-  p1.n_mtiles = ceil_div(I, kTileM);
-  p1.n_kc = H / kChunkK;
-  if (tm) rc = wf ? launch_gemm_tm<1, 1>(m1, p1, stream) : launch_gemm_tm<1, 0>(m1, p1, stream);
-  else rc = wf ? launch_gemm<1, 1>(m1, p1, B, stream) : launch_gemm<1, 0>(m1, p1, B, stream);
+// GEMM1 then GEMM2 over the blocks `filter` selects (flags: device [E]).
+int gemm_run(const GemmPlan& g, int filter, const uint8_t* flags, cudaStream_t stream) {
+  if (g.empty) return OES_OK;
+  GemmParams p1 = g.p1, p2 = g.p2;
+  p1.filter = p2.filter = filter;
+  p1.flags = p2.flags = flags;
+  const int B = p1.BN;
+  int rc;
+  if (g.tm) rc = g.wf ? launch_gemm_tm<1, 1>(g.m1, p1, stream) : launch_gemm_tm<1, 0>(g.m1, p1, stream);
+  else rc = g.wf ? launch_gemm<1, 1>(g.m1, p1, B, stream) : launch_gemm<1, 0>(g.m1, p1, B, stream);
   if (rc) return rc;
-  GemmParams p2 = p;
-  p2.n_mtiles = tm ? ceil_div(H, 256) : ceil_div(H, kTileM);
-  p2.n_kc = I / kChunkK;
-  if (tm) rc = wf ? launch_gemm_tm<2, 1>(m2, p2, stream) : launch_gemm_tm<2, 0>(m2, p2, stream);
-  else rc = wf ? launch_gemm<2, 1>(m2, p2, B, stream) : launch_gemm<2, 0>(m2, p2, B, stream);
-  if (rc) return rc;
-  const int64_t nvec = (int64_t)T * (H / 8);
+  if (g.tm) rc = g.wf ? launch_gemm_tm<2, 1>(g.m2, p2, stream) : launch_gemm_tm<2, 0>(g.m2, p2, stream);
+  else rc = g.wf ? launch_gemm<2, 1>(g.m2, p2, B, stream) : launch_gemm<2, 0>(g.m2, p2, B, stream);
+  return rc;
+}
+
+int gemm_combine(const GemmPlan& g, const int32_t* ids, const float* weights, uint16_t* out,
+                 cudaStream_t stream) {
+  if (g.empty) return OES_OK;
+  OES_REQUIRE(ids && weights && out && ((uintptr_t)out & 15) == 0,
+              "moe_grouped_gemm_slots: ids, weights and a 16-byte aligned out are required");
+  const int64_t nvec = (int64_t)g.T * (g.H / 8);
   combine_kernel<<<(int)std::min<int64_t>(ceil_div64(nvec, 256), (int64_t)num_sms() * 8), 256, 0,
-                   stream>>>(ws.y, weights, ids, T, k, H, E, out);
+                   stream>>>(g.y, weights, ids, g.T, g.k, g.H, g.E, out);
   OES_CHECK_LAUNCH("combine_kernel");
   return OES_OK;
+}
+
+}  // namespace oes
+
+extern "C" int moe_grouped_gemm_slots(const oes_routed_experts* v, const uint16_t* x, int T, int k,
+                                      const int32_t* ids, const float* weights,
+                                      const int32_t* sorted_ids, const int32_t* block_expert,
+                                      const int32_t* n_post_pad, int B, void* workspace,
+                                      size_t workspace_bytes, uint16_t* out, int32_t* status,
+                                      oes_stream_t stream) {
+  OES_REQUIRE(ids && weights && out, "moe_grouped_gemm_slots: null pointer");
+  GemmPlan g;
+  int rc = gemm_prepare(v, x, T, k, sorted_ids, block_expert, n_post_pad, B, workspace,
+                        workspace_bytes, status, stream, &g);
+  if (rc) return rc;
+  if ((rc = gemm_run(g, 0, nullptr, stream))) return rc;
+  return gemm_combine(g, ids, weights, out, stream);
 }

@@ -1,0 +1,58 @@
+// Parameters of the grouped GEMM kernels, and the host-side plan the layer
+// composites use to launch the GEMM in parts (private to liboes).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "oes.h"
+
+namespace oes {
+
+struct GemmMaps {
+  CUtensorMap a;   // 16-bit weights [S][rows][K] (bf16 path)
+  CUtensorMap q;   // NVFP4 values [S][rows][K/2] bytes
+  CUtensorMap sc;  // NVFP4 scales [S][K/64][rows] u32
+  CUtensorMap b;   // GEMM2: h [cap][I]
+};
+
+struct GemmParams {
+  const int32_t* sorted_ids;
+  const int32_t* block_expert;
+  const int32_t* n_post_pad;
+  const int32_t* e2s;
+  const uint8_t* flags;  // [E] 1 = expert resident before the chunk (filtered launches)
+  int filter;            // 0 all blocks; 1 resident experts only; 2 the others only
+  const uint8_t* pool;
+  int64_t row_bytes;
+  int64_t scal_off;  // NVFP4: byte offset of the fp32 scalars in a row
+  int R, k, BN, H, I, E, S;
+  int n_mtiles, n_kc, up_row0;  // up_row0: first up row of w13 (= I)
+  int NS, NR;                   // pipeline depths
+  uint32_t tmem_cols;
+  const uint16_t* xg;  // GEMM1: token rows to gather, [T, H] (bf16, or f16 for NVFP4)
+  uint16_t* h;  // [cap, I]
+  uint16_t* y;  // [R, H] bf16
+  int32_t* status;
+};
+
+// Everything needed to launch GEMM1 / GEMM2 / combine of one call.
+struct GemmPlan {
+  GemmMaps m1, m2;
+  GemmParams p1, p2;
+  bool empty, tm;
+  int wf, T, k, H, E;
+  uint16_t* y;
+};
+
+int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
+                 const int32_t* sorted_ids, const int32_t* block_expert, const int32_t* n_post_pad,
+                 int B, void* workspace, size_t workspace_bytes, int32_t* status, cudaStream_t stream,
+                 GemmPlan* plan);
+// filter: 0 every block; 1 blocks of experts with flags[e] != 0; 2 the others
+int gemm_run(const GemmPlan& plan, int filter, const uint8_t* flags, cudaStream_t stream);
+int gemm_combine(const GemmPlan& plan, const int32_t* ids, const float* weights, uint16_t* out,
+                 cudaStream_t stream);
+
+}  // namespace oes

@@ -5,6 +5,8 @@
 
 #include <vector>
 
+#include <cuda_runtime.h>
+
 #include "oes.h"
 
 struct oes_slot_cache {
@@ -16,6 +18,10 @@ struct oes_slot_cache {
   int64_t* slot_ts;      // [S] timestamp of the last query that touched the slot, 0 if empty
   int64_t* ctr;          // [4] clock, hits, misses, evictions
   int64_t* decode_freq;  // [L*E]
+  // side stream and events of moe_layer_forward_slots: the GEMM over experts
+  // resident before the chunk runs there while the misses are copied
+  cudaStream_t side;
+  cudaEvent_t fork, join;
 };
 
 struct oes_expert_source {

@@ -9,6 +9,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "gemm_types.h"
 #include "internal.h"
 
 namespace oes {
@@ -26,6 +27,7 @@ struct LayerWs {
   int32_t* block_expert;
   int32_t* n_post_pad;
   int32_t* e2s_identity;
+  uint8_t* resident;  // [E] expert resident before the chunk
   void* align_ws;
   size_t align_bytes;
   void* gemm_ws;
@@ -57,6 +59,7 @@ LayerWs carve_layer(void* base, const oes_layer_desc* d, int T, int k) {
   w.block_expert = static_cast<int32_t*>(take((size_t)std::max<int64_t>(cap / B, 1) * 4));
   w.n_post_pad = static_cast<int32_t*>(take(4));
   w.e2s_identity = static_cast<int32_t*>(take((size_t)E * 4));
+  w.resident = static_cast<uint8_t*>(take((size_t)E));
   w.align_bytes = moe_align_workspace_size(R, E, B);
   w.align_ws = take(w.align_bytes);
   oes_routed_experts v{};
@@ -68,6 +71,20 @@ LayerWs carve_layer(void* base, const oes_layer_desc* d, int T, int k) {
   w.gemm_ws = take(w.gemm_bytes);
   w.total = off + 256;
   return w;
+}
+
+// resident[e] = 1 for the chunk's experts that already have a slot.  Taken
+// before the first ensure: a layer never routes to more experts than the pool
+// holds, so no query of the chunk evicts a slot the chunk uses, and these
+// experts keep their slots (and bytes) through all of the chunk's queries.
+__global__ void resident_flags_kernel(const int32_t* __restrict__ distinct, int n, int E, int layer,
+                                      const int32_t* __restrict__ map, uint8_t* __restrict__ resident) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) resident[e] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int e = distinct[i];
+    if (e >= 0 && e < E) resident[e] = map[(int64_t)layer * E + e] >= 0 ? 1 : 0;
+  }
 }
 
 __global__ void iota_kernel(int32_t* a, int n) {
@@ -146,14 +163,8 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
   if ((rc = route(d, c, w, stream))) return rc;
   if ((rc = moe_distinct_experts(w.ids, R, E, w.distinct, w.d_count, stream))) return rc;
   const int Lq = std::min(R, E);
-  for (int q0 = 0; q0 < Lq; q0 += OES_QUERY_MAX) {
-    const int n = std::min(OES_QUERY_MAX, Lq - q0);
-    if ((rc = slot_cache_ensure(cache, layer, w.distinct + q0, n, record_stats, w.miss, w.n_miss,
-                                c->status, stream)))
-      return rc;
-    if ((rc = slot_cache_copy_misses(src, pool, cache->S, w.miss, w.n_miss, n, c->status, stream)))
-      return rc;
-  }
+  resident_flags_kernel<<<1, 1024, 0, stream>>>(w.distinct, Lq, E, layer, cache->map, w.resident);
+  OES_CHECK_LAUNCH("resident_flags_kernel");
   if ((rc = moe_align_block_size(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad,
                                  c->status, w.align_ws, w.align_bytes, stream)))
     return rc;
@@ -169,8 +180,29 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
   v.I = d->I;
   v.input_scale13 = d->input_scale13;
   v.input_scale2 = d->input_scale2;
-  return moe_grouped_gemm_slots(&v, c->x, T, k, w.ids, w.w, w.sorted_ids, w.block_expert,
-                                w.n_post_pad, B, w.gemm_ws, w.gemm_bytes, c->out, c->status, stream);
+  GemmPlan g;
+  if ((rc = gemm_prepare(&v, c->x, T, k, w.sorted_ids, w.block_expert, w.n_post_pad, B, w.gemm_ws,
+                         w.gemm_bytes, c->status, stream, &g)))
+    return rc;
+  // side stream: the GEMM over the experts already resident, overlapping the
+  // copies of the misses on the caller's stream
+  OES_TRY_CUDA(cudaEventRecord(cache->fork, stream));
+  OES_TRY_CUDA(cudaStreamWaitEvent(cache->side, cache->fork, 0));
+  if ((rc = gemm_run(g, 1, w.resident, cache->side))) return rc;
+  OES_TRY_CUDA(cudaEventRecord(cache->join, cache->side));
+  // caller's stream: each query of at most OES_QUERY_MAX distinct experts is
+  // ensured and its misses copied before the next query
+  for (int q0 = 0; q0 < Lq; q0 += OES_QUERY_MAX) {
+    const int n = std::min(OES_QUERY_MAX, Lq - q0);
+    if ((rc = slot_cache_ensure(cache, layer, w.distinct + q0, n, record_stats, w.miss, w.n_miss,
+                                c->status, stream)))
+      return rc;
+    if ((rc = slot_cache_copy_misses(src, pool, cache->S, w.miss, w.n_miss, n, c->status, stream)))
+      return rc;
+  }
+  if ((rc = gemm_run(g, 2, w.resident, stream))) return rc;   // the experts just copied
+  OES_TRY_CUDA(cudaStreamWaitEvent(stream, cache->join, 0));
+  return gemm_combine(g, w.ids, w.w, c->out, stream);
 }
 
 extern "C" int moe_layer_forward_stream(const oes_expert_source* src, void* layer_buf, int layer,

@@ -253,10 +253,21 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   const size_t LE = (size_t)L * E;
   const size_t bytes = LE * 4 + (size_t)S * 4 + (size_t)S * 8 + 4 * 8 + LE * 8 + 64;
   c->block_bytes = bytes;
+  c->side = nullptr;
+  c->fork = c->join = nullptr;
   cudaError_t e = cudaMalloc(&c->block, bytes);
   if (e != cudaSuccess) {
     delete c;
     return cuda_fail(e, "cudaMalloc(slot cache tables)");
+  }
+  if ((e = cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking)) != cudaSuccess ||
+      (e = cudaEventCreateWithFlags(&c->fork, cudaEventDisableTiming)) != cudaSuccess ||
+      (e = cudaEventCreateWithFlags(&c->join, cudaEventDisableTiming)) != cudaSuccess) {
+    if (c->fork) cudaEventDestroy(c->fork);
+    if (c->side) cudaStreamDestroy(c->side);
+    cudaFree(c->block);
+    delete c;
+    return cuda_fail(e, "slot_cache_create: side stream / events");
   }
   uint8_t* p = static_cast<uint8_t*>(c->block);
   c->slot_ts = reinterpret_cast<int64_t*>(p);
@@ -282,6 +293,10 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
 
 extern "C" int slot_cache_destroy(oes_slot_cache* c) {
   if (!c) return OES_OK;
+  if (c->side) cudaStreamSynchronize(c->side);
+  if (c->join) cudaEventDestroy(c->join);
+  if (c->fork) cudaEventDestroy(c->fork);
+  if (c->side) cudaStreamDestroy(c->side);
   cudaError_t e = cudaFree(c->block);
   delete c;
   if (e != cudaSuccess) return cuda_fail(e, "cudaFree(slot cache tables)");
