@@ -33,8 +33,8 @@ class LayerConfig:
     layer: int = 0         # layer that is forwarded
     seed: int = 0
     # NVFP4 only: the forwarded layers' input scales and the value every
-    # other slot carries (FreeToken PR #676, Tests: "9.0 in every slot
-    # against the layer's 2.0 and 3.0").
+    # other slot carries (FreeToken PR #676, Tests: the layer's scales are
+    # 2.0 and 3.0, every slot holds 9.0).
     layer_input_scales: tuple = ()
     other_slot_input_scale: float = 0.0
     distinct_source_layers: int = 0   # 0: one pinned source per layer

@@ -1,8 +1,9 @@
 // moe_align_block_size for any expert count: a stable counting sort of
 // routes by expert in three launches (FreeToken PR #676, Solution and Tests:
-// sgl_kernel counts experts in one 1024-thread block and reads out of
-// bounds once num_experts + 1 > 1024; every route must land once, in a block
-// of its expert; vLLM fork PR #48, What: ignore_invalid_experts).
+// sgl_kernel's single-block count breaks once the experts and the padding
+// id no longer fit 1024 threads; each route must be placed exactly once,
+// in a block of its own expert; vLLM fork PR #48, What:
+// ignore_invalid_experts).
 //
 //   count:   CTA g histograms its contiguous range of routes -> cnt[g][e]
 //   scan:    one CTA: per expert, exclusive prefix over CTAs; padded sizes;

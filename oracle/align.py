@@ -1,9 +1,10 @@
 """moe_align_block_size as a stable counting sort of routes by expert.
 
 Test infrastructure only.  Sources: FreeToken PR #676, Solution and Tests
-(the align must be right past 1024 experts; "every route lands once, in a
-block of its expert"), gdevenyi's review comment there (sgl_kernel's align
-reads out of bounds once num_experts + 1 > 1024), vLLM fork PR #48, What
+(the align must be right past 1024 experts, with each route placed exactly
+once and only in a block of its own expert), gdevenyi's review comment there
+(sgl_kernel's single-block align breaks once num_experts + 1 exceeds 1024
+threads), vLLM fork PR #48, What
 (logical alignment with ignore_invalid_experts, then a physical-row remap).
 
 Input: ids [R] (route r = t*k + j), E experts, block size B.

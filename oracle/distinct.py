@@ -1,9 +1,9 @@
 """The chunk's distinct experts as a sorted list of fixed length.
 
 Test infrastructure only.  FreeToken PR #676, Solution: the distinct experts
-are "a sorted list of fixed length, so there is no host sync"; gdevenyi's
-review comment on the same page hands the kernel "the chunk's unique ids (at
-most num_experts)".  Reading: length min(R, E), ascending, padded at the
+form a sorted list whose length is fixed in advance, so the host never waits
+to learn it; gdevenyi's review comment on the same page dedups the ids
+first, which bounds them by num_experts.  Reading: length min(R, E), ascending, padded at the
 tail with -1; ids outside [0, E) are not experts and are dropped.
 """
 from __future__ import annotations

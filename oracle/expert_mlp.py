@@ -1,8 +1,8 @@
 """SwiGLU expert MLP over decoded expert rows, and the top-k combine.
 
-Test infrastructure only.  The pages name the step -- "the same grouped GEMM
-over its layer's slot pool at their slots" (FreeToken PR #676, Solution) --
-but not its formula; the workloads fix "SwiGLU experts".  Readings:
+Test infrastructure only.  The pages name the step (FreeToken PR #676,
+Solution: the decode GEMM reused over the slot pool, each expert at its
+slot) but not its formula; the workloads fix SwiGLU experts.  Readings:
   * an expert row holds w13 = [gate; up] stacked along the output axis
     (rows 0..I-1 gate, rows I..2I-1 up) and w2 [H, I];
   * y = w2 @ (silu(gate @ x) * (up @ x)), silu(g) = g / (1 + exp(-g));

@@ -1,10 +1,10 @@
 """The whole MoE layer forward: over the slot cache, and streamed.
 
 Test infrastructure only.  FreeToken PR #676, Solution: a short prefill
-chunk "loads the experts it routes to into the slot cache, as decode does,
-and runs the same grouped GEMM over its layer's slot pool at their slots, so
-its output is bit-identical to the streamed layer's"; the streamed path
-copies every expert of the layer (Problem).  Slot path, in the pages' order:
+chunk brings only its routed experts into the slot cache, the way decode
+does, then reuses the decode GEMM with each expert read at its slot, and
+must give exactly the streamed layer's bytes; the streamed path moves all of
+the layer's experts (Problem).  Slot path, in the pages' order:
 route -> distinct experts -> queries of at most `query_width` keys, each
 query ensured and its misses copied before the next -> expert->slot remap
 (vLLM fork PR #48, What: physical-row remap) -> align -> expert MLP reading
@@ -56,9 +56,9 @@ def forward_slots(cfg, router_in, source_row, cache, pool, block, layer=None,
     """source_row(layer, e) -> host source row bytes; cache: SlotCache;
     pool: dict slot -> row bytes (updated by the copies).
 
-    A layer must never route to more experts than the pool holds (FreeToken
-    PR #676, the author's reply; gdevenyi fork PR #68 sends such a layer down
-    the whole-layer path).  The bound known before routing is min(R, E): a
+    The pool must hold all of the chunk's experts at once (FreeToken PR
+    #676, the author's reply; gdevenyi fork PR #68 streams a layer that
+    needs too much of the cache).  The bound known before routing is min(R, E): a
     chunk with min(R, E) > S is refused here and takes the streamed path.
     """
     layer = cfg.layer if layer is None else layer

@@ -1,13 +1,13 @@
 """LRU slot cache with an explicit recency list: the ensure step.
 
 Test infrastructure only.  Sources:
-  * FreeToken PR #676, Solution: the cache is handed the chunk's distinct
-    experts 128 at a time and each query's misses are copied before the next
-    query evicts; the admissions stay out of the decode-frequency counts and
-    the LRU statistics.
-  * The author's reply on that page: the cache is LRU only; earlier queries
-    need no pin because LRU evicts them last, and a layer never routes to
-    more experts than the cache holds.
+  * FreeToken PR #676, Solution: the chunk's distinct experts reach the
+    cache in queries of at most 128; a query's misses are copied before the
+    following query may evict; a prefill's admissions change neither the
+    decode-frequency counts nor the LRU statistics.
+  * The author's reply on that page: LRU only; an earlier query's slots need
+    no pin, since LRU takes them last and the pool is at least as large as
+    the set of experts a layer routes to.
   * vLLM fork PR #48, What: one bank shared by all layers, keyed by
     (layer, expert).
 

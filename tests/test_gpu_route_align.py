@@ -110,8 +110,8 @@ def test_align_workload_sizes(cfg):
 @pytest.mark.parametrize("E", list(C5B.Es) + [1024, 4096])
 def test_align_past_1024_experts(E):
     """FreeToken PR #676, Tests: 8192 tokens x top-8 uniformly routed at 1023
-    and 2100 experts, block 64: every route lands once, in a block of its
-    expert -- here bit-exact against the oracle."""
+    and 2100 experts, block 64: each route exactly once, inside a block of
+    its own expert -- here bit-exact against the oracle."""
     lib()
     ids = uniform_routes(C5B.T, C5B.k, E, C5B.seed)
     s, b, n, st = gpu_align(ids, E, C5B.block)

@@ -20,7 +20,7 @@ def test_hand_cases():
 
 
 def check_align_invariants(ids, E, B, s, b, n):
-    """Every valid route exactly once, in a block of its own expert, in
+    """Every valid route exactly once, inside a block of its own expert, in
     ascending route order; blocks padded with R; nothing past n_post_pad."""
     R = ids.size
     assert n % B == 0
@@ -70,8 +70,8 @@ def test_random_small_against_stable_sort(seed):
 
 @pytest.mark.parametrize("E", [1023, 1024, 2100])
 def test_past_1024_experts(E):
-    """FreeToken PR #676, Tests: at 1023 and 2100 experts every route lands
-    once, in a block of its expert (smaller than the sweep's 8192 x 8 to keep
+    """FreeToken PR #676, Tests: at 1023 and 2100 experts each route sits
+    exactly once in a block of its own expert (smaller than the sweep's 8192 x 8 to keep
     the CPU suite short; the GPU tests run the full size)."""
     ids = uniform_routes(512, 8, E, seed=1006)
     s, b, n, _ = moe_align_block_size(ids, E, 64)

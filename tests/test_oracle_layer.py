@@ -4,9 +4,9 @@
   give out[t] = (sum_j w[t, j] * 2^ids[t, j]) * MLP(x[t]); a route sent to
   the wrong expert, the wrong token or the wrong weight breaks it.
 * The slot path equals the streamed path (FreeToken PR #676, Solution).
-* A chunk routing to 160 experts admits them in queries of 128 and 32,
-  copies each query's misses, and records no statistic (FreeToken PR #676,
-  Tests).
+* 160 distinct experts go in as two queries (128, then 32), the copies of
+  each landing before the next, with no statistic recorded (FreeToken PR
+  #676, Tests).
 * Resident rows the chunk does not evict are untouched (vLLM fork PR #51,
   Tests: "resident rows untouched").
 """
