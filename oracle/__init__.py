@@ -17,6 +17,7 @@ loops where the steps are sequential, one function per step of the path:
   numerics.py     bf16, e2m1 and e4m3 decoding from their definitions
   expert_mlp.py   SwiGLU expert MLP over decoded weights, and the combine
   layer.py        the whole slot path and the whole-layer streamed path
+  stage.py        prefill staging: non-resident runs, staged row reads
 
 Sources (page title, section):
   FreeToken PR #676 "--moe-prefill-demand-tokens": Solution, Tests, Known
