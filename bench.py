@@ -552,6 +552,125 @@ def sweep(args):
                           "bytes": b, "GB/s": b / ms / 1e6, "hbm_frac": b / ms / 1e6 / hbm}))
 
 
+def crossover(args):
+    """Slot path vs staged whole-layer path over a sequence of layers, per
+    chunk size: where on-demand loading stops paying (FreeToken PR #676,
+    A/B and Known limits; vLLM fork PR #51, Details).  Per chunk size T and
+    routing, milliseconds per layer over `n_layers` layers for
+      slots      moe_layer_forward_slots per layer (no admission stats), the
+                 pool restored to its pre-fill first;
+      staged     oes_stage_plan_create (skip resident; one map readback)
+                 + moe_layers_forward_staged (next layer copied during this
+                 layer's compute) + destroy;
+      streamed   the whole layer copied into the staging rows (no skip),
+                 with the same prefetch;
+      serial     moe_layer_forward_stream per layer (copy, then compute).
+    The pool is pre-filled to every slot with seeded keys of all layers, as
+    decode would leave it.  One JSON line per (routing, T); not the headline."""
+    import torch
+    from offloaded_expert_slot_gb300 import build, oes
+    from offloaded_expert_slot_gb300.configs import scaled
+    from offloaded_expert_slot_gb300.inputs import (empty_slot_row, expert_layer_rows,
+                                                    n_source_buffers, pool_prefill,
+                                                    router_inputs, source_layer_index)
+    build.build()
+    oes.load()
+    base = CONFIGS[args.config]
+    if base.wfmt == "bf16":
+        base = scaled(base, L=8, distinct_source_layers=2)
+    base = scaled(base, prefill=base.S)
+    n_layers = min(8, base.L)
+    E, S, rb = base.E, base.S, base.row_bytes
+    srcs = []
+    for l in range(n_source_buffers(base)):
+        buf = torch.empty((E, rb), dtype=torch.uint8, pin_memory=True)
+        expert_layer_rows(base, l, device="cuda", out=buf)
+        srcs.append(buf)
+    src = oes.oes_expert_source_create([srcs[source_layer_index(base, l)] for l in range(base.L)],
+                                       E, rb)
+    pool_all = torch.empty((S + 2 * E, rb), dtype=torch.uint8, device="cuda")
+    pool = pool_all[:S]
+    cache = oes.slot_cache_create(S, base.L, E)
+    st = pool_prefill(base)
+    oes.slot_cache_load_state(cache, st["slot_key"], st["slot_ts"], st["clock"])
+    pool[:] = torch.from_numpy(empty_slot_row(base)).cuda()
+    for s_ in np.nonzero(st["slot_key"] >= 0)[0]:
+        k_ = int(st["slot_key"][s_])
+        pool[int(s_)].copy_(srcs[source_layer_index(base, k_ // E)][k_ % E])
+    snap = torch.empty(oes.slot_cache_state_bytes(cache), dtype=torch.uint8, device="cuda")
+    oes.slot_cache_snapshot(cache, snap)
+    layer_buf = pool_all[S:S + E]
+    wfmt = oes.OES_WFMT_BF16 if base.wfmt == "bf16" else oes.OES_WFMT_NVFP4
+    desc = oes.layer_desc(E, base.H, base.I, wfmt)
+    copy_stream = torch.cuda.Stream()
+    layers = list(range(n_layers))
+    link = None
+    for routing in ("normal", "normal+zipf"):
+        best = []
+        for T in (8, 16, 32, 64, 128, 256, 384, 512, 768, 1024):
+            cfg = scaled(base, T=T, logits=routing, zipf_s=1.1 if routing != "normal" else 0.0)
+            rin = router_inputs(cfg)
+            x = torch.from_numpy(rin["x"].view(np.int16)).cuda()
+            logits = torch.from_numpy(rin["logits"]).cuda()
+            wsb = oes.moe_layer_workspace_size(desc, T, cfg.k)
+            ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+            out = torch.empty((T, cfg.H), dtype=torch.bfloat16, device="cuda")
+            status = torch.zeros(1, dtype=torch.int32, device="cuda")
+            ch = oes.chunk(x, T, cfg.k, out, status, ws, wsb, logits=logits)
+
+            def slots():
+                oes.slot_cache_restore(cache, snap)
+                for l in layers:
+                    oes.moe_layer_forward_slots(cache, src, pool, l, desc, ch, 0)
+
+            def staged(skip):
+                def run():
+                    oes.slot_cache_restore(cache, snap)
+                    plan = oes.oes_stage_plan_create(cache, layers, skip)
+                    oes.moe_layers_forward_staged(plan, src, pool_all, desc, [ch] * n_layers,
+                                                  copy_stream=copy_stream)
+                    oes.oes_stage_plan_destroy(plan)
+                return run
+
+            def serial():
+                for l in layers:
+                    oes.moe_layer_forward_stream(src, layer_buf, l, desc, ch,
+                                                 copy_stream=copy_stream)
+
+            def timed(fn, steps=3):
+                fn()
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(steps):
+                    fn()
+                e1.record()
+                torch.cuda.synchronize()
+                return e0.elapsed_time(e1) / steps / n_layers
+
+            row = {"crossover": base.wfmt, "routing": routing, "T": T, "k": cfg.k, "E": E,
+                   "S": S, "n_layers": n_layers,
+                   "ms_per_layer": {"slots": timed(slots), "staged": timed(staged(True)),
+                                    "streamed": timed(staged(False)), "serial": timed(serial)}}
+            assert int(status.item()) == 0
+            slots()                                  # the distinct count of the chunk
+            torch.cuda.synchronize()
+            off = oes.moe_layer_workspace_views(desc, T, cfg.k, ws)["d_count"] - ws.data_ptr()
+            row["distinct_experts"] = int(ws[off:off + 4].view(torch.int32).item())
+            row["layer_bytes"] = E * rb
+            m = row["ms_per_layer"]
+            row["faster"] = "slots" if m["slots"] < min(m["staged"], m["streamed"]) else "staged"
+            best.append((T, row["faster"]))
+            print(json.dumps(row), flush=True)
+            del x, logits, ws, out
+        cross = next((T for T, f in best if f != "slots"), None)
+        print(json.dumps({"crossover_summary": base.wfmt, "routing": routing,
+                          "first_T_where_staging_wins": cross}), flush=True)
+    oes.slot_cache_destroy(cache)
+    oes.oes_expert_source_destroy(src)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -561,7 +680,12 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(CONFIGS))
     ap.add_argument("--sweep", action="store_true",
                     help="bandwidth sweep of the routing and align kernels (not the headline)")
+    ap.add_argument("--crossover", action="store_true",
+                    help="slot path vs staged whole-layer path per chunk size (not the headline)")
     args = ap.parse_args()
+    if args.crossover:
+        crossover(args)
+        return
     if args.sweep:
         sweep(args)
         return

@@ -9,7 +9,7 @@
  * next query evicts; routes are sorted into per-expert blocks
  * (moe_align_block_size); the grouped SwiGLU expert GEMM runs over the slot
  * pool through an expert->slot remap with its tiles sized by the layer's
- * expert count, so its output is bit-identical to the same GEMM over the
+ * expert count, and it gives exactly the bytes the same GEMM gives over the
  * whole streamed layer.
  *
  * Conventions for every call:
@@ -97,8 +97,8 @@ int moe_route_topk(const float *logits, int T, int E, int k, int32_t *ids, float
                    oes_stream_t stream);
 
 /* The chunk's distinct experts as a sorted list of fixed length (FreeToken
- * PR #676, Solution: "a sorted list of fixed length, so there is no host
- * sync").  distinct: device [min(R, E)] int32, ascending, padded at the tail
+ * PR #676, Solution: the list's length does not depend on the routing, so
+ * the host never waits on the device to size it).  distinct: device [min(R, E)] int32, ascending, padded at the tail
  * with -1; d_count: device [1] int32 = number of distinct experts.  ids out
  * of [0, E) are ignored.  ids: device [R] int32, R >= 0. */
 int moe_distinct_experts(const int32_t *ids, int R, int E, int32_t *distinct, int32_t *d_count,
@@ -148,8 +148,8 @@ int slot_cache_restore(oes_slot_cache *cache, const void *src, oes_stream_t stre
  * What: "physical-row remap").  Valid until slot_cache_destroy. */
 int slot_cache_layer_map(const oes_slot_cache *cache, int layer, const int32_t **e2s);
 
-/* One LRU ensure query (FreeToken PR #676, Solution: lru_ensure is handed
- * the chunk's distinct experts 128 at a time; the author's reply: LRU only).
+/* One LRU ensure query (FreeToken PR #676, Solution: the distinct experts
+ * go to lru_ensure in queries of at most 128; the author's reply: LRU only).
  * experts: device [n] int32, the query's experts of `layer`, strictly
  * ascending, -1 entries ignored; n <= OES_QUERY_MAX.
  * Effect: one clock tick; every hit slot and every filled slot gets the new
@@ -159,8 +159,9 @@ int slot_cache_layer_map(const oes_slot_cache *cache, int layer, const int32_t *
  * miss: device [3 * OES_QUERY_MAX] int32, entry i = (key, slot, evicted key
  * or -1) for i < *n_miss; n_miss: device [1] int32.
  * record_stats = 0 (demand admission): hits / misses / evictions /
- * decode_freq are not touched (FreeToken PR #676, Solution: "the admissions
- * stay out of collect_decode_freq and the LRU stats"); 1: they grow, and
+ * decode_freq are not touched (FreeToken PR #676, Solution: a prefill's
+ * admissions count neither as decode frequency nor in the LRU stats); 1:
+ * they grow, and
  * decode_freq[key] += 1 for every key of the query.
  * Device status: OES_DEV_BAD_ID (id out of range or not ascending) or
  * OES_DEV_CAPACITY (more misses than non-hit slots): nothing changes and
@@ -179,9 +180,9 @@ int oes_expert_source_create(const void *const *layer_base, int L, int E, int64_
 int oes_expert_source_destroy(oes_expert_source *src);
 
 /* Copies each miss of one query from the host source into its slot
- * (FreeToken PR #676, Solution: "copies each query's misses before the next
- * query evicts"; vLLM fork PR #48, What: "row copies are fixed-grid kernels
- * from the host source's accelerator view").  For i < *n_miss (read on the
+ * (FreeToken PR #676, Solution: a query's misses land before the following
+ * query may evict anything; vLLM fork PR #48, What: the rows move by a
+ * kernel with a fixed grid that reads the mapped host memory directly).  For i < *n_miss (read on the
  * device; at most max_misses): pool[slot] <- source row of key, the whole
  * row (weights, scales and per-expert scalars).  pool: device [S, row_bytes]
  * with the source's row_bytes.  Rows not named by the miss list are not
@@ -198,7 +199,8 @@ int oes_copy_layer(const oes_expert_source *src, int layer, void *dst, oes_strea
 /* ------------------------------------------------------------------ align */
 
 /* moe_align_block_size (FreeToken PR #676, Solution and Tests: correct past
- * 1024 experts, "every route lands once, in a block of its expert"; vLLM
+ * 1024 experts, each route placed exactly once and only in one of its own
+ * expert's blocks; vLLM
  * fork PR #48, What: logical alignment, ignore_invalid_experts).  A stable
  * counting sort of routes r = 0..R-1 by expert ids[r]:
  *   sorted_ids: device [OES_ALIGN_CAPACITY(R, E, B)] int32: experts in
@@ -244,8 +246,8 @@ int moe_align_block_size_noalloc(const int32_t *ids, int R, int E, int B, int ig
 /* ------------------------------------------------------------ expert GEMM */
 
 /* The experts a chunk routes to, as the grouped GEMM sees them (FreeToken
- * PR #676, Solution: "RoutedExperts" carries the layer's expert count and
- * input scales beside the slot range).  E is the LAYER's expert count and
+ * PR #676, Solution: RoutedExperts; the view knows both the slot pool and
+ * the layer, whose expert count and input scales it takes).  E is the LAYER's expert count and
  * alone sizes the tiles; S is only the pool's extent.
  * Expert row layout (row_bytes each, one per slot):
  *   bf16:  w13 [2I, H] bf16 (rows 0..I-1 gate, I..2I-1 up), w2 [H, I] bf16;
@@ -267,18 +269,20 @@ typedef struct {
   const float *input_scale2;  /* device [E] or NULL: the layer's w2 input scales */
 } oes_routed_experts;
 
-/* Tile plan (FreeToken PR #676, Solution: tiles from tokens per expert of
- * the layer, nvfp4_moe.prefill_config): the block size B shared by
- * moe_align_block_size and the GEMM, a function of R and the layer's E only:
- * 16, 32, 64 or 128, the smallest not below ceil(R / E). */
+/* Tile plan (FreeToken PR #676, Solution: nvfp4_moe.prefill_config sizes
+ * the tiles by routes per expert of the layer, never per slot): the block
+ * size B shared by moe_align_block_size and the GEMM, a function of R and
+ * the layer's E only: 16 when ceil(R / E) <= 8 (the weight-major kernel,
+ * 128 weight rows x 16 routes per MMA), else 128 (the token-major kernel,
+ * 128 routes x 256 weight rows per MMA). */
 int oes_tile_plan(int R, int E, int *block);
 
 /* Workspace bytes of moe_grouped_gemm_slots for T tokens at top-k. */
 size_t moe_grouped_gemm_workspace_size(const oes_routed_experts *view, int T, int k);
 
 /* The grouped SwiGLU expert GEMM over the slot pool (FreeToken PR #676,
- * Solution: "runs the same grouped GEMM over its layer's slot pool at their
- * slots, so its output is bit-identical to the streamed layer's").  For
+ * Solution: a demand chunk reuses the decode GEMM, reading each expert at
+ * its slot, and must match the streamed layer byte for byte).  For
  * every block b < n_post_pad / B of expert e = block_expert[b], with
  * weights at slot e2s[e]:
  *   h = silu(x_r @ gate^T) * (x_r @ up^T), y_r = h @ w2^T    (fp32 sums)
@@ -336,12 +340,18 @@ int moe_layer_workspace_views(const oes_layer_desc *layer, int T, int k, void *w
 
 /* The slot path, stream-ordered on `stream` with no host synchronisation
  * (FreeToken PR #676, Solution): route (or gate logits + route) -> distinct
- * experts -> for each query of OES_QUERY_MAX distinct experts: ensure
- * (record_stats as given) then copy its misses -> align -> grouped GEMM
- * over `pool` through the layer's remap.  The number of queries is
- * ceil(min(T*k, E) / OES_QUERY_MAX), known on the host.
- * A layer must never route to more experts than the cache holds (the
- * author's reply on FreeToken PR #676): with min(T*k, E) > S this returns
+ * experts -> the queries of OES_QUERY_MAX distinct experts, each ensured
+ * (record_stats as given) in order -> align -> grouped GEMM over `pool`
+ * through the layer's remap: the experts that were hits run at once on the
+ * cache's side stream while each query's misses are copied, in query order,
+ * on `stream`; the copied experts run after their copies.  The number of
+ * queries is ceil(min(T*k, E) / OES_QUERY_MAX), known on the host.  All
+ * ensures go before the copies: ensure reads no pool bytes, and with the
+ * chunk fitting the pool no query evicts a slot an earlier query touched,
+ * so the tables, the slots written and the bytes are those of ensuring and
+ * copying query by query.
+ * The pool must hold every expert the chunk needs at once (the author's
+ * reply on FreeToken PR #676): with min(T*k, E) > S this returns
  * OES_ERR_CAPACITY and launches nothing; the caller streams the layer. */
 int moe_layer_forward_slots(oes_slot_cache *cache, const oes_expert_source *src, void *pool,
                             int layer, const oes_layer_desc *desc, const oes_chunk *chunk,
@@ -352,10 +362,81 @@ int moe_layer_forward_slots(oes_slot_cache *cache, const oes_expert_source *src,
  * chunk): copy all E rows of `layer` into layer_buf (device [E, row_bytes])
  * on copy_stream, route and align on compute_stream meanwhile, then run the
  * same grouped GEMM over layer_buf with the identity remap once the copy is
- * done.  copy_stream may equal compute_stream. */
+ * done.  The copy waits for the work queued on compute_stream before the
+ * call (an earlier GEMM over the same buffer).  copy_stream may equal
+ * compute_stream. */
 int moe_layer_forward_stream(const oes_expert_source *src, void *layer_buf, int layer,
                              const oes_layer_desc *desc, const oes_chunk *chunk,
                              oes_stream_t copy_stream, oes_stream_t compute_stream);
+
+/* Demand-token dispatch (FreeToken PR #676, Solution and Tests).  A
+ * threshold N (0 = off, the default) sends prefill chunks of up to N tokens
+ * through the slot cache as decode does; longer chunks stream the whole
+ * layer.  Returns 1 when a chunk of T tokens at top-k over E experts takes the
+ * slot path of an S-slot pool: 0 < T <= demand_tokens and min(T*k, E) <= S
+ * (a chunk needing more distinct experts than the pool holds streams, since a
+ * later query would evict a slot the chunk still reads); else 0.  Host only,
+ * no CUDA call. */
+int oes_takes_slot_path(int T, int k, int E, int S, int demand_tokens);
+
+/* One layer forward with the demand-token dispatch: the slot path
+ * (moe_layer_forward_slots on `stream`) when oes_takes_slot_path() says so,
+ * else the whole-layer streamed path (moe_layer_forward_stream, copying on
+ * copy_stream into layer_buf).  *took_slots (host, may be NULL) reports the
+ * choice.  Both paths give the same bytes for the same chunk. */
+int moe_layer_forward(oes_slot_cache *cache, const oes_expert_source *src, void *pool,
+                      void *layer_buf, int layer, const oes_layer_desc *desc,
+                      const oes_chunk *chunk, int demand_tokens, int record_stats,
+                      oes_stream_t copy_stream, oes_stream_t stream, int *took_slots);
+
+/* ------------------------------------------------- staged layer sequence */
+
+/* Prefill staging over a sequence of layers (vLLM fork PR #51, Details,
+ * "Prefill staging"): two device buffers of one whole layer each alternate
+ * by layer; the rows of layer i+1 are copied by DMA on a copy stream while
+ * layer i computes, ordered by events; at the start of the step the
+ * placement tables are read back once and each layer's non-resident experts
+ * become contiguous runs.  Resident experts are read from their slots and
+ * their rows are never written.
+ *
+ * Pool layout for the staged runner: one allocation of S + 2E rows of
+ * row_bytes.  Rows 0..S-1 are the cache's slots; rows S + b*E + e
+ * (b = 0, 1) are staging buffer b, expert e at its own row, so one 3-D
+ * tensor map and one remap serve both kinds of expert and the GEMM is the
+ * very kernel of the slot and streamed paths.
+ *
+ * oes_stage_plan_create: layers host [n] (each in [0, L), repeats allowed).
+ * skip_resident = 1: an expert with a slot is read from it and not copied;
+ * 0: every expert of the layer is copied (the whole-layer stream, with
+ * prefetch).  Reads the cache's map back with one host synchronisation of
+ * `stream` (work queued there before the call is part of the placement the
+ * plan sees), allocates the plan's device remap [n][E] and its events.  The
+ * plan describes the cache as it is now: it is valid until the next call
+ * that changes the cache (ensure, load_state, restore). */
+typedef struct oes_stage_plan oes_stage_plan;
+int oes_stage_plan_create(const oes_slot_cache *cache, const int *layers, int n, int skip_resident,
+                          oes_stream_t stream, oes_stage_plan **out);
+int oes_stage_plan_destroy(oes_stage_plan *plan);
+
+/* Layer i of the plan: *n_runs runs [runs[2j], runs[2j+1]) of staged
+ * experts, ascending and maximal (runs: host [2*E] or NULL), *rows = the
+ * staged experts in all. */
+int oes_stage_plan_layer(const oes_stage_plan *plan, int i, int *n_runs, int32_t *runs, int *rows);
+
+/* Forwards the plan's n layers in order: layer i = plan layer i with chunk
+ * chunks[i] (host array [n]; chunks run one after another on
+ * compute_stream, so they may share x, out and workspace).  Per layer: DMA
+ * copies of the runs into staging buffer i % 2 on copy_stream (after the
+ * compute of layer i-2 released that buffer, and after all work queued on
+ * compute_stream before the call), then on compute_stream route -> align
+ * -> wait for the copies -> grouped GEMM -> combine, with the plan's remap.
+ * Each chunk's output equals moe_layer_forward_stream's for that layer and
+ * chunk, byte for byte.  pool: device [S + 2E, row_bytes] as above.  The
+ * plan's events order the copies, so one plan feeds one runner at a time;
+ * oes_stage_plan_destroy waits for the last runner's compute to finish. */
+int moe_layers_forward_staged(const oes_stage_plan *plan, const oes_expert_source *src, void *pool,
+                              const oes_layer_desc *desc, const oes_chunk *chunks,
+                              oes_stream_t copy_stream, oes_stream_t compute_stream);
 
 #ifdef __cplusplus
 }

@@ -1,9 +1,9 @@
 // The grouped SwiGLU expert GEMM over the slot pool, on tcgen05 / TMEM / TMA.
 //
-// FreeToken PR #676, Solution: the chunk "runs the same grouped GEMM over
-// its layer's slot pool at their slots, so its output is bit-identical to
-// the streamed layer's"; the expert view carries the layer's expert count
-// and the NVFP4 prefill sizes its tiles by tokens per expert of the layer.
+// FreeToken PR #676, Solution: a demand chunk reuses the decode GEMM, each
+// expert read at its slot, and must give the streamed layer's bytes exactly;
+// the expert view knows the layer's expert count, and the NVFP4 prefill
+// takes its tiles from routes per expert of the layer, not of the pool.
 // vLLM fork PR #48, What: logical alignment plus a physical-row remap.
 //
 // Design (swap-AB): the weight rows of an expert are the MMA's M side (128
@@ -89,11 +89,7 @@ __device__ __forceinline__ Unit unit_info(const GemmParams& p, int u, int nb) {
   t.m = u % p.n_mtiles;
   const int e = p.block_expert[t.b];
   const bool valid_e = e >= 0 && e < p.E;
-  bool filtered = false;
-  if (p.filter && valid_e) {
-    const bool resident = p.flags[e] != 0;
-    filtered = (p.filter == 1) ? !resident : resident;
-  }
+  const bool filtered = p.filter && valid_e && p.flags[e] != p.filter;
   t.slot = filtered ? kFiltered : (valid_e ? p.e2s[e] : -1);
   const int32_t* s = p.sorted_ids + (int64_t)t.b * p.BN;
   if (s[p.BN - 1] < p.R) {
@@ -1152,7 +1148,8 @@ int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
   return OES_OK;
 }
 
-// GEMM1 then GEMM2 over the blocks `filter` selects (flags: device [E]).
+// GEMM1 then GEMM2 over the blocks `filter` selects (flags: device [E]
+// group of each expert; filter 0 = every block).
 int gemm_run(const GemmPlan& g, int filter, const uint8_t* flags, cudaStream_t stream) {
   if (g.empty) return OES_OK;
   GemmParams p1 = g.p1, p2 = g.p2;

@@ -22,8 +22,8 @@ struct GemmParams {
   const int32_t* block_expert;
   const int32_t* n_post_pad;
   const int32_t* e2s;
-  const uint8_t* flags;  // [E] 1 = expert resident before the chunk (filtered launches)
-  int filter;            // 0 all blocks; 1 resident experts only; 2 the others only
+  const uint8_t* flags;  // [E] group of each expert (filtered launches)
+  int filter;            // 0 all blocks; g > 0 the blocks of experts with flags[e] == g
   const uint8_t* pool;
   int64_t row_bytes;
   int64_t scal_off;  // NVFP4: byte offset of the fp32 scalars in a row
@@ -50,7 +50,7 @@ int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
                  const int32_t* sorted_ids, const int32_t* block_expert, const int32_t* n_post_pad,
                  int B, void* workspace, size_t workspace_bytes, int32_t* status, cudaStream_t stream,
                  GemmPlan* plan);
-// filter: 0 every block; 1 blocks of experts with flags[e] != 0; 2 the others
+// filter: 0 every block; g > 0 the blocks of experts with flags[e] == g
 int gemm_run(const GemmPlan& plan, int filter, const uint8_t* flags, cudaStream_t stream);
 int gemm_combine(const GemmPlan& plan, const int32_t* ids, const float* weights, uint16_t* out,
                  cudaStream_t stream);

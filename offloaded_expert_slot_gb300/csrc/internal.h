@@ -18,10 +18,13 @@ struct oes_slot_cache {
   int64_t* slot_ts;      // [S] timestamp of the last query that touched the slot, 0 if empty
   int64_t* ctr;          // [4] clock, hits, misses, evictions
   int64_t* decode_freq;  // [L*E]
-  // side stream and events of moe_layer_forward_slots: the GEMM over experts
-  // resident before the chunk runs there while the misses are copied
+  // side stream and events of moe_layer_forward_slots: the later queries'
+  // ensures and every GEMM run there while the misses are copied on the
+  // caller's stream; ensured[q] / copied[q] mark query q's ensure and copies
+  static constexpr int kMaxQueries = OES_MAX_EXPERTS / OES_QUERY_MAX;
   cudaStream_t side;
   cudaEvent_t fork, join;
+  cudaEvent_t ensured[kMaxQueries], copied[kMaxQueries];
 };
 
 struct oes_expert_source {

@@ -1,12 +1,14 @@
 // The whole-layer composites: the slot path and the streamed path, each a
 // stream-ordered sequence of the library's own calls with no host sync.
 //
-// FreeToken PR #676, Solution: a prefill chunk loads the experts it routes
-// to into the slot cache, in queries of 128 distinct experts, each query's
-// misses copied before the next, then runs the same grouped GEMM over the
-// slot pool at their slots; Problem: the streamed path copies every expert
-// of the layer for the chunk.
+// FreeToken PR #676, Solution: a short prefill chunk fills the slot cache
+// with just its routed experts, 128 distinct experts per query with every
+// query's copies done before the next query, and then reuses the decode
+// GEMM over the slots; Problem: streaming moves all of the layer's experts
+// for every chunk.
 #include <algorithm>
+#include <utility>
+#include <vector>
 
 #include "common.cuh"
 #include "gemm_types.h"
@@ -53,8 +55,9 @@ LayerWs carve_layer(void* base, const oes_layer_desc* d, int T, int k) {
   w.w = static_cast<float*>(take((size_t)R * 4));
   w.distinct = static_cast<int32_t*>(take((size_t)std::max(1, std::min(R, E)) * 4));
   w.d_count = static_cast<int32_t*>(take(4));
-  w.miss = static_cast<int32_t*>(take(3 * OES_QUERY_MAX * 4));
-  w.n_miss = static_cast<int32_t*>(take(4));
+  const int Q = std::max(1, (std::min(R, E) + OES_QUERY_MAX - 1) / OES_QUERY_MAX);
+  w.miss = static_cast<int32_t*>(take((size_t)Q * 3 * OES_QUERY_MAX * 4));
+  w.n_miss = static_cast<int32_t*>(take((size_t)Q * 4));
   w.sorted_ids = static_cast<int32_t*>(take((size_t)std::max<int64_t>(cap, 1) * 4));
   w.block_expert = static_cast<int32_t*>(take((size_t)std::max<int64_t>(cap / B, 1) * 4));
   w.n_post_pad = static_cast<int32_t*>(take(4));
@@ -73,17 +76,35 @@ LayerWs carve_layer(void* base, const oes_layer_desc* d, int T, int k) {
   return w;
 }
 
-// resident[e] = 1 for the chunk's experts that already have a slot.  Taken
-// before the first ensure: a layer never routes to more experts than the pool
-// holds, so no query of the chunk evicts a slot the chunk uses, and these
-// experts keep their slots (and bytes) through all of the chunk's queries.
-__global__ void resident_flags_kernel(const int32_t* __restrict__ distinct, int n, int E, int layer,
-                                      const int32_t* __restrict__ map, uint8_t* __restrict__ resident) {
-  for (int e = threadIdx.x; e < E; e += blockDim.x) resident[e] = 0;
+// group[e] of the chunk's experts, taken after every query of the chunk has
+// been ensured: kGroupHit for an expert that was a hit in its own query,
+// kGroupMiss0 + q for one that query q missed (0 for experts not in the
+// chunk).  A hit keeps its slot and bytes to the end of the chunk: its query
+// gives it a newer timestamp than any slot no query of the chunk has
+// touched, and since the pool holds all of the chunk's experts at once
+// (checked up front) every later query finds enough such older slots to
+// evict.  An expert resident before the chunk but belonging to a later query
+// has no such guarantee: an earlier query may evict it, and it is then a
+// miss of its own query like any other.
+constexpr int kGroupHit = 1, kGroupMiss0 = 2;
+
+__global__ void group_flags_kernel(const int32_t* __restrict__ distinct, int n, int E, int layer,
+                                   const int32_t* __restrict__ miss,
+                                   const int32_t* __restrict__ n_miss, int Q,
+                                   uint8_t* __restrict__ group) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) group[e] = 0;
   __syncthreads();
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const int e = distinct[i];
-    if (e >= 0 && e < E) resident[e] = map[(int64_t)layer * E + e] >= 0 ? 1 : 0;
+    if (e >= 0 && e < E) group[e] = kGroupHit;
+  }
+  __syncthreads();
+  for (int q = 0; q < Q; ++q) {
+    const int m = min(n_miss[q], OES_QUERY_MAX);
+    for (int i = threadIdx.x; i < m; i += blockDim.x) {
+      const int e = miss[(q * OES_QUERY_MAX + i) * 3] - layer * E;
+      if (e >= 0 && e < E) group[e] = (uint8_t)(kGroupMiss0 + q);
+    }
   }
 }
 
@@ -160,13 +181,38 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
   if (T == 0) return OES_OK;
   const LayerWs w = carve_layer(c->workspace, d, T, k);
   const int B = tile_plan(R, E);
+  const int Lq = std::min(R, E);
+  const int Q = (Lq + OES_QUERY_MAX - 1) / OES_QUERY_MAX;
+  cudaStream_t side = cache->side;
+  auto miss_of = [&](int q) { return w.miss + (size_t)q * 3 * OES_QUERY_MAX; };
+  auto query = [&](int q, cudaStream_t s) {
+    const int n = std::min(OES_QUERY_MAX, Lq - q * OES_QUERY_MAX);
+    return slot_cache_ensure(cache, layer, w.distinct + q * OES_QUERY_MAX, n, record_stats,
+                             miss_of(q), w.n_miss + q, c->status, s);
+  };
+  auto copy = [&](int q, cudaStream_t s) {
+    const int n = std::min(OES_QUERY_MAX, Lq - q * OES_QUERY_MAX);
+    return slot_cache_copy_misses(src, pool, cache->S, miss_of(q), w.n_miss + q, n, c->status, s);
+  };
+  // caller's stream: route, distinct experts, the first query
   if ((rc = route(d, c, w, stream))) return rc;
   if ((rc = moe_distinct_experts(w.ids, R, E, w.distinct, w.d_count, stream))) return rc;
-  const int Lq = std::min(R, E);
-  resident_flags_kernel<<<1, 1024, 0, stream>>>(w.distinct, Lq, E, layer, cache->map, w.resident);
-  OES_CHECK_LAUNCH("resident_flags_kernel");
+  if ((rc = query(0, stream))) return rc;
+  OES_TRY_CUDA(cudaEventRecord(cache->fork, stream));
+  // side stream: the later queries in order (ensure reads no pool bytes, and
+  // with the chunk fitting the pool no query evicts a slot an earlier query
+  // touched, so a query's copies may trail the later ensures), then the
+  // expert groups, the align and the GEMM over the hits
+  OES_TRY_CUDA(cudaStreamWaitEvent(side, cache->fork, 0));
+  for (int q = 1; q < Q; ++q) {
+    if ((rc = query(q, side))) return rc;
+    OES_TRY_CUDA(cudaEventRecord(cache->ensured[q], side));
+  }
+  group_flags_kernel<<<1, 1024, 0, side>>>(w.distinct, Lq, E, layer, w.miss, w.n_miss, Q,
+                                           w.resident);
+  OES_CHECK_LAUNCH("group_flags_kernel");
   if ((rc = moe_align_block_size(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad,
-                                 c->status, w.align_ws, w.align_bytes, stream)))
+                                 c->status, w.align_ws, w.align_bytes, side)))
     return rc;
   oes_routed_experts v{};
   v.layer = layer;
@@ -182,25 +228,22 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
   v.input_scale2 = d->input_scale2;
   GemmPlan g;
   if ((rc = gemm_prepare(&v, c->x, T, k, w.sorted_ids, w.block_expert, w.n_post_pad, B, w.gemm_ws,
-                         w.gemm_bytes, c->status, stream, &g)))
+                         w.gemm_bytes, c->status, side, &g)))
     return rc;
-  // side stream: the GEMM over the experts already resident, overlapping the
-  // copies of the misses on the caller's stream
-  OES_TRY_CUDA(cudaEventRecord(cache->fork, stream));
-  OES_TRY_CUDA(cudaStreamWaitEvent(cache->side, cache->fork, 0));
-  if ((rc = gemm_run(g, 1, w.resident, cache->side))) return rc;
-  OES_TRY_CUDA(cudaEventRecord(cache->join, cache->side));
-  // caller's stream: each query of at most OES_QUERY_MAX distinct experts is
-  // ensured and its misses copied before the next query
-  for (int q0 = 0; q0 < Lq; q0 += OES_QUERY_MAX) {
-    const int n = std::min(OES_QUERY_MAX, Lq - q0);
-    if ((rc = slot_cache_ensure(cache, layer, w.distinct + q0, n, record_stats, w.miss, w.n_miss,
-                                c->status, stream)))
-      return rc;
-    if ((rc = slot_cache_copy_misses(src, pool, cache->S, w.miss, w.n_miss, n, c->status, stream)))
-      return rc;
+  if ((rc = gemm_run(g, kGroupHit, w.resident, side))) return rc;
+  // caller's stream: each query's misses in query order, each query's copies
+  // after its own ensure; the side stream runs each query's copied experts
+  // once their copies are in
+  for (int q = 0; q < Q; ++q) {
+    if (q > 0) OES_TRY_CUDA(cudaStreamWaitEvent(stream, cache->ensured[q], 0));
+    if ((rc = copy(q, stream))) return rc;
+    OES_TRY_CUDA(cudaEventRecord(cache->copied[q], stream));
   }
-  if ((rc = gemm_run(g, 2, w.resident, stream))) return rc;   // the experts just copied
+  for (int q = 0; q < Q; ++q) {
+    OES_TRY_CUDA(cudaStreamWaitEvent(side, cache->copied[q], 0));
+    if ((rc = gemm_run(g, kGroupMiss0 + q, w.resident, side))) return rc;
+  }
+  OES_TRY_CUDA(cudaEventRecord(cache->join, side));
   OES_TRY_CUDA(cudaStreamWaitEvent(stream, cache->join, 0));
   return gemm_combine(g, w.ids, w.w, c->out, stream);
 }
@@ -216,8 +259,17 @@ extern "C" int moe_layer_forward_stream(const oes_expert_source* src, void* laye
   if (T == 0) return OES_OK;
   const LayerWs w = carve_layer(c->workspace, d, T, k);
   const int B = tile_plan(R, E);
-  if ((rc = oes_copy_layer(src, layer, layer_buf, copy_stream))) return rc;
   cudaEvent_t copied = nullptr;
+  if (copy_stream != compute_stream) {
+    // the copy overwrites layer_buf only after work queued earlier on
+    // compute_stream (a previous layer's GEMM over the same buffer) is done
+    cudaEvent_t entry = nullptr;
+    OES_TRY_CUDA(cudaEventCreateWithFlags(&entry, cudaEventDisableTiming));
+    OES_TRY_CUDA(cudaEventRecord(entry, compute_stream));
+    OES_TRY_CUDA(cudaStreamWaitEvent(copy_stream, entry, 0));
+    OES_TRY_CUDA(cudaEventDestroy(entry));
+  }
+  if ((rc = oes_copy_layer(src, layer, layer_buf, copy_stream))) return rc;
   if (copy_stream != compute_stream) {
     OES_TRY_CUDA(cudaEventCreateWithFlags(&copied, cudaEventDisableTiming));
     OES_TRY_CUDA(cudaEventRecord(copied, copy_stream));
@@ -247,4 +299,193 @@ extern "C" int moe_layer_forward_stream(const oes_expert_source* src, void* laye
   return moe_grouped_gemm_slots(&v, c->x, T, k, w.ids, w.w, w.sorted_ids, w.block_expert,
                                 w.n_post_pad, B, w.gemm_ws, w.gemm_bytes, c->out, c->status,
                                 compute_stream);
+}
+
+extern "C" int oes_takes_slot_path(int T, int k, int E, int S, int demand_tokens) {
+  if (T <= 0 || demand_tokens <= 0 || T > demand_tokens) return 0;
+  const int64_t R = (int64_t)T * k;
+  return (R < E ? R : E) <= S ? 1 : 0;
+}
+
+extern "C" int moe_layer_forward(oes_slot_cache* cache, const oes_expert_source* src, void* pool,
+                                 void* layer_buf, int layer, const oes_layer_desc* d,
+                                 const oes_chunk* c, int demand_tokens, int record_stats,
+                                 oes_stream_t copy_stream, oes_stream_t stream, int* took_slots) {
+  OES_REQUIRE(d && c && cache, "moe_layer_forward: null desc, chunk or cache");
+  const int slots = oes_takes_slot_path(c->T, c->k, d->E, cache->S, demand_tokens);
+  if (took_slots) *took_slots = slots;
+  if (slots) return moe_layer_forward_slots(cache, src, pool, layer, d, c, record_stats, stream);
+  return moe_layer_forward_stream(src, layer_buf, layer, d, c, copy_stream, stream);
+}
+
+// ------------------------------------------------------------------ staging
+// vLLM fork PR #51, Details ("Prefill staging"): whole-layer double buffer,
+// next-layer prefetch by DMA on a side stream, contiguous non-resident runs
+// from one placement readback per step.
+
+struct oes_stage_plan {
+  int n, S, L, E, device;
+  std::vector<int> layers;
+  std::vector<std::vector<std::pair<int, int>>> runs;  // [n] staged runs [e0, e1)
+  std::vector<int> rows;                               // [n] staged experts
+  int32_t* e2s;                                        // device [n][E]
+  cudaEvent_t entry, copied[2], done[2];
+};
+
+namespace {
+
+void destroy_plan(oes_stage_plan* p) {
+  if (!p) return;
+  cudaFree(p->e2s);
+  for (cudaEvent_t e : {p->entry, p->copied[0], p->copied[1], p->done[0], p->done[1]})
+    if (e) cudaEventDestroy(e);
+  delete p;
+}
+
+}  // namespace
+
+extern "C" int oes_stage_plan_create(const oes_slot_cache* cache, const int* layers, int n,
+                                     int skip_resident, oes_stream_t stream, oes_stage_plan** out) {
+  OES_REQUIRE(cache && layers && out, "oes_stage_plan_create: null pointer");
+  OES_REQUIRE(n >= 1 && n <= (1 << 16), "oes_stage_plan_create: bad layer count %d", n);
+  const int L = cache->L, E = cache->E, S = cache->S;
+  for (int i = 0; i < n; ++i)
+    OES_REQUIRE(layers[i] >= 0 && layers[i] < L, "oes_stage_plan_create: layer %d out of range",
+                layers[i]);
+  std::vector<int32_t> map;
+  if (skip_resident) {
+    map.resize((size_t)L * E);
+    OES_TRY_CUDA(cudaMemcpyAsync(map.data(), cache->map, map.size() * sizeof(int32_t),
+                                 cudaMemcpyDeviceToHost, stream));
+    OES_TRY_CUDA(cudaStreamSynchronize(stream));
+  }
+  auto* p = new oes_stage_plan();
+  p->n = n;
+  p->S = S;
+  p->L = L;
+  p->E = E;
+  p->device = cache->device;
+  p->layers.assign(layers, layers + n);
+  p->runs.resize(n);
+  p->rows.assign(n, 0);
+  std::vector<int32_t> e2s((size_t)n * E);
+  for (int i = 0; i < n; ++i) {
+    const int32_t* m = skip_resident ? map.data() + (size_t)layers[i] * E : nullptr;
+    const int32_t staged0 = S + (i & 1) * E;
+    int e = 0;
+    while (e < E) {
+      if (m && m[e] >= 0) {
+        e2s[(size_t)i * E + e] = m[e];
+        ++e;
+        continue;
+      }
+      const int e0 = e;
+      while (e < E && !(m && m[e] >= 0)) {
+        e2s[(size_t)i * E + e] = staged0 + e;
+        ++e;
+      }
+      p->runs[i].emplace_back(e0, e);
+      p->rows[i] += e - e0;
+    }
+  }
+  cudaError_t err = cudaMalloc(&p->e2s, e2s.size() * sizeof(int32_t));
+  if (err == cudaSuccess)
+    err = cudaMemcpy(p->e2s, e2s.data(), e2s.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+  if (err == cudaSuccess) err = cudaEventCreateWithFlags(&p->entry, cudaEventDisableTiming);
+  for (int b = 0; b < 2 && err == cudaSuccess; ++b) {
+    err = cudaEventCreateWithFlags(&p->copied[b], cudaEventDisableTiming);
+    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&p->done[b], cudaEventDisableTiming);
+  }
+  if (err != cudaSuccess) {
+    destroy_plan(p);
+    return cuda_fail(err, "oes_stage_plan_create");
+  }
+  *out = p;
+  return OES_OK;
+}
+
+extern "C" int oes_stage_plan_destroy(oes_stage_plan* p) {
+  if (!p) return OES_OK;
+  cudaError_t err = cudaEventSynchronize(p->done[0]);
+  if (err == cudaSuccess) err = cudaEventSynchronize(p->done[1]);
+  destroy_plan(p);
+  if (err != cudaSuccess) return cuda_fail(err, "oes_stage_plan_destroy");
+  return OES_OK;
+}
+
+extern "C" int oes_stage_plan_layer(const oes_stage_plan* p, int i, int* n_runs, int32_t* runs,
+                                    int* rows) {
+  OES_REQUIRE(p && i >= 0 && i < p->n, "oes_stage_plan_layer: bad plan or index");
+  const auto& r = p->runs[i];
+  if (n_runs) *n_runs = (int)r.size();
+  if (rows) *rows = p->rows[i];
+  if (runs)
+    for (size_t j = 0; j < r.size(); ++j) {
+      runs[2 * j] = r[j].first;
+      runs[2 * j + 1] = r[j].second;
+    }
+  return OES_OK;
+}
+
+extern "C" int moe_layers_forward_staged(const oes_stage_plan* p, const oes_expert_source* src,
+                                         void* pool, const oes_layer_desc* d,
+                                         const oes_chunk* chunks, oes_stream_t copy_stream,
+                                         oes_stream_t compute_stream) {
+  OES_REQUIRE(p && src && pool && d && chunks, "moe_layers_forward_staged: null pointer");
+  OES_REQUIRE(src->L == p->L && src->E == p->E && d->E == p->E,
+              "moe_layers_forward_staged: source, plan and layer disagree on L or E");
+  OES_REQUIRE(((uintptr_t)pool & 15) == 0, "moe_layers_forward_staged: pool not 16-byte aligned");
+  for (int i = 0; i < p->n; ++i) {
+    int rc = check_chunk(d, &chunks[i]);
+    if (rc) return rc;
+  }
+  const int E = p->E;
+  const int64_t rb = src->row_bytes;
+  uint8_t* base = static_cast<uint8_t*>(pool);
+  OES_TRY_CUDA(cudaEventRecord(p->entry, compute_stream));
+  OES_TRY_CUDA(cudaStreamWaitEvent(copy_stream, p->entry, 0));
+  for (int i = 0; i < p->n; ++i) {
+    const int b = i & 1, layer = p->layers[i];
+    const oes_chunk* c = &chunks[i];
+    // copy stream: this layer's runs into staging buffer b once layer i-2 let go of it
+    if (i >= 2) OES_TRY_CUDA(cudaStreamWaitEvent(copy_stream, p->done[b], 0));
+    const uint8_t* host = static_cast<const uint8_t*>(src->host_bases[layer]);
+    for (const auto& r : p->runs[i])
+      OES_TRY_CUDA(cudaMemcpyAsync(base + ((int64_t)p->S + (int64_t)b * E + r.first) * rb,
+                                   host + (int64_t)r.first * rb, (size_t)(r.second - r.first) * rb,
+                                   cudaMemcpyDefault, copy_stream));
+    OES_TRY_CUDA(cudaEventRecord(p->copied[b], copy_stream));
+    // compute stream: route and align overlap the copies; the GEMM waits for them
+    const int T = c->T, k = c->k, R = T * k;
+    if (T > 0) {
+      const LayerWs w = carve_layer(c->workspace, d, T, k);
+      const int B = tile_plan(R, E);
+      int rc = route(d, c, w, compute_stream);
+      if (!rc)
+        rc = moe_align_block_size(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad,
+                                  c->status, w.align_ws, w.align_bytes, compute_stream);
+      if (rc) return rc;
+      OES_TRY_CUDA(cudaStreamWaitEvent(compute_stream, p->copied[b], 0));
+      oes_routed_experts v{};
+      v.layer = layer;
+      v.E = E;
+      v.e2s = p->e2s + (size_t)i * E;
+      v.wfmt = d->wfmt;
+      v.pool = pool;
+      v.row_bytes = rb;
+      v.S = p->S + 2 * E;
+      v.H = d->H;
+      v.I = d->I;
+      v.input_scale13 = d->input_scale13;
+      v.input_scale2 = d->input_scale2;
+      rc = moe_grouped_gemm_slots(&v, c->x, T, k, w.ids, w.w, w.sorted_ids, w.block_expert,
+                                  w.n_post_pad, B, w.gemm_ws, w.gemm_bytes, c->out, c->status,
+                                  compute_stream);
+      if (rc) return rc;
+    } else {
+      OES_TRY_CUDA(cudaStreamWaitEvent(compute_stream, p->copied[b], 0));
+    }
+    OES_TRY_CUDA(cudaEventRecord(p->done[b], compute_stream));
+  }
+  return OES_OK;
 }

@@ -1,13 +1,13 @@
 // The LRU slot cache (tables in GPU memory, updated without a host sync),
 // the pinned-host expert source, and the miss-row copies.
 //
-// FreeToken PR #676, Solution: lru_ensure is handed the chunk's distinct
-// experts 128 at a time and each query's misses are copied before the next
-// query evicts; the admissions stay out of collect_decode_freq and the LRU
-// statistics.  The author's reply on that page: the cache is LRU only.
-// vLLM fork PR #48, What: one bank shared by all MoE layers, keyed by
-// (layer, expert); row copies are fixed-grid kernels reading the host
-// source through its accelerator view.
+// FreeToken PR #676, Solution: the distinct experts reach lru_ensure in
+// queries of at most 128, a query's misses land before the following query
+// may evict, and a prefill's admissions count neither as decode frequency
+// nor in the LRU statistics.  The author's reply on that page: LRU only.
+// vLLM fork PR #48, What: all MoE layers share one bank, keyed by
+// (layer, expert), and the rows move by a fixed-grid kernel that reads the
+// mapped host memory directly.
 #include <algorithm>
 #include <vector>
 
@@ -194,11 +194,17 @@ __global__ void __launch_bounds__(kEnsureThreads)
   }
 }
 
-constexpr int kCopyThreads = 512;
-constexpr int kCopyUnroll = 4;
+constexpr int kCopyThreads = 32;
+constexpr int kCopyUnroll = 8;
 
-// Fixed grid: work item = (miss i, 32 KB chunk of its row).  Each thread
-// moves 4 x 16 bytes per item: all four loads are issued before the stores.
+// Fixed grid of one warp per SM: work item = (miss i, 4 KB chunk of its
+// row).  Each lane moves 8 x 16 bytes per item, all eight loads issued
+// before the stores.  4 KB in flight per SM (0.6 MB over the GPU) keeps the
+// NVLink-C2C host link full (99% of a pinned DMA copy on a GB300), while
+// the kernels the slot path runs beside the copies (the later queries'
+// ensures, the GEMM over the hits) keep their speed: with 32 KB in flight
+// per SM their loads queued behind the copy's host reads and ran 4-10x
+// slower.
 __global__ void __launch_bounds__(kCopyThreads)
     copy_misses_kernel(const uint8_t* const* __restrict__ bases, int L, int E, int64_t row_bytes,
                        uint8_t* __restrict__ pool, int S, const int32_t* __restrict__ miss,
@@ -239,6 +245,21 @@ __global__ void __launch_bounds__(kCopyThreads)
 
 using namespace oes;
 
+// Frees whatever part of a cache handle exists (creation failures included).
+static int release_cache(oes_slot_cache* c) {
+  for (int q = 0; q < oes_slot_cache::kMaxQueries; ++q) {
+    if (c->ensured[q]) cudaEventDestroy(c->ensured[q]);
+    if (c->copied[q]) cudaEventDestroy(c->copied[q]);
+  }
+  if (c->join) cudaEventDestroy(c->join);
+  if (c->fork) cudaEventDestroy(c->fork);
+  if (c->side) cudaStreamDestroy(c->side);
+  cudaError_t e = c->block ? cudaFree(c->block) : cudaSuccess;
+  delete c;
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFree(slot cache tables)");
+  return OES_OK;
+}
+
 extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   OES_REQUIRE(out, "slot_cache_create: null out");
   OES_REQUIRE(S >= 1 && S <= OES_MAX_SLOTS, "slot_cache_create: S=%d out of [1, %d]", S,
@@ -255,19 +276,19 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   c->block_bytes = bytes;
   c->side = nullptr;
   c->fork = c->join = nullptr;
+  for (int q = 0; q < oes_slot_cache::kMaxQueries; ++q) c->ensured[q] = c->copied[q] = nullptr;
+  c->block = nullptr;
   cudaError_t e = cudaMalloc(&c->block, bytes);
-  if (e != cudaSuccess) {
-    delete c;
-    return cuda_fail(e, "cudaMalloc(slot cache tables)");
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->join, cudaEventDisableTiming);
+  for (int q = 0; q < oes_slot_cache::kMaxQueries && e == cudaSuccess; ++q) {
+    e = cudaEventCreateWithFlags(&c->ensured[q], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->copied[q], cudaEventDisableTiming);
   }
-  if ((e = cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking)) != cudaSuccess ||
-      (e = cudaEventCreateWithFlags(&c->fork, cudaEventDisableTiming)) != cudaSuccess ||
-      (e = cudaEventCreateWithFlags(&c->join, cudaEventDisableTiming)) != cudaSuccess) {
-    if (c->fork) cudaEventDestroy(c->fork);
-    if (c->side) cudaStreamDestroy(c->side);
-    cudaFree(c->block);
-    delete c;
-    return cuda_fail(e, "slot_cache_create: side stream / events");
+  if (e != cudaSuccess) {
+    release_cache(c);
+    return cuda_fail(e, "slot_cache_create: tables, side stream or events");
   }
   uint8_t* p = static_cast<uint8_t*>(c->block);
   c->slot_ts = reinterpret_cast<int64_t*>(p);
@@ -283,8 +304,7 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   std::vector<int64_t> ts(S, 0);
   int rc = slot_cache_load_state(c, key.data(), ts.data(), 0);
   if (rc != OES_OK) {
-    cudaFree(c->block);
-    delete c;
+    release_cache(c);
     return rc;
   }
   *out = c;
@@ -294,13 +314,7 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
 extern "C" int slot_cache_destroy(oes_slot_cache* c) {
   if (!c) return OES_OK;
   if (c->side) cudaStreamSynchronize(c->side);
-  if (c->join) cudaEventDestroy(c->join);
-  if (c->fork) cudaEventDestroy(c->fork);
-  if (c->side) cudaStreamDestroy(c->side);
-  cudaError_t e = cudaFree(c->block);
-  delete c;
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFree(slot cache tables)");
-  return OES_OK;
+  return release_cache(c);
 }
 
 extern "C" int slot_cache_load_state(oes_slot_cache* c, const int32_t* slot_key,
@@ -395,6 +409,12 @@ extern "C" int slot_cache_ensure(oes_slot_cache* c, int layer, const int32_t* ex
                                       (int)smem));
     configured_smem = smem;
   }
+  // the largest shared carveout, as for the copies (an ensure may run beside
+  // the copies and the GEMM)
+  static const cudaError_t carve = cudaFuncSetAttribute(
+      ensure_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+      cudaSharedmemCarveoutMaxShared);
+  OES_REQUIRE(carve == cudaSuccess, "slot_cache_ensure: carveout attribute failed");
   ensure_kernel<<<1, kEnsureThreads, smem, stream>>>(view_of(c), layer, experts, n, record_stats,
                                                      spad, miss, n_miss, status);
   OES_CHECK_LAUNCH("ensure_kernel");
@@ -445,7 +465,14 @@ extern "C" int slot_cache_copy_misses(const oes_expert_source* src, void* pool, 
               "slot_cache_copy_misses: bad S=%d max_misses=%d", S, max_misses);
   OES_REQUIRE(((uintptr_t)pool & 15) == 0, "slot_cache_copy_misses: pool not 16-byte aligned");
   if (max_misses == 0) return OES_OK;
-  const int grid = num_sms() * 2;
+  // the copies run beside kernels that need most of an SM's shared memory;
+  // an SM changes its L1 / shared split only when idle, so the copy kernel
+  // asks for the largest shared carveout and never shrinks it
+  static const cudaError_t carve = cudaFuncSetAttribute(
+      copy_misses_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+      cudaSharedmemCarveoutMaxShared);
+  OES_REQUIRE(carve == cudaSuccess, "slot_cache_copy_misses: carveout attribute failed");
+  const int grid = num_sms();
   copy_misses_kernel<<<grid, kCopyThreads, 0, stream>>>(
       src->dev_bases, src->L, src->E, src->row_bytes, static_cast<uint8_t*>(pool), S, miss, n_miss,
       max_misses, status);

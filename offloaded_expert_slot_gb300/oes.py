@@ -94,6 +94,14 @@ _SIGS = {
                                      _vp]),
     "moe_layer_forward_stream": (_i, [_vp, _vp, _i, C.POINTER(LayerDesc), C.POINTER(Chunk), _vp,
                                       _vp]),
+    "oes_takes_slot_path": (_i, [_i, _i, _i, _i, _i]),
+    "oes_stage_plan_create": (_i, [_vp, C.POINTER(_i), _i, _i, _vp, C.POINTER(_vp)]),
+    "oes_stage_plan_destroy": (_i, [_vp]),
+    "oes_stage_plan_layer": (_i, [_vp, _i, C.POINTER(_i), _vp, C.POINTER(_i)]),
+    "moe_layers_forward_staged": (_i, [_vp, _vp, _vp, C.POINTER(LayerDesc), C.POINTER(Chunk), _vp,
+                                       _vp]),
+    "moe_layer_forward": (_i, [_vp, _vp, _vp, _vp, _i, C.POINTER(LayerDesc), C.POINTER(Chunk), _i,
+                               _i, _vp, _vp, C.POINTER(_i)]),
 }
 
 
@@ -312,4 +320,45 @@ def moe_layer_forward_slots(cache, src, pool, layer, desc: LayerDesc, ch: Chunk,
 def moe_layer_forward_stream(src, layer_buf, layer, desc: LayerDesc, ch: Chunk, copy_stream=None,
                              compute_stream=None):
     _call("moe_layer_forward_stream", src, _ptr(layer_buf), layer, C.byref(desc), C.byref(ch),
+          _stream(copy_stream), _stream(compute_stream))
+
+
+def oes_takes_slot_path(T, k, E, S, demand_tokens) -> bool:
+    return bool(load().oes_takes_slot_path(T, k, E, S, demand_tokens))
+
+
+def moe_layer_forward(cache, src, pool, layer_buf, layer, desc: LayerDesc, ch: Chunk, demand_tokens,
+                      record_stats, copy_stream=None, stream=None) -> bool:
+    """Returns True when the chunk took the slot path."""
+    took = C.c_int(-1)
+    _call("moe_layer_forward", cache, src, _ptr(pool), _ptr(layer_buf), layer, C.byref(desc),
+          C.byref(ch), demand_tokens, int(bool(record_stats)), _stream(copy_stream), _stream(stream),
+          C.byref(took))
+    return bool(took.value)
+
+
+def oes_stage_plan_create(cache, layers, skip_resident, stream=None):
+    arr = (_i * len(layers))(*[int(l) for l in layers])
+    out = _vp()
+    _call("oes_stage_plan_create", cache, arr, len(layers), int(bool(skip_resident)),
+          _stream(stream), C.byref(out))
+    return out.value
+
+
+def oes_stage_plan_destroy(plan):
+    _call("oes_stage_plan_destroy", plan)
+
+
+def oes_stage_plan_layer(plan, i, E):
+    """(runs as a list of (e0, e1), staged rows) of layer i of the plan."""
+    n, rows = _i(), _i()
+    buf = (C.c_int32 * (2 * E))()
+    _call("oes_stage_plan_layer", plan, i, C.byref(n), C.cast(buf, _vp), C.byref(rows))
+    return [(buf[2 * j], buf[2 * j + 1]) for j in range(n.value)], rows.value
+
+
+def moe_layers_forward_staged(plan, src, pool, desc: LayerDesc, chunks, copy_stream=None,
+                              compute_stream=None):
+    arr = (Chunk * len(chunks))(*chunks)
+    _call("moe_layers_forward_staged", plan, src, _ptr(pool), C.byref(desc), arr,
           _stream(copy_stream), _stream(compute_stream))

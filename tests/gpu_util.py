@@ -53,7 +53,8 @@ class Workload:
     """One layer config set up on the GPU: router inputs, pinned host source,
     slot pool with the seeded pre-fill, slot cache and expert source handles."""
 
-    def __init__(self, cfg: LayerConfig, with_pool: bool = True, gen_device: str = "cuda"):
+    def __init__(self, cfg: LayerConfig, with_pool: bool = True, gen_device: str = "cuda",
+                 extra_rows: int = 0):
         lib()
         self.cfg = cfg
         self.rin = router_inputs(cfg)
@@ -73,7 +74,11 @@ class Workload:
         self.cache = None
         self.pool = None
         if with_pool:
-            self.pool = torch.empty((cfg.S, rb), dtype=torch.uint8, device="cuda")
+            # rows past S (the staging buffers of the staged runner) start as
+            # a byte pattern no expert row has
+            self.pool_all = torch.full((cfg.S + extra_rows, rb), 0x5A, dtype=torch.uint8,
+                                       device="cuda")
+            self.pool = self.pool_all[:cfg.S]
             self.cache = oes.slot_cache_create(cfg.S, cfg.L, cfg.E)
             self.reset_pool()
 

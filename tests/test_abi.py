@@ -52,8 +52,8 @@ def test_host_argument_checks(lib):
 
 
 def test_tile_plan_uses_the_layers_expert_count(lib):
-    """FreeToken PR #676, Solution and Tests: the prefill picks its tiles from
-    tokens per expert of the layer, not of the slot pool.  At 600 tokens x
+    """FreeToken PR #676, Solution and Tests: tiles follow routes per expert
+    of the layer, never of the slot pool.  At 600 tokens x
     top-10 the layer's 512 experts get 11.7 routes each (blocks of 128 routes,
     token-major kernel); sizing by the 1100 slots would give 5.5 (blocks of
     16, weight-major kernel)."""
@@ -71,3 +71,11 @@ def test_align_capacity_macro_matches_the_oracle():
     from oracle.align import align_capacity
     for R, E, B in [(0, 5, 4), (1, 1, 1), (10, 3, 8), (40960, 512, 128), (65536, 2100, 64)]:
         assert oes.align_capacity(R, E, B) == align_capacity(R, E, B)
+
+
+def test_demand_token_dispatch_rule(lib):
+    """The page's threshold examples (tests/golden/demand_dispatch.json)."""
+    import json
+    from conftest import GOLDEN
+    for c in json.load(open(os.path.join(GOLDEN, "demand_dispatch.json")))["cases"]:
+        assert oes.oes_takes_slot_path(c["T"], c["k"], c["E"], c["S"], c["N"]) == c["slots"], c

@@ -5,8 +5,7 @@ streamed path, against the oracle.
 * Layer output vs the oracle (fp64): max-abs <= 2e-2 and rel-L2 <= 5e-3 for
   bf16 weights, <= 5e-2 and <= 1e-2 for NVFP4 weights.  The GPU rounds h
   (16-bit), y (bf16) and out (bf16); the oracle keeps fp64 throughout.
-* Slot path == streamed path, byte for byte (FreeToken PR #676, Solution:
-  "bit-identical to the streamed layer's").
+* Slot path == streamed path, byte for byte (FreeToken PR #676, Solution).
 * A demand admission records no statistic; a chunk the pool cannot hold is
   refused and streams.
 """
@@ -152,6 +151,24 @@ def test_medium_layers_match_oracle_and_stream(cfg):
     w.close()
 
 
+def test_full_pool_two_queries():
+    """Every slot full and two queries: query 1's misses evict the oldest
+    slots, some holding experts of query 2 that were resident before the
+    chunk; the overlapped GEMM must only take experts that were hits in their
+    own query (tables, output and slot == stream as everywhere)."""
+    lib()
+    cfg = scaled(C2, name="full_pool_bf16", T=40, k=4, E=512, H=256, I=192, S=200, L=2,
+                 prefill=200)
+    w = Workload(cfg, gen_device="cpu")
+    o, _ = oracle_slots(w)
+    q1 = {k_ for k_, _s, _old in o["queries"][0]["misses"]}
+    evicted = {old for q in o["queries"][:1] for _k, _s, old in q["misses"] if old >= 0}
+    later = {int(k_) for q in o["queries"][1:] for k_ in q["keys"] if k_ >= 0}
+    assert len(o["queries"]) >= 2 and q1 and evicted & later, "the case must evict a later query's expert"
+    full_check(w)
+    w.close()
+
+
 def test_tiny_workload_streams_and_is_refused_by_slots():
     lib()
     w = Workload(C1, gen_device="cpu")
@@ -245,3 +262,42 @@ def test_long_prefill_layers_sequence():
         if layer != 1:
             check_close(r.out, o["out"], "nvfp4", toks)
     w.close()
+
+
+def test_demand_token_dispatch():
+    """FreeToken PR #676, Solution and Tests: with threshold N a chunk of at
+    most N tokens goes through the slot cache, a longer one (or any chunk at
+    N = 0) streams and leaves the cache alone; both give the same bytes; a
+    chunk the pool cannot hold streams at any threshold."""
+    lib()
+    cfg = MEDIUM_SWAP_BF16
+    w = Workload(cfg, gen_device="cpu")
+    st0 = oes.slot_cache_read_state(w.cache, cfg.S, cfg.L, cfg.E)
+    outs = {}
+    for N, want_slots in [(0, False), (cfg.T - 1, False), (cfg.T, True)]:
+        r = Run(w)
+        buf = torch.empty((cfg.E, cfg.row_bytes), dtype=torch.uint8, device="cuda")
+        took = oes.moe_layer_forward(w.cache, w.src, w.pool, buf, cfg.layer, r.desc, r.chunk, N, 0,
+                                     copy_stream=torch.cuda.Stream())
+        torch.cuda.synchronize()
+        assert took == want_slots and int(r.status.item()) == 0
+        st = oes.slot_cache_read_state(w.cache, cfg.S, cfg.L, cfg.E)
+        if not want_slots:
+            assert np.array_equal(st["slot_key"], st0["slot_key"])
+            assert np.array_equal(st["slot_ts"], st0["slot_ts"])
+        outs[N] = r.out.view(torch.int16).clone()
+    o, ocache = oracle_slots(w)
+    st = oes.slot_cache_read_state(w.cache, cfg.S, cfg.L, cfg.E)
+    assert np.array_equal(st["slot_key"], ocache.slot_key)
+    assert np.array_equal(st["map"], ocache.map)
+    assert torch.equal(outs[0], outs[cfg.T]) and torch.equal(outs[0], outs[cfg.T - 1])
+    check_close(outs[cfg.T].view(torch.bfloat16), o["out"], "bf16")
+    w.close()
+
+    t = Workload(C1, gen_device="cpu")
+    r = Run(t)
+    buf = torch.empty((C1.E, C1.row_bytes), dtype=torch.uint8, device="cuda")
+    assert not oes.moe_layer_forward(t.cache, t.src, t.pool, buf, 0, r.desc, r.chunk, 1 << 20, 0)
+    torch.cuda.synchronize()
+    assert int(r.status.item()) == 0
+    t.close()

@@ -5,8 +5,8 @@
    (timestamp, slot) with no recency list -- on thousands of random query
    sequences.
 3. The invariants the pages fix: map and slot_key stay a bijection; no query
-   evicts its own hits; when a layer routes to no more experts than the pool
-   holds, later queries never evict an earlier query's slots (FreeToken PR
+   evicts its own hits; when the pool can hold all of a chunk's experts,
+   later queries never evict an earlier query's slots (FreeToken PR
    #676, the author's reply); with record_stats off no statistic moves.
 """
 import json
@@ -167,3 +167,52 @@ def test_record_stats_counts():
     c.ensure([0, 5], record_stats=False)       # demand admission: no stats
     assert c.stats() == snap[0] and (c.decode_freq == snap[1]).all()
     assert c.map[0] >= 0 and c.map[5] >= 0
+
+
+def test_a_later_querys_resident_expert_can_be_evicted_but_touched_ones_cannot():
+    """The pages protect what earlier queries touched (the author's reply on
+    FreeToken PR #676: LRU takes those last), not what a later query will
+    hit: with a full pool, query 1's misses evict the oldest slots, which
+    may hold an expert of query 2.  Pinned by hand: 4 slots, query width 2,
+    chunk experts {0, 1, 2, 3} of one layer; slots hold 3 (oldest), 9, 8,
+    1.  Query {0, 1}: 1 hits, 0 misses and evicts the oldest non-hit slot,
+    the one holding 3, which query {2, 3} then misses again."""
+    c = SlotCache.from_state(4, 1, 16, np.array([3, 9, 8, 1]), np.array([1, 2, 3, 4]), 4)
+    st, m1 = c.ensure([0, 1])
+    assert st == OK and m1 == [(0, 0, 3)]
+    st, m2 = c.ensure([2, 3])
+    assert st == OK and m2 == [(2, 1, 9), (3, 2, 8)]
+    assert c.map[1] == 3 and c.map[0] == 0          # touched by query 1: kept
+
+
+@pytest.mark.parametrize("seed", range(200))
+def test_touched_slots_survive_the_chunk_with_a_full_pool(seed):
+    """Random full pools and chunks that fit: every expert a query touched
+    (hit or filled) keeps its slot through the rest of the chunk; an expert
+    that was a hit in its own query keeps the slot it had before."""
+    rng = np.random.default_rng(seed)
+    E, L = int(rng.integers(8, 60)), int(rng.integers(1, 4))
+    S = int(rng.integers(4, min(L * E, 80) + 1))
+    keys = rng.choice(L * E, size=S, replace=False)
+    c = SlotCache.from_state(S, L, E, keys.astype(np.int32),
+                             rng.permutation(S).astype(np.int64) + 1, S)
+    before = c.map.copy()
+    D = int(rng.integers(1, min(S, E) + 1))
+    layer = int(rng.integers(0, L))
+    chunk = np.sort(rng.choice(E, size=D, replace=False)) + layer * E
+    width = int(rng.integers(1, 6))
+    touched = {}
+    hits = set()
+    for q0 in range(0, D, width):
+        q = chunk[q0:q0 + width]
+        for key in q:
+            if c.map[key] >= 0:
+                hits.add(int(key))
+        st, _ = c.ensure(q)
+        assert st == OK
+        for key in q:
+            touched[int(key)] = int(c.map[key])
+        for key, slot in touched.items():
+            assert c.map[key] == slot
+    for key in hits:
+        assert c.map[key] == before[key]
