@@ -232,6 +232,25 @@ class Bench:
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / steps
 
+    # -- the same step as one CUDA graph, replayed
+    def graph_timed(self, steps, warmup):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                self.step()
+        torch.cuda.current_stream().wait_stream(s)
+        for _ in range(warmup):
+            g.replay()
+        ms = self.timed(g.replay, steps)
+        st = int(self.status.item())
+        if st:
+            raise RuntimeError(f"device status {st} after graph replays")
+        del g
+        return ms
+
     # -- end to end through the C ABI with host buffers
     def e2e(self, steps, warmup):
         torch, oes, cfg = self.torch, self.oes, self.cfg
@@ -361,7 +380,9 @@ def gpu_launches(cfg, with_restore=True):
     """Kernels of liboes launched per step of the slot path."""
     R = cfg.T * cfg.k
     Q = (min(R, cfg.E) + 127) // 128
-    n = 1 + 1 + 2 * Q + 3 + 3          # topk, distinct, Q x (ensure, copy), align x3, gemm1/2 + combine
+    # topk, distinct, Q x (ensure, copy), group flags, align x3, gemm1/2 over
+    # the hits, gemm1/2 per query over its copied experts, combine
+    n = 1 + 1 + 2 * Q + 1 + 3 + 2 + 2 * Q + 1
     if cfg.logits == "gate":
         n += 1
     if cfg.wfmt == "nvfp4":
@@ -412,6 +433,9 @@ def gpu_arm(args, cfg):
     barrier()
     ms_max = reduce_max(ms, dist, "cuda")
     value = job_value(cfg.T, world, ms_max)
+
+    graph_ms = b.graph_timed(args.steps, args.warmup)
+    graph_ms = reduce_max(graph_ms, dist, "cuda")
 
     e2e_ms, bi, bo = b.e2e(args.steps, args.warmup)
     e2e_ms = reduce_max(e2e_ms, dist, "cuda")
@@ -478,6 +502,9 @@ def gpu_arm(args, cfg):
                 "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": bi,
                         "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms},
                 "gpu_launches": gpu_launches(cfg) * args.steps,
+                "graph": {"value": job_value(cfg.T, world, graph_ms), "unit": "tokens/s",
+                          "ms_per_step": graph_ms,
+                          "what": "the same step captured once as a CUDA graph and replayed"},
                 "clocks": clocks, "roofline": roofline, "roofline_gemm": roof_gemm,
                 "steps_breakdown": kernels, "host_link_gbs": link, "cpu_baseline": cpu}
         print(json.dumps(line))

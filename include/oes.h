@@ -145,7 +145,7 @@ int slot_cache_restore(oes_slot_cache *cache, const void *src, oes_stream_t stre
 
 /* Device pointer to the layer's expert->slot remap: map + layer * E, [E]
  * int32, the slot of each of the layer's experts or -1 (vLLM fork PR #48,
- * What: "physical-row remap").  Valid until slot_cache_destroy. */
+ * What: the remap from logical expert to physical row).  Valid until slot_cache_destroy. */
 int slot_cache_layer_map(const oes_slot_cache *cache, int layer, const int32_t **e2s);
 
 /* One LRU ensure query (FreeToken PR #676, Solution: the distinct experts
@@ -352,7 +352,13 @@ int moe_layer_workspace_views(const oes_layer_desc *layer, int T, int k, void *w
  * copying query by query.
  * The pool must hold every expert the chunk needs at once (the author's
  * reply on FreeToken PR #676): with min(T*k, E) > S this returns
- * OES_ERR_CAPACITY and launches nothing; the caller streams the layer. */
+ * OES_ERR_CAPACITY and launches nothing; the caller streams the layer.
+ * The call makes no host synchronisation and no allocation, and its side
+ * stream forks from and joins `stream` through events.  So a decode step
+ * (record_stats = 1) can be captured from `stream` into a CUDA graph and
+ * replayed on new tokens written into the same x / logits buffers.  The
+ * first call with a given shape sets one-time kernel attributes, so run it
+ * once before capturing. */
 int moe_layer_forward_slots(oes_slot_cache *cache, const oes_expert_source *src, void *pool,
                             int layer, const oes_layer_desc *desc, const oes_chunk *chunk,
                             int record_stats, oes_stream_t stream);

@@ -3,7 +3,7 @@
 Bit-exact: every miss list, n_miss, map, slot_key, slot_ts, clock, the
 counters and decode_freq, and the status word.  Copies: miss slots hold the
 source rows byte for byte, every other slot is untouched (vLLM fork PR #51,
-Tests: "resident rows untouched").
+Tests: rows already resident keep their bytes).
 """
 import json
 import os

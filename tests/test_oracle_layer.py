@@ -8,7 +8,7 @@
   each landing before the next, with no statistic recorded (FreeToken PR
   #676, Tests).
 * Resident rows the chunk does not evict are untouched (vLLM fork PR #51,
-  Tests: "resident rows untouched").
+  Tests: rows already resident keep their bytes).
 """
 import numpy as np
 import pytest
