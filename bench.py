@@ -39,6 +39,11 @@ from offloaded_expert_slot_gb300.configs import CONFIGS  # noqa: E402
 DEFAULT_CONFIG = "c2_decode_width"
 METRIC = "routed tokens/s per MoE layer (1xGB300)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes (read + write) per copy_misses_kernel launch on the decode-width
+# workload, from one ncu capture of the current kernel (one warp per SM):
+# 0.05 MB read + 123.2 MB written.  Valid only for that workload and kernel.
+COPY_TRAFFIC_WORKLOAD = "c2_decode_width"
+COPY_TRAFFIC_PER_LAUNCH = 123.26e6
 
 
 def peaks():
@@ -480,10 +485,16 @@ def gpu_arm(args, cfg):
                  "algorithmic_bytes": step_bytes["gemm"], "launch_ms": bd["gemm"]}
     if dom == "copy":
         c = kernels["copy"]
+        q = info["queries"]
+        traffic = COPY_TRAFFIC_PER_LAUNCH if cfg.name == COPY_TRAFFIC_WORKLOAD else None
         roofline = {"kernel": "copy_misses_kernel", "bound": "host_link", "achieved": c["GB/s"],
-                    "peak": link, "unit": "GB/s", "frac": c["frac"], "traffic": None,
+                    "peak": link, "unit": "GB/s", "frac": c["frac"], "traffic": traffic,
+                    "traffic_note": "DRAM read + write per launch from one ncu capture; the rows "
+                                    "are read over the host link, and up to ~40 MB of a launch's "
+                                    "writes is still in L2 when it ends",
                     "peak_source": "measured in this run: 1 GiB pinned host->device cudaMemcpyAsync",
-                    "algorithmic_bytes": step_bytes["copy"], "launch_ms": bd["copy"]}
+                    "launches": q, "algorithmic_bytes": step_bytes["copy"] / q,
+                    "launch_ms": bd["copy"] / q}
     else:
         roofline = roof_gemm
     if rank == 0:
