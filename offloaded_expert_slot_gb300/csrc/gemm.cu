@@ -511,8 +511,14 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
 // epilogue, which stores h / y rows with 16-byte vectors.  Same roles,
 // barriers and shared-memory stage layout as the kernel above (weights at
 // the stage start, 32 KB; tokens after them, 16 KB).
+// At most 64 registers a thread: the NVFP4 variant has 28 warps, 7 on each
+// of the SM's four sub-partitions, and at 72 registers they would leave 256
+// registers of a sub-partition free, too few for the miss-copy warp that
+// runs beside this kernel; the copy's CTAs then waited for GEMM CTAs to exit
+// and were packed onto the few SMs that freed first (a 2.5x slower copy).
+// At 64 nothing spills.
 template <int MODE, int WF>
-__global__ void __launch_bounds__(gemm_threads_tm(WF), 1)
+__global__ void __maxnreg__(64)
     grouped_gemm_tm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   constexpr int kN = 256;                  // weight rows per tile
   extern __shared__ uint8_t smem_raw[];
