@@ -61,7 +61,19 @@ enum {
   OES_DEV_TIMEOUT = 4   /* a bounded wait gave up */
 };
 
-enum { OES_WFMT_BF16 = 0, OES_WFMT_NVFP4 = 1 };
+/* Expert formats.  NVFP4 weights are decoded exactly to f16 in shared memory
+ * and the activations stay 16-bit (W4A16).  NVFP4_W4A4 uses the same expert
+ * rows but also quantises the activations to NVFP4, under the maximum of the
+ * layer's input scales (FreeToken PR #676, Solution and Tests: the W4A4
+ * path takes the layer's scales, never another slot's).  x per 16 along H and
+ * the SwiGLU output h per 16 along I become e2m1 codes with e4m3 block
+ * scales: s = amax / (6 a), q = v / (sf a) in fp32, each rounded to nearest
+ * even and saturating.  The GEMMs multiply the exact f16 products q * sf and
+ * scale their fp32 sums by a and the weights' global scale, which is what a
+ * block-scaled FP4 MMA computes, up to summation order.  It needs the view's
+ * input_scale13 / input_scale2 (positive; a non-positive maximum sets
+ * OES_DEV_BAD_ID and uses 1). */
+enum { OES_WFMT_BF16 = 0, OES_WFMT_NVFP4 = 1, OES_WFMT_NVFP4_W4A4 = 2 };
 
 #define OES_QUERY_MAX 128   /* ids per ensure query (FreeToken PR #676, Solution) */
 #define OES_MAX_TOPK 32
@@ -279,6 +291,15 @@ int oes_tile_plan(int R, int E, int *block);
 
 /* Workspace bytes of moe_grouped_gemm_slots for T tokens at top-k. */
 size_t moe_grouped_gemm_workspace_size(const oes_routed_experts *view, int T, int k);
+
+/* Device pointers to the GEMM's intermediates inside its workspace, for
+ * checking the steps: h [capacity, I] (16-bit: bf16 for bf16 weights, f16
+ * otherwise; for W4A4 the quantised q * sf), y [T*k, H] bf16, and x16 [T, H]
+ * f16, the 16-bit copy of x the NVFP4 GEMMs read (for W4A4, q * sf of the
+ * quantised x; NULL for bf16 weights).  Any output may be NULL. */
+int moe_grouped_gemm_workspace_views(const oes_routed_experts *view, int T, int k,
+                                     void *workspace, uint16_t **h, uint16_t **y,
+                                     uint16_t **x16);
 
 /* The grouped SwiGLU expert GEMM over the slot pool (FreeToken PR #676,
  * Solution: a demand chunk reuses the decode GEMM, reading each expert at

@@ -38,6 +38,9 @@ class LayerConfig:
     layer_input_scales: tuple = ()
     other_slot_input_scale: float = 0.0
     distinct_source_layers: int = 0   # 0: one pinned source per layer
+    # NVFP4 only: activations quantised to NVFP4 too (W4A4), under the
+    # maximum of the layer's input scales
+    w4a4: bool = False
 
     @property
     def R(self) -> int:

@@ -144,6 +144,57 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
+// f32 pair -> e2m1x2 byte, rounded to nearest even and saturating at 6:
+// `hi` in the upper nibble, `lo` in the lower one.
+__device__ __forceinline__ uint32_t cvt_f32x2_e2m1x2(float hi, float lo) {
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// f32 -> e4m3 byte, rounded to nearest even and saturating at 448.
+__device__ __forceinline__ uint32_t cvt_f32_e4m3(float x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
+  return r & 0xFFu;
+}
+
+// W4A4 activations (FreeToken PR #676, Solution: quantised under the max a of
+// the layer's input scales).  A block of 16 consecutive values along K
+// becomes e2m1 codes q with one e4m3 scale sf: s = amax / (6 a) and
+// q_i = v_i / (sf a) in fp32, each rounded to nearest even and saturating;
+// a block with sf = 0 is all zero.  The GEMM reads q_i * sf, exact in f16,
+// and a multiplies its fp32 sums.
+__device__ __forceinline__ uint32_t act_scale_f16x2(float amax, float a, float* sf) {
+  const uint32_t sc = cvt_f32_e4m3(__fdiv_rn(amax, __fmul_rn(6.0f, a)));
+  const uint32_t sf2 = cvt_e4m3x2_f16x2(sc | (sc << 8));
+  *sf = __half2float(__ushort_as_half(static_cast<unsigned short>(sf2 & 0xFFFFu)));
+  return sf2;
+}
+__device__ __forceinline__ void quant16_act(const float (&v)[16], float a, uint32_t (&out)[8]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  float sf;
+  const uint32_t sf2 = act_scale_f16x2(amax, a, &sf);
+  const float d = __fmul_rn(sf, a);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t b = sf > 0.0f ? cvt_f32x2_e2m1x2(__fdiv_rn(v[2 * j + 1], d), __fdiv_rn(v[2 * j], d)) : 0u;
+    out[j] = hmul2_u32(cvt_e2m1x2_f16x2(b), sf2);
+  }
+}
+// The same for a block spread over 16 consecutive lanes, one value each; all
+// 32 lanes of the warp call it.  Returns this lane's f16 q * sf.
+__device__ __forceinline__ uint16_t quant_lane_act(float v, float a) {
+  float amax = fabsf(v);
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  float sf;
+  const uint32_t sf2 = act_scale_f16x2(amax, a, &sf);
+  const uint32_t b = sf > 0.0f ? cvt_f32x2_e2m1x2(0.0f, __fdiv_rn(v, __fmul_rn(sf, a))) : 0u;
+  return static_cast<uint16_t>(hmul2_u32(cvt_e2m1x2_f16x2(b), sf2) & 0xFFFFu);
+}
 
 // One weight row of one K chunk: 32 bytes of e2m1 pairs and a 32-bit word of
 // four e4m3 scales (one per 16 elements) -> 64 f16 = 8 x 16 bytes, stored at
@@ -413,6 +464,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
       if (WF)
         gs = *reinterpret_cast<const float*>(p.pool + (int64_t)t.slot * p.row_bytes + p.scal_off +
                                              (MODE == 1 ? 0 : 4));
+      if (WF && p.a4) gs *= p.act[MODE - 1];
       const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16) + a * acc_cols;
       const int N = round16(t.nvalid);
       for (int c0 = 0; c0 < N; c0 += 16) {
@@ -423,7 +475,18 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
           tmem_ld_16(tl + p.BN + c0, v);
           tc_wait_ld();
           const int i = t.m * kTileM + row;
-          if (i < p.I) {
+          if (WF && p.a4) {
+            // W4A4: a block of 16 along I is 16 consecutive lanes
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int n = c0 + j;
+              const bool keep = i < p.I && n < t.nvalid;
+              const float hv = keep ? silu(__uint_as_float(g[j]) * gs) * (__uint_as_float(v[j]) * gs)
+                                    : 0.0f;
+              const uint16_t hb = quant_lane_act(hv, p.act[1]);
+              if (keep) p.h[((int64_t)t.b * p.BN + n) * p.I + i] = hb;
+            }
+          } else if (i < p.I) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int n = c0 + j;
@@ -740,6 +803,7 @@ __global__ void __maxnreg__(64)
       if (WF)
         gs = *reinterpret_cast<const float*>(p.pool + (int64_t)t.slot * p.row_bytes + p.scal_off +
                                              (MODE == 1 ? 0 : 4));
+      if (WF && p.a4) gs *= p.act[MODE - 1];
       const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16) + a * kN;
       if (MODE == 1) {
         uint16_t* hrow = p.h + ((int64_t)t.b * p.BN + row) * p.I;
@@ -751,19 +815,27 @@ __global__ void __maxnreg__(64)
           const int i0 = t.m * kTileM + c0;
           if (live && i0 < p.I) {
             uint32_t packed[8];
+            if (WF && p.a4) {
+              float hv[16];
 #pragma unroll
-            for (int j = 0; j < 16; j += 2) {
-              float h0 = silu(__uint_as_float(g[j]) * gs) * (__uint_as_float(v[j]) * gs);
-              float h1 = silu(__uint_as_float(g[j + 1]) * gs) * (__uint_as_float(v[j + 1]) * gs);
-              uint32_t lo, hi;
-              if (WF) {
-                lo = __half_as_ushort(__float2half_rn(h0));
-                hi = __half_as_ushort(__float2half_rn(h1));
-              } else {
-                lo = __bfloat16_as_ushort(__float2bfloat16_rn(h0));
-                hi = __bfloat16_as_ushort(__float2bfloat16_rn(h1));
+              for (int j = 0; j < 16; ++j)
+                hv[j] = silu(__uint_as_float(g[j]) * gs) * (__uint_as_float(v[j]) * gs);
+              quant16_act(hv, p.act[1], packed);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; j += 2) {
+                float h0 = silu(__uint_as_float(g[j]) * gs) * (__uint_as_float(v[j]) * gs);
+                float h1 = silu(__uint_as_float(g[j + 1]) * gs) * (__uint_as_float(v[j + 1]) * gs);
+                uint32_t lo, hi;
+                if (WF) {
+                  lo = __half_as_ushort(__float2half_rn(h0));
+                  hi = __half_as_ushort(__float2half_rn(h1));
+                } else {
+                  lo = __bfloat16_as_ushort(__float2bfloat16_rn(h0));
+                  hi = __bfloat16_as_ushort(__float2bfloat16_rn(h1));
+                }
+                packed[j / 2] = lo | (hi << 16);
               }
-              packed[j / 2] = lo | (hi << 16);
             }
             uint4* dst = reinterpret_cast<uint4*>(hrow + i0);
             dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
@@ -848,6 +920,62 @@ __global__ void x_to_f16_kernel(const uint16_t* __restrict__ x, uint16_t* __rest
   }
 }
 
+// W4A4: act[0] = max of the layer's w13 input scales, act[1] = max of its w2
+// input scales (one CTA).  A non-positive or non-finite maximum is flagged
+// OES_DEV_BAD_ID and replaced by 1.
+__global__ void act_scale_kernel(const float* __restrict__ in13, const float* __restrict__ in2,
+                                 int E, float* __restrict__ act, int32_t* __restrict__ status) {
+  __shared__ float red[2][32];
+  float m13 = -INFINITY, m2 = -INFINITY;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    m13 = fmaxf(m13, in13[e]);
+    m2 = fmaxf(m2, in2[e]);
+  }
+  for (int o = 16; o >= 1; o >>= 1) {
+    m13 = fmaxf(m13, __shfl_xor_sync(0xffffffffu, m13, o));
+    m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+  }
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) {
+    red[0][w] = m13;
+    red[1][w] = m2;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) {
+      m13 = fmaxf(m13, red[0][i]);
+      m2 = fmaxf(m2, red[1][i]);
+    }
+    const bool ok = m13 > 0.0f && m2 > 0.0f && isfinite(m13) && isfinite(m2);
+    if (!ok) set_status(status, OES_DEV_BAD_ID);
+    act[0] = ok ? m13 : 1.0f;
+    act[1] = ok ? m2 : 1.0f;
+  }
+}
+
+// W4A4: x [T, H] bf16 -> x16 [T, H] f16 holding q * sf per block of 16 along H.
+__global__ void x_quant_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ x16,
+                               int64_t nblk, const float* __restrict__ act) {
+  const float a = act[0];
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nblk;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + i * 16);
+    const uint4 b0 = src[0], b1 = src[1];
+    const uint32_t w[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[2 * j] = __uint_as_float(w[j] << 16);
+      v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+    uint32_t o[8];
+    quant16_act(v, a, o);
+    uint4* dst = reinterpret_cast<uint4*>(x16 + i * 16);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
 // out[t, :] = sum_{j=0..k-1} w[t, j] * y[t*k + j, :], fp32 in j order -> bf16.
 __global__ void combine_kernel(const uint16_t* __restrict__ y, const float* __restrict__ w,
                                const int32_t* __restrict__ ids, int T, int k, int H, int E,
@@ -911,6 +1039,7 @@ struct Ws {
   uint16_t* h;
   uint16_t* y;
   uint16_t* x16;
+  float* act;  // W4A4: the layer's two activation scales
   size_t bytes;
 };
 
@@ -926,7 +1055,9 @@ Ws carve(void* base, int T, int k, int E, int H, int I, int B, int wfmt) {
   w.y = reinterpret_cast<uint16_t*>(p + off);
   off += up((size_t)R * H * 2);
   w.x16 = reinterpret_cast<uint16_t*>(p + off);
-  if (wfmt == OES_WFMT_NVFP4) off += up((size_t)T * H * 2);
+  if (wfmt != OES_WFMT_BF16) off += up((size_t)T * H * 2);
+  w.act = reinterpret_cast<float*>(p + off);
+  if (wfmt == OES_WFMT_NVFP4_W4A4) off += 256;
   w.bytes = off + 256;
   return w;
 }
@@ -1028,6 +1159,18 @@ extern "C" size_t moe_grouped_gemm_workspace_size(const oes_routed_experts* v, i
   return carve(nullptr, T, k, v->E, v->H, v->I, B, v->wfmt).bytes;
 }
 
+extern "C" int moe_grouped_gemm_workspace_views(const oes_routed_experts* v, int T, int k,
+                                                void* workspace, uint16_t** h, uint16_t** y,
+                                                uint16_t** x16) {
+  OES_REQUIRE(v && workspace && T >= 0 && k >= 1 && v->E >= 1,
+              "moe_grouped_gemm_workspace_views: bad arguments");
+  const Ws ws = carve(workspace, T, k, v->E, v->H, v->I, tile_plan(T * k, v->E), v->wfmt);
+  if (h) *h = ws.h;
+  if (y) *y = ws.y;
+  if (x16) *x16 = v->wfmt == OES_WFMT_BF16 ? nullptr : ws.x16;
+  return OES_OK;
+}
+
 namespace oes {
 
 // Validates the call, writes the f16 copy of x (NVFP4), and builds the tensor
@@ -1042,7 +1185,11 @@ int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
   OES_REQUIRE(E >= 1 && E <= OES_MAX_EXPERTS && S >= 1, "moe_grouped_gemm_slots: bad E=%d S=%d", E, S);
   OES_REQUIRE(H >= 64 && I >= 64 && H % 64 == 0 && I % 64 == 0 && H <= 16384 && I <= 16384,
               "moe_grouped_gemm_slots: H=%d I=%d must be multiples of 64 in [64, 16384]", H, I);
-  OES_REQUIRE(v->wfmt == OES_WFMT_BF16 || v->wfmt == OES_WFMT_NVFP4, "moe_grouped_gemm_slots: bad wfmt");
+  OES_REQUIRE(v->wfmt == OES_WFMT_BF16 || v->wfmt == OES_WFMT_NVFP4 ||
+                  v->wfmt == OES_WFMT_NVFP4_W4A4,
+              "moe_grouped_gemm_slots: bad wfmt");
+  OES_REQUIRE(v->wfmt != OES_WFMT_NVFP4_W4A4 || (v->input_scale13 && v->input_scale2),
+              "moe_grouped_gemm_slots: W4A4 needs the layer's input scales in the view");
   OES_REQUIRE(T >= 0 && T <= (1 << 24) && k >= 1 && k <= OES_MAX_TOPK,
               "moe_grouped_gemm_slots: bad T=%d k=%d", T, k);
   const int64_t need_row = expected_row_bytes(v->wfmt, H, I);
@@ -1064,7 +1211,8 @@ int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
   const int64_t cap = OES_ALIGN_CAPACITY(R, E, B);
   const Sections sec = sections(v->wfmt, H, I);
   const uint8_t* pool = static_cast<const uint8_t*>(v->pool);
-  const int wf = v->wfmt == OES_WFMT_NVFP4;
+  const int wf = v->wfmt != OES_WFMT_BF16;
+  const int a4 = v->wfmt == OES_WFMT_NVFP4_W4A4;
   g->wf = wf;
   g->tm = (B == 128);  // token-major kernel for blocks of 128 routes
   g->y = ws.y;
@@ -1076,7 +1224,15 @@ int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
   GemmMaps m1{}, m2{};
   int rc;
   const uint16_t* xb = x;
-  if (wf) {
+  if (a4) {
+    act_scale_kernel<<<1, 256, 0, stream>>>(v->input_scale13, v->input_scale2, E, ws.act, status);
+    OES_CHECK_LAUNCH("act_scale_kernel");
+    const int64_t nblk = (int64_t)T * H / 16;
+    const int blocks = (int)std::min<int64_t>(ceil_div64(nblk, 256), (int64_t)num_sms() * 8);
+    x_quant_kernel<<<blocks, 256, 0, stream>>>(x, ws.x16, nblk, ws.act);
+    OES_CHECK_LAUNCH("x_quant_kernel");
+    xb = ws.x16;
+  } else if (wf) {
     const int blocks = (int)std::min<int64_t>(ceil_div64((int64_t)T * H, 256), (int64_t)num_sms() * 8);
     x_to_f16_kernel<<<blocks, 256, 0, stream>>>(x, ws.x16, (int64_t)T * H);
     OES_CHECK_LAUNCH("x_to_f16_kernel");
@@ -1140,6 +1296,8 @@ int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
   p.S = S;
   p.up_row0 = I;
   p.xg = xb;
+  p.a4 = a4;
+  p.act = ws.act;
   p.h = ws.h;
   p.y = ws.y;
   p.status = status;

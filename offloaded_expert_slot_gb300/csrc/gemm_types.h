@@ -24,6 +24,8 @@ struct GemmParams {
   const int32_t* e2s;
   const uint8_t* flags;  // [E] group of each expert (filtered launches)
   int filter;            // 0 all blocks; g > 0 the blocks of experts with flags[e] == g
+  int a4;                // W4A4: x and h hold NVFP4-quantised activations
+  const float* act;      // W4A4: device [2] activation scales of GEMM1, GEMM2
   const uint8_t* pool;
   int64_t row_bytes;
   int64_t scal_off;  // NVFP4: byte offset of the fp32 scalars in a row

@@ -22,7 +22,7 @@ from . import build as _build
 
 OES_OK, OES_ERR_INVALID_ARG, OES_ERR_UNSUPPORTED, OES_ERR_CUDA, OES_ERR_CAPACITY = range(5)
 OES_DEV_CAPACITY, OES_DEV_BAD_ID, OES_DEV_TIMEOUT = 1, 2, 4
-OES_WFMT_BF16, OES_WFMT_NVFP4 = 0, 1
+OES_WFMT_BF16, OES_WFMT_NVFP4, OES_WFMT_NVFP4_W4A4 = 0, 1, 2
 OES_QUERY_MAX = 128
 OES_MAX_TOPK = 32
 OES_MAX_EXPERTS = 4096
@@ -95,6 +95,8 @@ _SIGS = {
     "moe_layer_forward_stream": (_i, [_vp, _vp, _i, C.POINTER(LayerDesc), C.POINTER(Chunk), _vp,
                                       _vp]),
     "oes_takes_slot_path": (_i, [_i, _i, _i, _i, _i]),
+    "moe_grouped_gemm_workspace_views": (_i, [C.POINTER(RoutedExperts), _i, _i, _vp, C.POINTER(_vp),
+                                              C.POINTER(_vp), C.POINTER(_vp)]),
     "oes_stage_plan_create": (_i, [_vp, C.POINTER(_i), _i, _i, _vp, C.POINTER(_vp)]),
     "oes_stage_plan_destroy": (_i, [_vp]),
     "oes_stage_plan_layer": (_i, [_vp, _i, C.POINTER(_i), _vp, C.POINTER(_i)]),
@@ -362,3 +364,10 @@ def moe_layers_forward_staged(plan, src, pool, desc: LayerDesc, chunks, copy_str
     arr = (Chunk * len(chunks))(*chunks)
     _call("moe_layers_forward_staged", plan, src, _ptr(pool), C.byref(desc), arr,
           _stream(copy_stream), _stream(compute_stream))
+
+
+def moe_grouped_gemm_workspace_views(view, T, k, workspace) -> dict:
+    ps = [C.c_void_p() for _ in range(3)]
+    _call("moe_grouped_gemm_workspace_views", C.byref(view), T, k, _ptr(workspace),
+          *[C.byref(p) for p in ps])
+    return {n: p.value for n, p in zip(["h", "y", "x16"], ps)}

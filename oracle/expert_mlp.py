@@ -71,6 +71,19 @@ def swiglu_expert(x: np.ndarray, w13: np.ndarray, w2: np.ndarray) -> np.ndarray:
     return (silu(g) * u) @ w2.T
 
 
+def swiglu_expert_w4a4(x: np.ndarray, w13: np.ndarray, w2: np.ndarray, a13: float,
+                       a2: float) -> np.ndarray:
+    """W4A4: x [n, H] (bf16 values) quantised per 16 along H under a13, the
+    SwiGLU output h quantised per 16 along I under a2 (its fp32 value decides
+    the codes, as on the GPU), weights decoded as in W4A16.  fp64 otherwise."""
+    from .quant import quantize_act
+    I = w2.shape[1]
+    xq = quantize_act(x.astype(np.float32), a13)[2] * a13
+    h = silu(xq @ w13[:I].T) * (xq @ w13[I:].T)
+    hq = quantize_act(h.astype(np.float32), a2)[2] * a2
+    return hq @ w2.T
+
+
 def combine(y: np.ndarray, w: np.ndarray, T: int, k: int) -> np.ndarray:
     """y [T*k, H], w [T, k] -> out [T, H]: sum over j in order 0..k-1."""
     H = y.shape[1]

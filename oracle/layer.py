@@ -19,7 +19,7 @@ import numpy as np
 
 from .align import moe_align_block_size
 from .distinct import distinct_experts
-from .expert_mlp import combine, expert_weights, swiglu_expert
+from .expert_mlp import combine, expert_weights, input_scales, swiglu_expert, swiglu_expert_w4a4
 from .numerics import bf16_to_f64
 from .router import gate_logits, route_topk
 from .slot_cache import OK
@@ -33,9 +33,22 @@ def route(router_in: dict, k: int):
     return logits, ids, w
 
 
-def expert_outputs(x_bits, ids, row_of_expert, wfmt, H, I, tokens=None):
+def _wfmt(cfg) -> str:
+    return "nvfp4_w4a4" if getattr(cfg, "w4a4", False) else cfg.wfmt
+
+
+def layer_act_scales(layer_row, E, H, I):
+    """W4A4 activation scales of a layer: the maximum of its experts' w13
+    and w2 input scales, read from the layer's own rows (FreeToken PR #676,
+    Solution and Tests: the layer's scales, not other slots')."""
+    s = [input_scales(layer_row(e), H, I) for e in range(E)]
+    return max(v[0] for v in s), max(v[1] for v in s)
+
+
+def expert_outputs(x_bits, ids, row_of_expert, wfmt, H, I, tokens=None, act=None):
     """y [R, H] fp64 for the routes of `tokens` (all tokens when None); other
-    rows are NaN.  row_of_expert(e) -> that expert's row bytes."""
+    rows are NaN.  row_of_expert(e) -> that expert's row bytes.  act: the
+    (a13, a2) activation scales of a W4A4 layer."""
     T, k = ids.shape
     x = bf16_to_f64(x_bits)
     y = np.full((T * k, H), np.nan, dtype=np.float64)
@@ -44,10 +57,14 @@ def expert_outputs(x_bits, ids, row_of_expert, wfmt, H, I, tokens=None):
     by_expert = {}
     for r in routes:
         by_expert.setdefault(int(ids.reshape(-1)[r]), []).append(int(r))
+    w4a4 = wfmt == "nvfp4_w4a4"
     for e, rs in sorted(by_expert.items()):
-        w13, w2 = expert_weights(row_of_expert(e), wfmt, H, I)
+        w13, w2 = expert_weights(row_of_expert(e), "nvfp4" if w4a4 else wfmt, H, I)
         rs = np.array(rs)
-        y[rs] = swiglu_expert(x[rs // k], w13, w2)
+        if w4a4:
+            y[rs] = swiglu_expert_w4a4(x[rs // k], w13, w2, act[0], act[1])
+        else:
+            y[rs] = swiglu_expert(x[rs // k], w13, w2)
     return y
 
 
@@ -78,8 +95,10 @@ def forward_slots(cfg, router_in, source_row, cache, pool, block, layer=None,
         queries.append({"keys": keys, "status": status, "misses": misses})
     e2s = cache.map[layer * E:(layer + 1) * E].copy()
     sorted_ids, block_expert, n_post_pad, _bad = moe_align_block_size(ids.reshape(-1), E, block)
-    y = expert_outputs(router_in["x"], ids, lambda e: pool[int(e2s[e])], cfg.wfmt, cfg.H, cfg.I,
-                       tokens=tokens)
+    act = (layer_act_scales(lambda e: source_row(layer, e), E, cfg.H, cfg.I)
+           if getattr(cfg, "w4a4", False) else None)
+    y = expert_outputs(router_in["x"], ids, lambda e: pool[int(e2s[e])], _wfmt(cfg), cfg.H, cfg.I,
+                       tokens=tokens, act=act)
     out = combine(np.nan_to_num(y), w, cfg.T, k)
     return {"logits": logits, "ids": ids, "w": w, "distinct": distinct, "D": D,
             "queries": queries, "e2s": e2s, "sorted_ids": sorted_ids,
@@ -92,7 +111,9 @@ def forward_stream(cfg, router_in, layer_rows, block, tokens=None):
     E, k = cfg.E, cfg.k
     logits, ids, w = route(router_in, k)
     sorted_ids, block_expert, n_post_pad, _bad = moe_align_block_size(ids.reshape(-1), E, block)
-    y = expert_outputs(router_in["x"], ids, layer_rows, cfg.wfmt, cfg.H, cfg.I, tokens=tokens)
+    act = layer_act_scales(layer_rows, E, cfg.H, cfg.I) if getattr(cfg, "w4a4", False) else None
+    y = expert_outputs(router_in["x"], ids, layer_rows, _wfmt(cfg), cfg.H, cfg.I, tokens=tokens,
+                       act=act)
     out = combine(np.nan_to_num(y), w, cfg.T, k)
     return {"ids": ids, "w": w, "sorted_ids": sorted_ids, "block_expert": block_expert,
             "n_post_pad": n_post_pad, "y": y, "out": out}
