@@ -75,6 +75,19 @@ enum {
  * OES_DEV_BAD_ID and uses 1). */
 enum { OES_WFMT_BF16 = 0, OES_WFMT_NVFP4 = 1, OES_WFMT_NVFP4_W4A4 = 2 };
 
+/* Eviction policies of the slot cache.  LRU is the pages' (FreeToken PR #676,
+ * the author's reply: the cache is LRU only).  LRFU is the scored policy the
+ * pages name without a formula (one author's build admits by LRFU;
+ * gdevenyi's review comment: a scored policy must pin a chunk's earlier
+ * queries against its later ones).  It follows Lee et al. (IEEE Trans.
+ * Computers 2001) with F(x) = (1 - 2^-k)^x in Q32.32 fixed point: each ensure
+ * decays every slot's score once (score -= score >> k; k = 0 never decays,
+ * which is LFU), evicts the non-hit, unpinned slots of smallest (score, slot),
+ * empty slots first, adds 1.0 to each hit, starts each fill at 1.0, and
+ * saturates at 2^51 - 1 units. */
+enum { OES_POLICY_LRU = 0, OES_POLICY_LRFU = 1 };
+#define OES_LRFU_MAX_K 18
+
 #define OES_QUERY_MAX 128   /* ids per ensure query (FreeToken PR #676, Solution) */
 #define OES_MAX_TOPK 32
 #define OES_MAX_EXPERTS 4096
@@ -181,6 +194,27 @@ int slot_cache_layer_map(const oes_slot_cache *cache, int layer, const int32_t *
 int slot_cache_ensure(oes_slot_cache *cache, int layer, const int32_t *experts, int n,
                       int record_stats, int32_t *miss, int32_t *n_miss, int32_t *status,
                       oes_stream_t stream);
+
+/* slot_cache_ensure with a pin tag.  Under LRFU, a nonzero tag excludes from
+ * the victims every slot pinned to it and pins every slot the query touches,
+ * so the queries of one chunk, sharing a tag, never evict one another's
+ * slots.  Under LRU the tag is ignored (LRU already takes those slots last).
+ * moe_layer_forward_slots hands each call a new tag. */
+int slot_cache_ensure_tagged(oes_slot_cache *cache, int layer, const int32_t *experts, int n,
+                             int record_stats, int32_t tag, int32_t *miss, int32_t *n_miss,
+                             int32_t *status, oes_stream_t stream);
+
+/* Selects the eviction policy (OES_POLICY_LRU, the default, or
+ * OES_POLICY_LRFU with decay shift k in [0, OES_LRFU_MAX_K]).  Waits for the
+ * device, then gives every occupied slot the score 1.0 and clears the pins.
+ * slot_cache_load_state does the same reset and keeps the policy; snapshot
+ * and restore include scores and pins. */
+int slot_cache_set_policy(oes_slot_cache *cache, int policy, int lrfu_k);
+
+/* Copies the LRFU scores (host [S] uint64, Q32.32) and pins (host [S] int32)
+ * out; either may be NULL.  Synchronises `stream` first. */
+int slot_cache_read_lrfu(const oes_slot_cache *cache, uint64_t *crf, int32_t *pin,
+                         oes_stream_t stream);
 
 /* Where the experts live on the host: L layers of E rows of row_bytes each;
  * layer l's rows start at the mapped address layer_base[l] (several layers

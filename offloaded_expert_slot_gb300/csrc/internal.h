@@ -18,6 +18,10 @@ struct oes_slot_cache {
   int64_t* slot_ts;      // [S] timestamp of the last query that touched the slot, 0 if empty
   int64_t* ctr;          // [4] clock, hits, misses, evictions
   int64_t* decode_freq;  // [L*E]
+  uint64_t* crf;         // [S] LRFU score of each slot, Q32.32
+  int32_t* pin;          // [S] LRFU pin tag of each slot, 0 = none
+  int policy, lrfu_k;    // OES_POLICY_*, LRFU decay shift
+  int32_t chunk_tag;     // last pin tag moe_layer_forward_slots handed out
   // side stream and events of moe_layer_forward_slots: the later queries'
   // ensures and every GEMM run there while the misses are copied on the
   // caller's stream; ensured[q] / copied[q] mark query q's ensure and copies

@@ -7,6 +7,7 @@
 // GEMM over the slots; Problem: streaming moves all of the layer's experts
 // for every chunk.
 #include <algorithm>
+#include <climits>
 #include <utility>
 #include <vector>
 
@@ -185,10 +186,14 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
   const int Q = (Lq + OES_QUERY_MAX - 1) / OES_QUERY_MAX;
   cudaStream_t side = cache->side;
   auto miss_of = [&](int q) { return w.miss + (size_t)q * 3 * OES_QUERY_MAX; };
+  // the chunk's pin tag: its queries never evict one another's slots under
+  // a scored policy (LRU ignores it)
+  cache->chunk_tag = cache->chunk_tag == INT32_MAX ? 1 : cache->chunk_tag + 1;
+  const int32_t tag = cache->chunk_tag;
   auto query = [&](int q, cudaStream_t s) {
     const int n = std::min(OES_QUERY_MAX, Lq - q * OES_QUERY_MAX);
-    return slot_cache_ensure(cache, layer, w.distinct + q * OES_QUERY_MAX, n, record_stats,
-                             miss_of(q), w.n_miss + q, c->status, s);
+    return slot_cache_ensure_tagged(cache, layer, w.distinct + q * OES_QUERY_MAX, n, record_stats,
+                                    tag, miss_of(q), w.n_miss + q, c->status, s);
   };
   auto copy = [&](int q, cudaStream_t s) {
     const int n = std::min(OES_QUERY_MAX, Lq - q * OES_QUERY_MAX);

@@ -24,20 +24,34 @@ struct CacheView {
   int64_t* slot_ts;
   int64_t* ctr;
   int64_t* decode_freq;
+  uint64_t* crf;
+  int32_t* pin;
+  int policy, lrfu_k;
 };
 
 CacheView view_of(oes_slot_cache* c) {
-  return CacheView{c->S, c->L, c->E, c->map, c->slot_key, c->slot_ts, c->ctr, c->decode_freq};
+  return CacheView{c->S,   c->L,      c->E,           c->map, c->slot_key, c->slot_ts,
+                   c->ctr, c->decode_freq, c->crf, c->pin,   c->policy,   c->lrfu_k};
 }
+
+constexpr uint64_t kCrfOne = 1ull << 32;           // LRFU score 1.0 (Q32.32)
+constexpr uint64_t kCrfSat = (1ull << 51) - 1;     // saturation; leaves 13 bits for the slot
 
 constexpr int kEnsureThreads = 1024;
 
-// One ensure query in one CTA.  Victims: the non-hit slots ordered by the
-// 64-bit key (timestamp << 16 | slot) -- empty slots have timestamp 0 and so
-// come first, in slot order -- sorted with a shared-memory bitonic network.
+// One ensure query in one CTA.  Victims: the non-hit slots ordered by a
+// 64-bit key sorted with a shared-memory bitonic network.  LRU: key =
+// (timestamp << 16 | slot); empty slots have timestamp 0 and so come first,
+// in slot order.  LRFU (Lee et al., IEEE Trans. Computers 2001, with
+// F(x) = (1 - 2^-k)^x): every slot's score decays once (crf -= crf >> k),
+// then key = (score << 13 | slot) over the slots that are neither hit nor
+// pinned to this query's tag, empty slots scoring 0; hits gain 1.0, fills
+// start at 1.0, and a nonzero tag pins every touched slot (gdevenyi's review
+// comment on FreeToken PR #676: a scored policy must pin a chunk's earlier
+// queries against its later ones).
 __global__ void __launch_bounds__(kEnsureThreads)
     ensure_kernel(CacheView c, int layer, const int32_t* __restrict__ experts, int n,
-                  int record_stats, int spad, int32_t* __restrict__ miss,
+                  int record_stats, int tag, int spad, int32_t* __restrict__ miss,
                   int32_t* __restrict__ n_miss, int32_t* __restrict__ status) {
   extern __shared__ uint64_t skey[];  // [spad]
   __shared__ int32_t qkey[OES_QUERY_MAX];
@@ -45,13 +59,16 @@ __global__ void __launch_bounds__(kEnsureThreads)
   __shared__ int32_t qrank[OES_QUERY_MAX];
   __shared__ int32_t wvalid[4], wmiss[4];
   __shared__ uint32_t hitmask[OES_MAX_SLOTS / 32];
-  __shared__ int32_t s_bad, s_nvalid, s_nmiss, s_nhit, s_evict;
+  __shared__ int32_t s_bad, s_nvalid, s_nmiss, s_nhit, s_evict, s_navail;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int LE = c.L * c.E;
 
+  const bool lrfu = c.policy == OES_POLICY_LRFU;
+  const int use_tag = lrfu ? tag : 0;
   if (tid == 0) {
     s_bad = 0;
     s_evict = 0;
+    s_navail = 0;
   }
   for (int i = tid; i < (c.S + 31) / 32; i += blockDim.x) hitmask[i] = 0;
   __syncthreads();
@@ -122,7 +139,29 @@ __global__ void __launch_bounds__(kEnsureThreads)
   }
   __syncthreads();
   const int nmiss = s_nmiss, nhit = s_nhit;
-  if (nmiss > c.S - nhit) {
+  const int slot_bits = lrfu ? 13 : 16;
+
+  // 3. key the evictable slots (LRU: timestamp, LRFU: decayed score) and,
+  // when there are misses, sort them ascending
+  for (int s = tid; s < spad; s += blockDim.x) {
+    uint64_t k = ~0ull;
+    if (s < c.S && !(hitmask[s >> 5] & (1u << (s & 31))) && !(use_tag && c.pin[s] == use_tag)) {
+      uint64_t v;
+      if (c.slot_key[s] < 0) {
+        v = 0;
+      } else if (lrfu) {
+        const uint64_t crf = c.crf[s];
+        v = min(c.lrfu_k ? crf - (crf >> c.lrfu_k) : crf, kCrfSat);
+      } else {
+        v = static_cast<uint64_t>(c.slot_ts[s]);
+      }
+      k = (v << slot_bits) | static_cast<uint64_t>(s);
+      atomicAdd(&s_navail, 1);
+    }
+    skey[s] = k;
+  }
+  __syncthreads();
+  if (nmiss > s_navail) {
     if (tid == 0) {
       set_status(status, OES_DEV_CAPACITY);
       *n_miss = 0;
@@ -130,18 +169,7 @@ __global__ void __launch_bounds__(kEnsureThreads)
     return;
   }
   const int64_t clock_new = c.ctr[0] + 1;
-
-  // 3. order the evictable slots: (timestamp, slot) ascending
   if (nmiss > 0) {
-    for (int s = tid; s < spad; s += blockDim.x) {
-      uint64_t k = ~0ull;
-      if (s < c.S && !(hitmask[s >> 5] & (1u << (s & 31)))) {
-        const int64_t ts = c.slot_key[s] < 0 ? 0 : c.slot_ts[s];
-        k = (static_cast<uint64_t>(ts) << 16) | static_cast<uint64_t>(s);
-      }
-      skey[s] = k;
-    }
-    __syncthreads();
     for (int kk = 2; kk <= spad; kk <<= 1) {
       for (int j = kk >> 1; j > 0; j >>= 1) {
         for (int i = tid; i < spad; i += blockDim.x) {
@@ -160,12 +188,17 @@ __global__ void __launch_bounds__(kEnsureThreads)
     }
   }
 
-  // 4. fills, evictions and recency
+  // LRFU: every slot decays by one query before the hits and fills
+  if (lrfu && c.lrfu_k)
+    for (int s = tid; s < c.S; s += blockDim.x) c.crf[s] -= c.crf[s] >> c.lrfu_k;
+  __syncthreads();
+
+  // 4. fills, evictions, recency (and LRFU scores and pins)
   if (tid < nvalid) {
     const int k = qkey[tid];
     const int r = qrank[tid];
     if (r >= 0) {
-      const int v = static_cast<int>(skey[r] & 0xFFFFu);
+      const int v = static_cast<int>(skey[r] & ((1u << slot_bits) - 1u));
       const int old = c.slot_key[v];
       if (old >= 0 && old < LE) {
         c.map[old] = -1;
@@ -177,8 +210,13 @@ __global__ void __launch_bounds__(kEnsureThreads)
       miss[3 * r + 0] = k;
       miss[3 * r + 1] = v;
       miss[3 * r + 2] = old;
+      if (lrfu) c.crf[v] = kCrfOne;
+      if (use_tag) c.pin[v] = use_tag;
     } else {
-      c.slot_ts[qslot[tid]] = clock_new;
+      const int h = qslot[tid];
+      c.slot_ts[h] = clock_new;
+      if (lrfu) c.crf[h] = min(c.crf[h] + kCrfOne, kCrfSat);
+      if (use_tag) c.pin[h] = use_tag;
     }
     if (record_stats) c.decode_freq[k] += 1;
   }
@@ -260,6 +298,15 @@ static int release_cache(oes_slot_cache* c) {
   return OES_OK;
 }
 
+// LRFU scores 1.0 for occupied slots, 0 for empty ones; no pins.
+static int reset_lrfu(oes_slot_cache* c, const int32_t* slot_key) {
+  std::vector<uint64_t> crf(c->S);
+  for (int s = 0; s < c->S; ++s) crf[s] = slot_key[s] >= 0 ? kCrfOne : 0;
+  OES_TRY_CUDA(cudaMemcpy(c->crf, crf.data(), (size_t)c->S * 8, cudaMemcpyHostToDevice));
+  OES_TRY_CUDA(cudaMemset(c->pin, 0, (size_t)c->S * 4));
+  return OES_OK;
+}
+
 extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   OES_REQUIRE(out, "slot_cache_create: null out");
   OES_REQUIRE(S >= 1 && S <= OES_MAX_SLOTS, "slot_cache_create: S=%d out of [1, %d]", S,
@@ -272,7 +319,8 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   c->E = E;
   cudaGetDevice(&c->device);
   const size_t LE = (size_t)L * E;
-  const size_t bytes = LE * 4 + (size_t)S * 4 + (size_t)S * 8 + 4 * 8 + LE * 8 + 64;
+  const size_t bytes = LE * 4 + (size_t)S * 4 + (size_t)S * 8 + 4 * 8 + LE * 8 + (size_t)S * 8 +
+                       (size_t)S * 4 + 64;
   c->block_bytes = bytes;
   c->side = nullptr;
   c->fork = c->join = nullptr;
@@ -297,9 +345,16 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   p += 4 * 8;
   c->decode_freq = reinterpret_cast<int64_t*>(p);
   p += LE * 8;
+  c->crf = reinterpret_cast<uint64_t*>(p);
+  p += (size_t)S * 8;
   c->map = reinterpret_cast<int32_t*>(p);
   p += LE * 4;
   c->slot_key = reinterpret_cast<int32_t*>(p);
+  p += (size_t)S * 4;
+  c->pin = reinterpret_cast<int32_t*>(p);
+  c->policy = OES_POLICY_LRU;
+  c->lrfu_k = 0;
+  c->chunk_tag = 0;
   std::vector<int32_t> key(S, -1);
   std::vector<int64_t> ts(S, 0);
   int rc = slot_cache_load_state(c, key.data(), ts.data(), 0);
@@ -344,6 +399,29 @@ extern "C" int slot_cache_load_state(oes_slot_cache* c, const int32_t* slot_key,
   OES_TRY_CUDA(cudaMemcpy(c->slot_ts, ts.data(), (size_t)S * 8, cudaMemcpyHostToDevice));
   OES_TRY_CUDA(cudaMemcpy(c->ctr, ctr, sizeof(ctr), cudaMemcpyHostToDevice));
   OES_TRY_CUDA(cudaMemset(c->decode_freq, 0, LE * 8));
+  return reset_lrfu(c, slot_key);
+}
+
+extern "C" int slot_cache_set_policy(oes_slot_cache* c, int policy, int lrfu_k) {
+  OES_REQUIRE(c, "slot_cache_set_policy: null cache");
+  OES_REQUIRE(policy == OES_POLICY_LRU || policy == OES_POLICY_LRFU,
+              "slot_cache_set_policy: unknown policy %d", policy);
+  OES_REQUIRE(lrfu_k >= 0 && lrfu_k <= OES_LRFU_MAX_K, "slot_cache_set_policy: k=%d out of [0, %d]",
+              lrfu_k, OES_LRFU_MAX_K);
+  OES_TRY_CUDA(cudaDeviceSynchronize());
+  std::vector<int32_t> key(c->S);
+  OES_TRY_CUDA(cudaMemcpy(key.data(), c->slot_key, (size_t)c->S * 4, cudaMemcpyDeviceToHost));
+  c->policy = policy;
+  c->lrfu_k = lrfu_k;
+  return reset_lrfu(c, key.data());
+}
+
+extern "C" int slot_cache_read_lrfu(const oes_slot_cache* c, uint64_t* crf, int32_t* pin,
+                                    oes_stream_t stream) {
+  OES_REQUIRE(c, "slot_cache_read_lrfu: null cache");
+  OES_TRY_CUDA(cudaStreamSynchronize(stream));
+  if (crf) OES_TRY_CUDA(cudaMemcpy(crf, c->crf, (size_t)c->S * 8, cudaMemcpyDeviceToHost));
+  if (pin) OES_TRY_CUDA(cudaMemcpy(pin, c->pin, (size_t)c->S * 4, cudaMemcpyDeviceToHost));
   return OES_OK;
 }
 
@@ -393,9 +471,9 @@ extern "C" int slot_cache_layer_map(const oes_slot_cache* c, int layer, const in
   return OES_OK;
 }
 
-extern "C" int slot_cache_ensure(oes_slot_cache* c, int layer, const int32_t* experts, int n,
-                                 int record_stats, int32_t* miss, int32_t* n_miss, int32_t* status,
-                                 oes_stream_t stream) {
+extern "C" int slot_cache_ensure_tagged(oes_slot_cache* c, int layer, const int32_t* experts,
+                                        int n, int record_stats, int32_t tag, int32_t* miss,
+                                        int32_t* n_miss, int32_t* status, oes_stream_t stream) {
   OES_REQUIRE(c && miss && n_miss && (n == 0 || experts), "slot_cache_ensure: null pointer");
   OES_REQUIRE(layer >= 0 && layer < c->L, "slot_cache_ensure: layer %d out of [0, %d)", layer, c->L);
   OES_REQUIRE(n >= 0 && n <= OES_QUERY_MAX, "slot_cache_ensure: n=%d out of [0, %d]", n,
@@ -416,9 +494,16 @@ extern "C" int slot_cache_ensure(oes_slot_cache* c, int layer, const int32_t* ex
       cudaSharedmemCarveoutMaxShared);
   OES_REQUIRE(carve == cudaSuccess, "slot_cache_ensure: carveout attribute failed");
   ensure_kernel<<<1, kEnsureThreads, smem, stream>>>(view_of(c), layer, experts, n, record_stats,
-                                                     spad, miss, n_miss, status);
+                                                     tag, spad, miss, n_miss, status);
   OES_CHECK_LAUNCH("ensure_kernel");
   return OES_OK;
+}
+
+extern "C" int slot_cache_ensure(oes_slot_cache* c, int layer, const int32_t* experts, int n,
+                                 int record_stats, int32_t* miss, int32_t* n_miss, int32_t* status,
+                                 oes_stream_t stream) {
+  return slot_cache_ensure_tagged(c, layer, experts, n, record_stats, 0, miss, n_miss, status,
+                                  stream);
 }
 
 extern "C" int oes_expert_source_create(const void* const* layer_base, int L, int E,

@@ -23,6 +23,8 @@ from . import build as _build
 OES_OK, OES_ERR_INVALID_ARG, OES_ERR_UNSUPPORTED, OES_ERR_CUDA, OES_ERR_CAPACITY = range(5)
 OES_DEV_CAPACITY, OES_DEV_BAD_ID, OES_DEV_TIMEOUT = 1, 2, 4
 OES_WFMT_BF16, OES_WFMT_NVFP4, OES_WFMT_NVFP4_W4A4 = 0, 1, 2
+OES_POLICY_LRU, OES_POLICY_LRFU = 0, 1
+OES_LRFU_MAX_K = 18
 OES_QUERY_MAX = 128
 OES_MAX_TOPK = 32
 OES_MAX_EXPERTS = 4096
@@ -95,6 +97,9 @@ _SIGS = {
     "moe_layer_forward_stream": (_i, [_vp, _vp, _i, C.POINTER(LayerDesc), C.POINTER(Chunk), _vp,
                                       _vp]),
     "oes_takes_slot_path": (_i, [_i, _i, _i, _i, _i]),
+    "slot_cache_ensure_tagged": (_i, [_vp, _i, _vp, _i, _i, C.c_int32, _vp, _vp, _vp, _vp]),
+    "slot_cache_set_policy": (_i, [_vp, _i, _i]),
+    "slot_cache_read_lrfu": (_i, [_vp, _vp, _vp, _vp]),
     "moe_grouped_gemm_workspace_views": (_i, [C.POINTER(RoutedExperts), _i, _i, _vp, C.POINTER(_vp),
                                               C.POINTER(_vp), C.POINTER(_vp)]),
     "oes_stage_plan_create": (_i, [_vp, C.POINTER(_i), _i, _i, _vp, C.POINTER(_vp)]),
@@ -371,3 +376,20 @@ def moe_grouped_gemm_workspace_views(view, T, k, workspace) -> dict:
     _call("moe_grouped_gemm_workspace_views", C.byref(view), T, k, _ptr(workspace),
           *[C.byref(p) for p in ps])
     return {n: p.value for n, p in zip(["h", "y", "x16"], ps)}
+
+
+def slot_cache_ensure_tagged(cache, layer, experts, n, record_stats, tag, miss, n_miss, status,
+                             stream=None):
+    _call("slot_cache_ensure_tagged", cache, layer, _ptr(experts), n, int(bool(record_stats)), tag,
+          _ptr(miss), _ptr(n_miss), _ptr(status), _stream(stream))
+
+
+def slot_cache_set_policy(cache, policy, lrfu_k=0):
+    _call("slot_cache_set_policy", cache, policy, lrfu_k)
+
+
+def slot_cache_read_lrfu(cache, S, stream=None):
+    crf = np.zeros(S, np.uint64)
+    pin = np.zeros(S, np.int32)
+    _call("slot_cache_read_lrfu", cache, crf.ctypes.data, pin.ctypes.data, _stream(stream))
+    return crf, pin

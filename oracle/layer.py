@@ -69,7 +69,7 @@ def expert_outputs(x_bits, ids, row_of_expert, wfmt, H, I, tokens=None, act=None
 
 
 def forward_slots(cfg, router_in, source_row, cache, pool, block, layer=None,
-                  record_stats=False, tokens=None, query_width=None):
+                  record_stats=False, tokens=None, query_width=None, tag=0):
     """source_row(layer, e) -> host source row bytes; cache: SlotCache;
     pool: dict slot -> row bytes (updated by the copies).
 
@@ -89,7 +89,7 @@ def forward_slots(cfg, router_in, source_row, cache, pool, block, layer=None,
     for q0 in range(0, distinct.size, W):
         part = distinct[q0:q0 + W]
         keys = [layer * E + int(e) if e >= 0 else -1 for e in part]
-        status, misses = cache.ensure(keys, record_stats=record_stats)
+        status, misses = cache.ensure(keys, record_stats=record_stats, tag=tag)
         for key, slot, _old in misses:
             pool[slot] = source_row(key // E, key % E)
         queries.append({"keys": keys, "status": status, "misses": misses})
