@@ -1,11 +1,14 @@
 """Runs the slot path of one workload for a few steps, for a profiler.
 
     python -m offloaded_expert_slot_gb300.profile_case [--config NAME]
-        [--slots S --prefill P] [--steps N]
+        [--slots S --prefill P] [--steps N] [--warm]
 
 Each step restores the cache tables to the workload's seeded pre-fill and
 runs moe_layer_forward_slots on the default stream, as bench.py's timed
-step does.  --slots / --prefill shrink the pool (a smaller case with the
+step does.  --warm skips the restore: from the second step on every expert
+of the chunk is resident, and the GEMM over the hits covers the whole chunk
+in one GEMM1 + GEMM2 launch pair (the first two grouped-GEMM launches of
+that step).  --slots / --prefill shrink the pool (a smaller case with the
 same kernels and shapes, for multi-pass captures).  Exits non-zero if the
 device status is not 0.
 """
@@ -30,6 +33,7 @@ def main() -> int:
     ap.add_argument("--slots", type=int, default=0)
     ap.add_argument("--prefill", type=int, default=-1)
     ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warm", action="store_true")
     a = ap.parse_args()
     cfg = CONFIGS[a.config]
     if a.slots:
@@ -69,13 +73,15 @@ def main() -> int:
     ch = oes.chunk(x, cfg.T, cfg.k, out, status, ws, wsb, logits=logits, gate=gate)
     torch.cuda.synchronize()
     for _ in range(a.steps):
-        oes.slot_cache_restore(cache, snap)
+        if not a.warm:
+            oes.slot_cache_restore(cache, snap)
         oes.moe_layer_forward_slots(cache, src, pool, cfg.layer, desc, ch, 0)
     torch.cuda.synchronize()
     code = int(status.item())
     oes.slot_cache_destroy(cache)
     oes.oes_expert_source_destroy(src)
-    print(f"{cfg.name}: S={cfg.S} prefill={cfg.prefill} steps={a.steps} status={code}")
+    print(f"{cfg.name}: S={cfg.S} prefill={cfg.prefill} steps={a.steps} warm={a.warm} "
+          f"status={code}")
     return 0 if code == 0 else 1
 
 
