@@ -709,6 +709,97 @@ def crossover(args):
     oes.oes_expert_source_destroy(src)
 
 
+def layer_sweep(args):
+    """Every layer of the workload forwarded in turn, as a prefill does:
+      slots    moe_layer_forward_slots layer after layer (the cache evolves;
+               no restore), each layer timed with CUDA events;
+      staged   one plan over all layers + moe_layers_forward_staged
+               (non-resident runs, next layer copied during this layer);
+      serial   moe_layer_forward_stream layer after layer.
+    One JSON line with per-layer times of the slot path and the totals; not
+    the headline."""
+    import torch
+    from offloaded_expert_slot_gb300 import build, oes
+    from offloaded_expert_slot_gb300.inputs import (empty_slot_row, expert_layer_rows,
+                                                    n_source_buffers, pool_prefill,
+                                                    router_inputs, source_layer_index)
+    build.build()
+    oes.load()
+    cfg = CONFIGS[args.config]
+    E, S, rb, L = cfg.E, cfg.S, cfg.row_bytes, cfg.L
+    srcs = []
+    for l in range(n_source_buffers(cfg)):
+        buf = torch.empty((E, rb), dtype=torch.uint8, pin_memory=True)
+        expert_layer_rows(cfg, l, device="cuda", out=buf)
+        srcs.append(buf)
+    src = oes.oes_expert_source_create([srcs[source_layer_index(cfg, l)] for l in range(L)], E, rb)
+    pool_all = torch.empty((S + 2 * E, rb), dtype=torch.uint8, device="cuda")
+    pool = pool_all[:S]
+    cache = oes.slot_cache_create(S, L, E)
+
+    def reset():
+        st = pool_prefill(cfg)
+        oes.slot_cache_load_state(cache, st["slot_key"], st["slot_ts"], st["clock"])
+        pool[:] = torch.from_numpy(empty_slot_row(cfg)).cuda()
+        for s_ in np.nonzero(st["slot_key"] >= 0)[0]:
+            k_ = int(st["slot_key"][s_])
+            pool[int(s_)].copy_(srcs[source_layer_index(cfg, k_ // E)][k_ % E])
+        torch.cuda.synchronize()
+
+    rin = router_inputs(cfg)
+    x = torch.from_numpy(rin["x"].view(np.int16)).cuda()
+    logits = torch.from_numpy(rin["logits"]).cuda()
+    wfmt = oes.OES_WFMT_BF16 if cfg.wfmt == "bf16" else oes.OES_WFMT_NVFP4
+    desc = oes.layer_desc(E, cfg.H, cfg.I, wfmt)
+    wsb = oes.moe_layer_workspace_size(desc, cfg.T, cfg.k)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    out = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ch = oes.chunk(x, cfg.T, cfg.k, out, status, ws, wsb, logits=logits)
+    copy_stream = torch.cuda.Stream()
+    layers = list(range(L))
+
+    def ev():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()
+        return e
+
+    reset()
+    oes.moe_layer_forward_slots(cache, src, pool, 0, desc, ch, 0)       # warm-up
+    reset()
+    marks = [ev()]
+    for l in layers:
+        oes.moe_layer_forward_slots(cache, src, pool, l, desc, ch, 0)
+        marks.append(ev())
+    torch.cuda.synchronize()
+    per_layer = [marks[i].elapsed_time(marks[i + 1]) for i in range(L)]
+    reset()
+    t0 = ev()
+    plan = oes.oes_stage_plan_create(cache, layers, True)
+    oes.moe_layers_forward_staged(plan, src, pool_all, desc, [ch] * L, copy_stream=copy_stream)
+    t1 = ev()
+    torch.cuda.synchronize()
+    oes.oes_stage_plan_destroy(plan)
+    staged = t0.elapsed_time(t1)
+    buf = pool_all[S:S + E]
+    t0 = ev()
+    for l in layers:
+        oes.moe_layer_forward_stream(src, buf, l, desc, ch, copy_stream=copy_stream)
+    t1 = ev()
+    torch.cuda.synchronize()
+    serial = t0.elapsed_time(t1)
+    assert int(status.item()) == 0, int(status.item())
+    print(json.dumps({"layer_sweep": cfg.name, "layers": L, "T": cfg.T, "k": cfg.k, "E": E,
+                      "slots": S, "wfmt": cfg.wfmt,
+                      "slots_ms_per_layer": [round(v, 4) for v in per_layer],
+                      "slots_total_ms": sum(per_layer),
+                      "slots_median_ms": float(np.median(per_layer)),
+                      "staged_total_ms": staged, "serial_stream_total_ms": serial,
+                      "layer_bytes": E * rb}), flush=True)
+    oes.slot_cache_destroy(cache)
+    oes.oes_expert_source_destroy(src)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -720,7 +811,12 @@ def main():
                     help="bandwidth sweep of the routing and align kernels (not the headline)")
     ap.add_argument("--crossover", action="store_true",
                     help="slot path vs staged whole-layer path per chunk size (not the headline)")
+    ap.add_argument("--layers", action="store_true",
+                    help="every layer of the workload in turn: slot path, staged, streamed")
     args = ap.parse_args()
+    if args.layers:
+        layer_sweep(args)
+        return
     if args.crossover:
         crossover(args)
         return
