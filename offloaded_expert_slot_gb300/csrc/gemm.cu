@@ -113,6 +113,75 @@ struct UnitRec {  // shared-memory copy of a Unit
   int b, m, slot, nvalid;
 };
 
+// Number of routes of block b (padding, value R, only at its end).
+__device__ __forceinline__ int block_nvalid(const GemmParams& p, int b) {
+  const int32_t* s = p.sorted_ids + (int64_t)b * p.BN;
+  if (s[p.BN - 1] < p.R) return p.BN;
+  int lo = 0, hi = p.BN - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (s[mid] < p.R) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// A filtered launch deals out only the units of the selected blocks, densely,
+// so that its CTAs get equal shares: the selected block of rank g (blocks in
+// order) owns units g * n_mtiles + m (tile fastest, as everywhere), and this
+// CTA takes every gridDim.x-th of them into its table.  Every CTA computes the
+// same ranks.  Returns the number of units, or -1 when this CTA's share would
+// not fit the table (the caller then numbers units as an unfiltered launch and
+// skips the filtered ones).  All threads of the CTA call it.
+__device__ int fill_filtered_units(const GemmParams& p, int nb, UnitRec* utab, int* s_scan) {
+  const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  const int nw = nthr >> 5;
+  auto selected = [&](int b) {
+    const int e = p.block_expert[b];
+    return e >= 0 && e < p.E && p.flags[e] == p.filter && p.sorted_ids[(int64_t)b * p.BN] < p.R;
+  };
+  int mine = 0;
+  for (int b = tid; b < nb; b += nthr) mine += selected(b) ? 1 : 0;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+  if (lane == 0) s_scan[warp] = mine;
+  __syncthreads();
+  if (tid == 0) {
+    int n = 0;
+    for (int i = 0; i < nw; ++i) n += s_scan[i];
+    s_scan[32] = n;
+  }
+  __syncthreads();
+  const int units = s_scan[32] * p.n_mtiles;
+  __syncthreads();
+  if (units > kMaxUnitsPerCta * (int)gridDim.x) return -1;
+  int base = 0;
+  for (int b0 = 0; b0 < nb; b0 += nthr) {
+    const int b = b0 + tid;
+    const bool sel = b < nb && selected(b);
+    const unsigned bal = __ballot_sync(0xffffffffu, sel);
+    if (lane == 0) s_scan[warp] = __popc(bal);
+    __syncthreads();
+    int off = base, chunk = 0;
+    for (int i = 0; i < nw; ++i) {
+      if (i < warp) off += s_scan[i];
+      chunk += s_scan[i];
+    }
+    if (sel) {
+      const int g = off + __popc(bal & ((1u << lane) - 1u));
+      const int nvalid = block_nvalid(p, b);
+      const int slot = p.e2s[p.block_expert[b]];
+      for (int m = 0; m < p.n_mtiles; ++m) {
+        const int v = g * p.n_mtiles + m;
+        if (v % (int)gridDim.x == (int)blockIdx.x) utab[v / gridDim.x] = UnitRec{b, m, slot, nvalid};
+      }
+    }
+    base += chunk;
+    __syncthreads();
+  }
+  return units;
+}
+
 // The CTA's u-th unit (u counted in this CTA's sequence), from the table
 // filled at kernel start, or computed directly past the table's end.
 __device__ __forceinline__ Unit my_unit(const GemmParams& p, const UnitRec* tab, int idx, int u, int nb) {
@@ -290,15 +359,21 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
   const uint32_t tmem_base = *tmem_holder;
 
   const int nb = *p.n_post_pad / p.BN;
-  const int total = nb * p.n_mtiles;
+  int total = nb * p.n_mtiles;
   const uint32_t acc_cols = (MODE == 1) ? 2 * p.BN : p.BN;
-  // every thread looks up one of this CTA's units (independent loads in
-  // parallel), so the roles below never wait on global memory for them
-  for (int i = threadIdx.x; i < kMaxUnitsPerCta; i += blockDim.x) {
-    const int u = blockIdx.x + i * gridDim.x;
-    if (u >= total) break;
-    const Unit t = unit_info(p, u, nb);
-    utab[i] = UnitRec{t.b, t.m, t.slot, t.nvalid};
+  __shared__ int s_scan[33];
+  const int dense = p.filter ? fill_filtered_units(p, nb, utab, s_scan) : -1;
+  if (dense >= 0) {
+    total = dense;
+  } else {
+    // every thread looks up one of this CTA's units (independent loads in
+    // parallel), so the roles below never wait on global memory for them
+    for (int i = threadIdx.x; i < kMaxUnitsPerCta; i += blockDim.x) {
+      const int u = blockIdx.x + i * gridDim.x;
+      if (u >= total) break;
+      const Unit t = unit_info(p, u, nb);
+      utab[i] = UnitRec{t.b, t.m, t.slot, t.nvalid};
+    }
   }
   __syncthreads();
 
@@ -640,12 +715,18 @@ __global__ void __maxnreg__(64)
   const uint32_t tmem_base = *tmem_holder;
 
   const int nb = *p.n_post_pad / p.BN;
-  const int total = nb * p.n_mtiles;
-  for (int i = threadIdx.x; i < kMaxUnitsPerCta; i += blockDim.x) {
-    const int u = blockIdx.x + i * gridDim.x;
-    if (u >= total) break;
-    const Unit t = unit_info(p, u, nb);
-    utab[i] = UnitRec{t.b, t.m, t.slot, t.nvalid};
+  int total = nb * p.n_mtiles;
+  __shared__ int s_scan[33];
+  const int dense = p.filter ? fill_filtered_units(p, nb, utab, s_scan) : -1;
+  if (dense >= 0) {
+    total = dense;
+  } else {
+    for (int i = threadIdx.x; i < kMaxUnitsPerCta; i += blockDim.x) {
+      const int u = blockIdx.x + i * gridDim.x;
+      if (u >= total) break;
+      const Unit t = unit_info(p, u, nb);
+      utab[i] = UnitRec{t.b, t.m, t.slot, t.nvalid};
+    }
   }
   __syncthreads();
 
@@ -1103,8 +1184,12 @@ int launch_gemm_tm(const GemmMaps& maps, const GemmParams& p0, cudaStream_t stre
   p.tmem_cols = 512;
   static bool configured = false;
   if (!configured) {
+    // the largest dynamic size the kernel's own static shared memory leaves
+    cudaFuncAttributes fa{};
+    OES_TRY_CUDA(cudaFuncGetAttributes(&fa, grouped_gemm_tm_kernel<MODE, WF>));
     OES_TRY_CUDA(cudaFuncSetAttribute(grouped_gemm_tm_kernel<MODE, WF>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024));
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      227 * 1024 - (int)fa.sharedSizeBytes));
     configured = true;
   }
   grouped_gemm_tm_kernel<MODE, WF><<<num_sms(), gemm_threads_tm(WF), smem, stream>>>(maps, p);
@@ -1125,8 +1210,12 @@ int launch_gemm(const GemmMaps& maps, const GemmParams& p0, int BN, cudaStream_t
   if (p.tmem_cols < 32) p.tmem_cols = 32;
   static bool configured = false;
   if (!configured) {
+    // the largest dynamic size the kernel's own static shared memory leaves
+    cudaFuncAttributes fa{};
+    OES_TRY_CUDA(cudaFuncGetAttributes(&fa, grouped_gemm_kernel<MODE, WF>));
     OES_TRY_CUDA(cudaFuncSetAttribute(grouped_gemm_kernel<MODE, WF>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024));
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      227 * 1024 - (int)fa.sharedSizeBytes));
     configured = true;
   }
   grouped_gemm_kernel<MODE, WF><<<num_sms(), gemm_threads(WF), smem, stream>>>(maps, p);

@@ -30,7 +30,7 @@ struct LayerWs {
   int32_t* block_expert;
   int32_t* n_post_pad;
   int32_t* e2s_identity;
-  uint8_t* resident;  // [E] expert resident before the chunk
+  uint8_t* resident;  // [E] group of each of the chunk's experts (hit, or missed in query q)
   void* align_ws;
   size_t align_bytes;
   void* gemm_ws;
