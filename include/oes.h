@@ -2,15 +2,15 @@
  * oes.h -- offloaded expert slots: the C ABI of the offloaded-MoE layer
  * forward over a GPU slot cache, for one NVIDIA GB300 (sm_103a).
  *
- * The path (FreeToken PR #676 "--moe-prefill-demand-tokens", Solution):
+ * The path (FreeToken PR #676, Solution: the demand-token prefill):
  * a chunk is routed top-k; its distinct experts, a sorted list of fixed
- * length, are admitted into an LRU slot cache in queries of at most 128 ids,
- * each query's misses copied from a pinned-host expert source before the
- * next query evicts; routes are sorted into per-expert blocks
- * (moe_align_block_size); the grouped SwiGLU expert GEMM runs over the slot
- * pool through an expert->slot remap with its tiles sized by the layer's
- * expert count, and it gives exactly the bytes the same GEMM gives over the
- * whole streamed layer.
+ * length, are admitted into an LRU (or LRFU) slot cache in queries of at most
+ * 128 ids; each query's misses are copied from a pinned-host expert source,
+ * and no query evicts a slot an earlier query of the chunk touched; routes
+ * are sorted into per-expert blocks (moe_align_block_size); the grouped
+ * SwiGLU expert GEMM runs over the slot pool through an expert->slot remap
+ * with its tiles sized by the layer's expert count, and it gives exactly the
+ * bytes the same GEMM gives over the whole streamed layer.
  *
  * Conventions for every call:
  *   - Pointers are raw addresses.  "device" = GPU global memory; "host" =
@@ -20,8 +20,9 @@
  *     small device tables behind the two opaque handles (oes_slot_cache,
  *     oes_expert_source), created and destroyed explicitly.
  *   - Calls are asynchronous on the given stream and never synchronise the
- *     host, except the *_load_state / *_read_state / *_create / *_destroy
- *     calls, which say so.
+ *     host, except the *_load_state / *_read_state / *_read_lrfu /
+ *     *_set_policy / *_create / *_destroy calls and oes_stage_plan_create,
+ *     which say so.
  *   - The return value reports what the host can check before launching:
  *     OES_OK, OES_ERR_INVALID_ARG (null pointer, size out of range, buffer
  *     too small), OES_ERR_UNSUPPORTED (a size this build does not handle),
