@@ -203,6 +203,19 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
   asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(r) : "r"(byte));
   return r;
 }
+// Four e2m1 pairs (one 32-bit word, element 2i in the low nibble of byte i)
+// -> four f16x2, byte i -> o[i]; the word is split into bytes by one vector
+// move instead of a shift and a narrowing convert per byte.
+__device__ __forceinline__ void cvt_e2m1x8_f16x2(uint32_t wd, uint32_t (&o)[4]) {
+  asm("{ .reg .b8 b0, b1, b2, b3;\n"
+      "  mov.b32 {b0, b1, b2, b3}, %4;\n"
+      "  cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+      "  cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      "  cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+      "  cvt.rn.f16x2.e2m1x2 %3, b3; }"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(wd));
+}
 __device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t two) {
   uint32_t r;
   asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(r) : "r"(two));
@@ -286,11 +299,13 @@ __device__ __forceinline__ void convert_row(const uint8_t* q, uint32_t scales, u
     if (c < c_begin || c >= c_end) continue;
     const uint32_t wd = words[c];
     const uint32_t s = sc[c >> 1];
+    uint32_t f[4];
+    cvt_e2m1x8_f16x2(wd, f);
     uint4 o;
-    o.x = hmul2_u32(cvt_e2m1x2_f16x2(wd & 0xFFu), s);
-    o.y = hmul2_u32(cvt_e2m1x2_f16x2((wd >> 8) & 0xFFu), s);
-    o.z = hmul2_u32(cvt_e2m1x2_f16x2((wd >> 16) & 0xFFu), s);
-    o.w = hmul2_u32(cvt_e2m1x2_f16x2(wd >> 24), s);
+    o.x = hmul2_u32(f[0], s);
+    o.y = hmul2_u32(f[1], s);
+    o.z = hmul2_u32(f[2], s);
+    o.w = hmul2_u32(f[3], s);
     *reinterpret_cast<uint4*>(rowp + ((c ^ sw) << 4)) = o;
   }
 }
