@@ -35,7 +35,9 @@ W4A4_WM = scaled(C4, name="w4a4_weight_major", T=40, k=3, E=16, H=256, I=192, S=
 
 
 def f16_values(t: torch.Tensor) -> np.ndarray:
-    return t.cpu().numpy().view(np.float16).astype(np.float64)
+    # workspace regions include padding rows no kernel writes (any bits)
+    with np.errstate(invalid="ignore"):
+        return t.cpu().numpy().view(np.float16).astype(np.float64)
 
 
 @pytest.mark.parametrize("cfg", [W4A4_TM, W4A4_WM], ids=lambda c: c.name)
