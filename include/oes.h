@@ -200,7 +200,14 @@ int slot_cache_ensure(oes_slot_cache *cache, int layer, const int32_t *experts, 
  * the victims every slot pinned to it and pins every slot the query touches,
  * so the queries of one chunk, sharing a tag, never evict one another's
  * slots.  Under LRU the tag is ignored (LRU already takes those slots last).
- * moe_layer_forward_slots hands each call a new tag. */
+ * tag > 0 is used as given; OES_TAG_NEW_CHUNK draws the next tag from a
+ * counter in the cache's device tables (1, 2, ...; reset by load_state and
+ * set_policy, part of a snapshot) and OES_TAG_SAME_CHUNK reuses the last
+ * one drawn, so a chunk replayed from a CUDA graph still gets a fresh tag.
+ * moe_layer_forward_slots passes OES_TAG_NEW_CHUNK for its first query and
+ * OES_TAG_SAME_CHUNK for the others. */
+#define OES_TAG_NEW_CHUNK (-1)
+#define OES_TAG_SAME_CHUNK (-2)
 int slot_cache_ensure_tagged(oes_slot_cache *cache, int layer, const int32_t *experts, int n,
                              int record_stats, int32_t tag, int32_t *miss, int32_t *n_miss,
                              int32_t *status, oes_stream_t stream);

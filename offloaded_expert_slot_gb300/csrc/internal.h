@@ -21,7 +21,6 @@ struct oes_slot_cache {
   uint64_t* crf;         // [S] LRFU score of each slot, Q32.32
   int32_t* pin;          // [S] LRFU pin tag of each slot, 0 = none
   int policy, lrfu_k;    // OES_POLICY_*, LRFU decay shift
-  int32_t chunk_tag;     // last pin tag moe_layer_forward_slots handed out
   // side stream and events of moe_layer_forward_slots: the later queries'
   // ensures and every GEMM run there while the misses are copied on the
   // caller's stream; ensured[q] / copied[q] mark query q's ensure and copies

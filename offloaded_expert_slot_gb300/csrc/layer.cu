@@ -186,14 +186,14 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
   const int Q = (Lq + OES_QUERY_MAX - 1) / OES_QUERY_MAX;
   cudaStream_t side = cache->side;
   auto miss_of = [&](int q) { return w.miss + (size_t)q * 3 * OES_QUERY_MAX; };
-  // the chunk's pin tag: its queries never evict one another's slots under
-  // a scored policy (LRU ignores it)
-  cache->chunk_tag = cache->chunk_tag == INT32_MAX ? 1 : cache->chunk_tag + 1;
-  const int32_t tag = cache->chunk_tag;
+  // the chunk's pin tag, drawn on the device by its first query: its
+  // queries never evict one another's slots under a scored policy (LRU
+  // ignores it), also when the call is replayed from a CUDA graph
   auto query = [&](int q, cudaStream_t s) {
     const int n = std::min(OES_QUERY_MAX, Lq - q * OES_QUERY_MAX);
     return slot_cache_ensure_tagged(cache, layer, w.distinct + q * OES_QUERY_MAX, n, record_stats,
-                                    tag, miss_of(q), w.n_miss + q, c->status, s);
+                                    q == 0 ? OES_TAG_NEW_CHUNK : OES_TAG_SAME_CHUNK, miss_of(q),
+                                    w.n_miss + q, c->status, s);
   };
   auto copy = [&](int q, cudaStream_t s) {
     const int n = std::min(OES_QUERY_MAX, Lq - q * OES_QUERY_MAX);

@@ -9,6 +9,7 @@
 // (layer, expert), and the rows move by a fixed-grid kernel that reads the
 // mapped host memory directly.
 #include <algorithm>
+#include <climits>
 #include <vector>
 
 #include "common.cuh"
@@ -64,14 +65,26 @@ __global__ void __launch_bounds__(kEnsureThreads)
   const int LE = c.L * c.E;
 
   const bool lrfu = c.policy == OES_POLICY_LRFU;
-  const int use_tag = lrfu ? tag : 0;
+  __shared__ int32_t s_tag;
   if (tid == 0) {
     s_bad = 0;
     s_evict = 0;
     s_navail = 0;
+    // OES_TAG_NEW_CHUNK takes the next chunk tag from the tables (so that a
+    // replayed graph gets a fresh one every time), OES_TAG_SAME_CHUNK the
+    // current one; any other value is the tag itself
+    int64_t t = tag;
+    if (tag == OES_TAG_NEW_CHUNK) {
+      t = c.ctr[4] >= INT32_MAX ? 1 : c.ctr[4] + 1;
+      c.ctr[4] = t;
+    } else if (tag == OES_TAG_SAME_CHUNK) {
+      t = c.ctr[4];
+    }
+    s_tag = static_cast<int32_t>(t);
   }
   for (int i = tid; i < (c.S + 31) / 32; i += blockDim.x) hitmask[i] = 0;
   __syncthreads();
+  const int use_tag = lrfu ? s_tag : 0;
 
   // 1. compact the valid ids of the query into keys
   int key = -1;
@@ -304,6 +317,7 @@ static int reset_lrfu(oes_slot_cache* c, const int32_t* slot_key) {
   for (int s = 0; s < c->S; ++s) crf[s] = slot_key[s] >= 0 ? kCrfOne : 0;
   OES_TRY_CUDA(cudaMemcpy(c->crf, crf.data(), (size_t)c->S * 8, cudaMemcpyHostToDevice));
   OES_TRY_CUDA(cudaMemset(c->pin, 0, (size_t)c->S * 4));
+  OES_TRY_CUDA(cudaMemset(c->ctr + 4, 0, 8));  // chunk tags start again at 1
   return OES_OK;
 }
 
@@ -319,7 +333,7 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   c->E = E;
   cudaGetDevice(&c->device);
   const size_t LE = (size_t)L * E;
-  const size_t bytes = LE * 4 + (size_t)S * 4 + (size_t)S * 8 + 4 * 8 + LE * 8 + (size_t)S * 8 +
+  const size_t bytes = LE * 4 + (size_t)S * 4 + (size_t)S * 8 + 8 * 8 + LE * 8 + (size_t)S * 8 +
                        (size_t)S * 4 + 64;
   c->block_bytes = bytes;
   c->side = nullptr;
@@ -341,8 +355,8 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   uint8_t* p = static_cast<uint8_t*>(c->block);
   c->slot_ts = reinterpret_cast<int64_t*>(p);
   p += (size_t)S * 8;
-  c->ctr = reinterpret_cast<int64_t*>(p);
-  p += 4 * 8;
+  c->ctr = reinterpret_cast<int64_t*>(p);  // clock, hits, misses, evictions, chunk tag
+  p += 8 * 8;
   c->decode_freq = reinterpret_cast<int64_t*>(p);
   p += LE * 8;
   c->crf = reinterpret_cast<uint64_t*>(p);
@@ -354,7 +368,6 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   c->pin = reinterpret_cast<int32_t*>(p);
   c->policy = OES_POLICY_LRU;
   c->lrfu_k = 0;
-  c->chunk_tag = 0;
   std::vector<int32_t> key(S, -1);
   std::vector<int64_t> ts(S, 0);
   int rc = slot_cache_load_state(c, key.data(), ts.data(), 0);
@@ -393,7 +406,7 @@ extern "C" int slot_cache_load_state(oes_slot_cache* c, const int32_t* slot_key,
   }
   std::vector<int64_t> ts(S);
   for (int s = 0; s < S; ++s) ts[s] = slot_key[s] < 0 ? 0 : slot_ts[s];
-  int64_t ctr[4] = {clock, 0, 0, 0};
+  int64_t ctr[8] = {clock, 0, 0, 0, 0, 0, 0, 0};
   OES_TRY_CUDA(cudaMemcpy(c->map, map.data(), LE * 4, cudaMemcpyHostToDevice));
   OES_TRY_CUDA(cudaMemcpy(c->slot_key, slot_key, (size_t)S * 4, cudaMemcpyHostToDevice));
   OES_TRY_CUDA(cudaMemcpy(c->slot_ts, ts.data(), (size_t)S * 8, cudaMemcpyHostToDevice));
@@ -476,6 +489,8 @@ extern "C" int slot_cache_ensure_tagged(oes_slot_cache* c, int layer, const int3
                                         int32_t* n_miss, int32_t* status, oes_stream_t stream) {
   OES_REQUIRE(c && miss && n_miss && (n == 0 || experts), "slot_cache_ensure: null pointer");
   OES_REQUIRE(layer >= 0 && layer < c->L, "slot_cache_ensure: layer %d out of [0, %d)", layer, c->L);
+  OES_REQUIRE(tag >= 0 || tag == OES_TAG_NEW_CHUNK || tag == OES_TAG_SAME_CHUNK,
+              "slot_cache_ensure_tagged: tag %d is neither >= 0 nor a chunk-tag code", tag);
   OES_REQUIRE(n >= 0 && n <= OES_QUERY_MAX, "slot_cache_ensure: n=%d out of [0, %d]", n,
               OES_QUERY_MAX);
   int spad = 2;

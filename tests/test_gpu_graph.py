@@ -42,13 +42,23 @@ def tables(w):
     return oes.slot_cache_read_state(w.cache, cfg.S, cfg.L, cfg.E)
 
 
-def test_decode_step_graph_replays_match_eager_and_oracle():
+@pytest.mark.parametrize("policy", ["lru", "lrfu"])
+def test_decode_step_graph_replays_match_eager_and_oracle(policy):
+    """Under LRFU each replay must draw a fresh chunk pin tag on the device,
+    as each eager call does; a tag fixed in the graph would leave the last
+    step's pins in force."""
     lib()
     cfg = GRAPH_DECODE
+    k = 3
+
+    def set_policy(w):
+        if policy == "lrfu":
+            oes.slot_cache_set_policy(w.cache, oes.OES_POLICY_LRFU, k)
     ins = [step_inputs(cfg, s) for s in range(STEPS)]
 
     # eager reference on its own cache
     we = Workload(cfg, gen_device="cpu")
+    set_policy(we)
     re_ = Run(we)
     eager_out, eager_tab = [], []
     for rin in ins:
@@ -57,10 +67,12 @@ def test_decode_step_graph_replays_match_eager_and_oracle():
         torch.cuda.synchronize()
         assert int(re_.status.item()) == 0
         eager_out.append(re_.out.clone())
-        eager_tab.append(tables(we))
+        eager_tab.append(tables(we) | dict(zip(("crf", "pin"), oes.slot_cache_read_lrfu(we.cache,
+                                                                                      cfg.S))))
 
     # graph: one eager warm-up (one-time kernel attributes), back to the pre-fill, capture
     wg = Workload(cfg, gen_device="cpu")
+    set_policy(wg)
     rg = Run(wg)
     load_step(wg, ins[0])
     oes.moe_layer_forward_slots(wg.cache, wg.src, wg.pool, cfg.layer, rg.desc, rg.chunk, 1)
@@ -75,6 +87,8 @@ def test_decode_step_graph_replays_match_eager_and_oracle():
 
     ocache = SlotCache.from_state(cfg.S, cfg.L, cfg.E, wg.prefill["slot_key"],
                                   wg.prefill["slot_ts"], wg.prefill["clock"])
+    if policy == "lrfu":
+        ocache.set_policy("lrfu", k)
     opool = wg.oracle_pool()
     B = oes.oes_tile_plan(cfg.T * cfg.k, cfg.E)
     n_queries = []
@@ -85,13 +99,15 @@ def test_decode_step_graph_replays_match_eager_and_oracle():
         assert int(rg.status.item()) == 0
         assert torch.equal(rg.out.view(torch.int16), eager_out[s].view(torch.int16)), s
         t = tables(wg)
-        for key in ("map", "slot_key", "slot_ts", "decode_freq"):
+        t |= dict(zip(("crf", "pin"), oes.slot_cache_read_lrfu(wg.cache, cfg.S)))
+        for key in ("map", "slot_key", "slot_ts", "decode_freq", "crf", "pin"):
             assert np.array_equal(t[key], eager_tab[s][key]), (s, key)
         o = forward_slots(scaled(cfg, seed=cfg.seed + 101 * s), rin, wg.source_row, ocache, opool,
-                          block=B, record_stats=True)
+                          block=B, record_stats=True, tag=s + 1)
         n_queries.append(len(o["queries"]))
         assert np.array_equal(t["map"], ocache.map) and np.array_equal(t["slot_ts"], ocache.slot_ts)
         assert np.array_equal(t["decode_freq"], ocache.decode_freq)
+        assert [int(v) for v in t["crf"]] == ocache.crf and [int(v) for v in t["pin"]] == ocache.pin
         assert (t["hits"], t["misses"], t["evictions"]) == (ocache.hits, ocache.misses,
                                                           ocache.evictions)
         check_close(rg.out, o["out"], "bf16")
