@@ -17,8 +17,10 @@
  *     ordinary host memory; "mapped" = pinned host memory the GPU can read
  *     (cudaHostAlloc / cudaHostRegister; on GB300 any pinned allocation).
  *   - The caller allocates and owns every buffer.  The library owns only the
- *     small device tables behind the two opaque handles (oes_slot_cache,
- *     oes_expert_source), created and destroyed explicitly.
+ *     small device tables (and the streams and events) behind the opaque
+ *     handles oes_slot_cache, oes_expert_source and oes_stage_plan, created
+ *     and destroyed explicitly, and the fixed scratch of
+ *     moe_align_block_size_noalloc.
  *   - Calls are asynchronous on the given stream and never synchronise the
  *     host, except the *_load_state / *_read_state / *_read_lrfu /
  *     *_set_policy / *_create / *_destroy calls and oes_stage_plan_create,
