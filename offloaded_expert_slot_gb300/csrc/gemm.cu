@@ -1277,12 +1277,13 @@ extern "C" int moe_grouped_gemm_workspace_views(const oes_routed_experts* v, int
 
 namespace oes {
 
-// Validates the call, writes the f16 copy of x (NVFP4), and builds the tensor
-// maps and kernel parameters of both GEMMs.
+// Validates the call and builds the tensor maps and kernel parameters of both
+// GEMMs, on the host only: nothing is launched, so a composite call can
+// validate its GEMM before it changes any state.  gemm_prepare_x then writes
+// the GEMMs' 16-bit copy of x (NVFP4 weights).
 int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
                  const int32_t* sorted_ids, const int32_t* block_expert, const int32_t* n_post_pad,
-                 int B, void* workspace, size_t workspace_bytes, int32_t* status, cudaStream_t stream,
-                 GemmPlan* g) {
+                 int B, void* workspace, size_t workspace_bytes, int32_t* status, GemmPlan* g) {
   OES_REQUIRE(v && x && sorted_ids && block_expert && n_post_pad && workspace && v->pool && v->e2s,
               "moe_grouped_gemm_slots: null pointer");
   const int E = v->E, H = v->H, I = v->I, S = v->S;
@@ -1328,20 +1329,14 @@ int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
   GemmMaps m1{}, m2{};
   int rc;
   const uint16_t* xb = x;
-  if (a4) {
-    act_scale_kernel<<<1, 256, 0, stream>>>(v->input_scale13, v->input_scale2, E, ws.act, status);
-    OES_CHECK_LAUNCH("act_scale_kernel");
-    const int64_t nblk = (int64_t)T * H / 16;
-    const int blocks = (int)std::min<int64_t>(ceil_div64(nblk, 256), (int64_t)num_sms() * 8);
-    x_quant_kernel<<<blocks, 256, 0, stream>>>(x, ws.x16, nblk, ws.act);
-    OES_CHECK_LAUNCH("x_quant_kernel");
-    xb = ws.x16;
-  } else if (wf) {
-    const int blocks = (int)std::min<int64_t>(ceil_div64((int64_t)T * H, 256), (int64_t)num_sms() * 8);
-    x_to_f16_kernel<<<blocks, 256, 0, stream>>>(x, ws.x16, (int64_t)T * H);
-    OES_CHECK_LAUNCH("x_to_f16_kernel");
-    xb = ws.x16;
-  }
+  g->a4 = a4;
+  g->x = x;
+  g->x16 = ws.x16;
+  g->act = ws.act;
+  g->in13 = v->input_scale13;
+  g->in2 = v->input_scale2;
+  g->status = status;
+  if (wf) xb = ws.x16;
   const CUtensorMapDataType t16 = wf ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   {
     const uint64_t dims[2] = {(uint64_t)I, (uint64_t)cap};
@@ -1416,6 +1411,26 @@ int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
   return OES_OK;
 }
 
+// The x kernels of a prepared GEMM: the f16 copy of x (NVFP4 weights), or for
+// W4A4 the layer's activation scales and the quantised x.
+int gemm_prepare_x(const GemmPlan& g, cudaStream_t stream) {
+  if (g.empty || !g.wf) return OES_OK;
+  const int64_t n = (int64_t)g.T * g.H;
+  if (g.a4) {
+    act_scale_kernel<<<1, 256, 0, stream>>>(g.in13, g.in2, g.E, g.act, g.status);
+    OES_CHECK_LAUNCH("act_scale_kernel");
+    const int64_t nblk = n / 16;
+    const int blocks = (int)std::min<int64_t>(ceil_div64(nblk, 256), (int64_t)num_sms() * 8);
+    x_quant_kernel<<<blocks, 256, 0, stream>>>(g.x, g.x16, nblk, g.act);
+    OES_CHECK_LAUNCH("x_quant_kernel");
+  } else {
+    const int blocks = (int)std::min<int64_t>(ceil_div64(n, 256), (int64_t)num_sms() * 8);
+    x_to_f16_kernel<<<blocks, 256, 0, stream>>>(g.x, g.x16, n);
+    OES_CHECK_LAUNCH("x_to_f16_kernel");
+  }
+  return OES_OK;
+}
+
 // GEMM1 then GEMM2 over the blocks `filter` selects (flags: device [E]
 // group of each expert; filter 0 = every block).
 int gemm_run(const GemmPlan& g, int filter, const uint8_t* flags, cudaStream_t stream) {
@@ -1456,8 +1471,9 @@ extern "C" int moe_grouped_gemm_slots(const oes_routed_experts* v, const uint16_
   OES_REQUIRE(ids && weights && out, "moe_grouped_gemm_slots: null pointer");
   GemmPlan g;
   int rc = gemm_prepare(v, x, T, k, sorted_ids, block_expert, n_post_pad, B, workspace,
-                        workspace_bytes, status, stream, &g);
+                        workspace_bytes, status, &g);
   if (rc) return rc;
+  if ((rc = gemm_prepare_x(g, stream))) return rc;
   if ((rc = gemm_run(g, 0, nullptr, stream))) return rc;
   return gemm_combine(g, ids, weights, out, stream);
 }

@@ -44,14 +44,21 @@ struct GemmPlan {
   GemmMaps m1, m2;
   GemmParams p1, p2;
   bool empty, tm;
-  int wf, T, k, H, E;
+  int wf, a4, T, k, H, E;
   uint16_t* y;
+  const uint16_t* x;        // the chunk's x (bf16)
+  uint16_t* x16;            // its 16-bit copy for NVFP4 weights (workspace)
+  float* act;               // W4A4 activation scales (workspace)
+  const float *in13, *in2;  // W4A4: the layer's input scales
+  int32_t* status;
 };
 
+// host only: validation, tensor maps, kernel parameters
 int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
                  const int32_t* sorted_ids, const int32_t* block_expert, const int32_t* n_post_pad,
-                 int B, void* workspace, size_t workspace_bytes, int32_t* status, cudaStream_t stream,
-                 GemmPlan* plan);
+                 int B, void* workspace, size_t workspace_bytes, int32_t* status, GemmPlan* plan);
+// the x kernels of a prepared GEMM (NVFP4 weights), on `stream`
+int gemm_prepare_x(const GemmPlan& plan, cudaStream_t stream);
 // filter: 0 every block; g > 0 the blocks of experts with flags[e] == g
 int gemm_run(const GemmPlan& plan, int filter, const uint8_t* flags, cudaStream_t stream);
 int gemm_combine(const GemmPlan& plan, const int32_t* ids, const float* weights, uint16_t* out,

@@ -199,6 +199,24 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
     const int n = std::min(OES_QUERY_MAX, Lq - q * OES_QUERY_MAX);
     return slot_cache_copy_misses(src, pool, cache->S, miss_of(q), w.n_miss + q, n, c->status, s);
   };
+  // the GEMM is validated and its parameters built before anything is
+  // launched: a call that fails here leaves the cache as it was
+  oes_routed_experts v{};
+  v.layer = layer;
+  v.E = E;
+  v.e2s = cache->map + (size_t)layer * E;
+  v.wfmt = d->wfmt;
+  v.pool = pool;
+  v.row_bytes = src->row_bytes;
+  v.S = cache->S;
+  v.H = d->H;
+  v.I = d->I;
+  v.input_scale13 = d->input_scale13;
+  v.input_scale2 = d->input_scale2;
+  GemmPlan g;
+  if ((rc = gemm_prepare(&v, c->x, T, k, w.sorted_ids, w.block_expert, w.n_post_pad, B, w.gemm_ws,
+                         w.gemm_bytes, c->status, &g)))
+    return rc;
   // caller's stream: route, distinct experts, the first query
   if ((rc = route(d, c, w, stream))) return rc;
   if ((rc = moe_distinct_experts(w.ids, R, E, w.distinct, w.d_count, stream))) return rc;
@@ -219,22 +237,7 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
   if ((rc = moe_align_block_size(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad,
                                  c->status, w.align_ws, w.align_bytes, side)))
     return rc;
-  oes_routed_experts v{};
-  v.layer = layer;
-  v.E = E;
-  v.e2s = cache->map + (size_t)layer * E;
-  v.wfmt = d->wfmt;
-  v.pool = pool;
-  v.row_bytes = src->row_bytes;
-  v.S = cache->S;
-  v.H = d->H;
-  v.I = d->I;
-  v.input_scale13 = d->input_scale13;
-  v.input_scale2 = d->input_scale2;
-  GemmPlan g;
-  if ((rc = gemm_prepare(&v, c->x, T, k, w.sorted_ids, w.block_expert, w.n_post_pad, B, w.gemm_ws,
-                         w.gemm_bytes, c->status, side, &g)))
-    return rc;
+  if ((rc = gemm_prepare_x(g, side))) return rc;
   if ((rc = gemm_run(g, kGroupHit, w.resident, side))) return rc;
   // caller's stream: each query's misses in query order, each query's copies
   // after its own ensure; the side stream runs each query's copied experts
@@ -264,6 +267,23 @@ extern "C" int moe_layer_forward_stream(const oes_expert_source* src, void* laye
   if (T == 0) return OES_OK;
   const LayerWs w = carve_layer(c->workspace, d, T, k);
   const int B = tile_plan(R, E);
+  // the GEMM is validated before anything is launched
+  oes_routed_experts v{};
+  v.layer = layer;
+  v.E = E;
+  v.e2s = w.e2s_identity;
+  v.wfmt = d->wfmt;
+  v.pool = layer_buf;
+  v.row_bytes = src->row_bytes;
+  v.S = E;
+  v.H = d->H;
+  v.I = d->I;
+  v.input_scale13 = d->input_scale13;
+  v.input_scale2 = d->input_scale2;
+  GemmPlan g;
+  if ((rc = gemm_prepare(&v, c->x, T, k, w.sorted_ids, w.block_expert, w.n_post_pad, B, w.gemm_ws,
+                         w.gemm_bytes, c->status, &g)))
+    return rc;
   cudaEvent_t copied = nullptr;
   if (copy_stream != compute_stream) {
     // the copy overwrites layer_buf only after work queued earlier on
@@ -285,25 +305,13 @@ extern "C" int moe_layer_forward_stream(const oes_expert_source* src, void* laye
   if ((rc = moe_align_block_size(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad,
                                  c->status, w.align_ws, w.align_bytes, compute_stream)))
     return rc;
+  if ((rc = gemm_prepare_x(g, compute_stream))) return rc;  // overlaps the layer copy
   if (copied) {
     OES_TRY_CUDA(cudaStreamWaitEvent(compute_stream, copied, 0));
     OES_TRY_CUDA(cudaEventDestroy(copied));
   }
-  oes_routed_experts v{};
-  v.layer = layer;
-  v.E = E;
-  v.e2s = w.e2s_identity;
-  v.wfmt = d->wfmt;
-  v.pool = layer_buf;
-  v.row_bytes = src->row_bytes;
-  v.S = E;
-  v.H = d->H;
-  v.I = d->I;
-  v.input_scale13 = d->input_scale13;
-  v.input_scale2 = d->input_scale2;
-  return moe_grouped_gemm_slots(&v, c->x, T, k, w.ids, w.w, w.sorted_ids, w.block_expert,
-                                w.n_post_pad, B, w.gemm_ws, w.gemm_bytes, c->out, c->status,
-                                compute_stream);
+  if ((rc = gemm_run(g, 0, nullptr, compute_stream))) return rc;
+  return gemm_combine(g, w.ids, w.w, c->out, compute_stream);
 }
 
 extern "C" int oes_takes_slot_path(int T, int k, int E, int S, int demand_tokens) {
@@ -447,6 +455,29 @@ extern "C" int moe_layers_forward_staged(const oes_stage_plan* p, const oes_expe
   const int E = p->E;
   const int64_t rb = src->row_bytes;
   uint8_t* base = static_cast<uint8_t*>(pool);
+  // every layer's GEMM is validated and prepared before anything is launched
+  std::vector<GemmPlan> plans(p->n);
+  for (int i = 0; i < p->n; ++i) {
+    const oes_chunk* c = &chunks[i];
+    if (c->T == 0) continue;
+    const LayerWs w = carve_layer(c->workspace, d, c->T, c->k);
+    oes_routed_experts v{};
+    v.layer = p->layers[i];
+    v.E = E;
+    v.e2s = p->e2s + (size_t)i * E;
+    v.wfmt = d->wfmt;
+    v.pool = pool;
+    v.row_bytes = rb;
+    v.S = p->S + 2 * E;
+    v.H = d->H;
+    v.I = d->I;
+    v.input_scale13 = d->input_scale13;
+    v.input_scale2 = d->input_scale2;
+    const int rc = gemm_prepare(&v, c->x, c->T, c->k, w.sorted_ids, w.block_expert, w.n_post_pad,
+                                tile_plan(c->T * c->k, E), w.gemm_ws, w.gemm_bytes, c->status,
+                                &plans[i]);
+    if (rc) return rc;
+  }
   OES_TRY_CUDA(cudaEventRecord(p->entry, compute_stream));
   OES_TRY_CUDA(cudaStreamWaitEvent(copy_stream, p->entry, 0));
   for (int i = 0; i < p->n; ++i) {
@@ -469,24 +500,11 @@ extern "C" int moe_layers_forward_staged(const oes_stage_plan* p, const oes_expe
       if (!rc)
         rc = moe_align_block_size(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad,
                                   c->status, w.align_ws, w.align_bytes, compute_stream);
+      if (!rc) rc = gemm_prepare_x(plans[i], compute_stream);
       if (rc) return rc;
       OES_TRY_CUDA(cudaStreamWaitEvent(compute_stream, p->copied[b], 0));
-      oes_routed_experts v{};
-      v.layer = layer;
-      v.E = E;
-      v.e2s = p->e2s + (size_t)i * E;
-      v.wfmt = d->wfmt;
-      v.pool = pool;
-      v.row_bytes = rb;
-      v.S = p->S + 2 * E;
-      v.H = d->H;
-      v.I = d->I;
-      v.input_scale13 = d->input_scale13;
-      v.input_scale2 = d->input_scale2;
-      rc = moe_grouped_gemm_slots(&v, c->x, T, k, w.ids, w.w, w.sorted_ids, w.block_expert,
-                                  w.n_post_pad, B, w.gemm_ws, w.gemm_bytes, c->out, c->status,
-                                  compute_stream);
-      if (rc) return rc;
+      if ((rc = gemm_run(plans[i], 0, nullptr, compute_stream))) return rc;
+      if ((rc = gemm_combine(plans[i], w.ids, w.w, c->out, compute_stream))) return rc;
     } else {
       OES_TRY_CUDA(cudaStreamWaitEvent(compute_stream, p->copied[b], 0));
     }

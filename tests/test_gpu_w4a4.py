@@ -147,3 +147,27 @@ def test_w4a4_needs_the_layer_scales():
         oes.moe_grouped_gemm_slots(view, 256, cfg.T, cfg.k, 16, 16, 16, 16, 16, 16, 256, 1 << 30,
                                    256, 16, stream=0)
     assert e.value.code == oes.OES_ERR_INVALID_ARG
+
+
+def test_refused_gemm_leaves_the_cache_unchanged():
+    """A W4A4 layer handed without its input scales is refused before the
+    slot path launches anything: no ensure runs, so the tables still match
+    the pool's bytes."""
+    lib()
+    cfg = W4A4_WM
+    w = Workload(cfg, gen_device="cpu")
+    before = oes.slot_cache_read_state(w.cache, cfg.S, cfg.L, cfg.E)
+    desc = oes.layer_desc(cfg.E, cfg.H, cfg.I, oes.OES_WFMT_NVFP4_W4A4)
+    wsb = oes.moe_layer_workspace_size(desc, cfg.T, cfg.k)
+    ws = scratch(wsb)
+    out = torch.zeros((cfg.T, cfg.H), dtype=torch.bfloat16, device="cuda")
+    st = status()
+    ch = oes.chunk(w.x, cfg.T, cfg.k, out, st, ws, wsb, logits=w.logits)
+    with pytest.raises(oes.OesError) as e:
+        oes.moe_layer_forward_slots(w.cache, w.src, w.pool, 0, desc, ch, 1)
+    assert e.value.code == oes.OES_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    after = oes.slot_cache_read_state(w.cache, cfg.S, cfg.L, cfg.E)
+    for key in ("map", "slot_key", "slot_ts", "clock", "hits", "misses"):
+        assert np.array_equal(np.asarray(after[key]), np.asarray(before[key])), key
+    w.close()
