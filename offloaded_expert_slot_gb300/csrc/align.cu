@@ -228,11 +228,10 @@ extern "C" int moe_align_block_size(const int32_t* ids, int R, int E, int B, int
 
   const size_t hist_smem = (size_t)E * 4;
   const size_t scat_smem = (size_t)kAlignWarps * E * 4;
-  static size_t configured = 0;
-  if (scat_smem > 48 * 1024 && scat_smem > configured) {
-    OES_TRY_CUDA(cudaFuncSetAttribute(align_scatter_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scat_smem));
-    configured = scat_smem;
+  if (scat_smem > 48 * 1024) {
+    const int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(align_scatter_kernel),
+                                        scat_smem, "align_scatter_kernel: shared memory limit");
+    if (rc) return rc;
   }
   align_count_kernel<<<G, kAlignThreads, hist_smem, stream>>>(ids, R, E, C, ignore_invalid, ws, status);
   OES_CHECK_LAUNCH("align_count_kernel");

@@ -3,7 +3,10 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <atomic>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 
@@ -24,16 +27,50 @@ int cuda_fail(cudaError_t e, const char* what) {
 }
 
 int num_sms() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-  if (!cached[dev]) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (!n) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       n = 1;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
+}
+
+// Kernel attributes are set once per (device, kernel); calls from several
+// host threads are serialised by a mutex.
+namespace {
+std::mutex g_attr_mu;
+std::map<std::pair<int, const void*>, size_t> g_smem_set;     // largest dynamic size set
+std::map<std::pair<int, const void*>, bool> g_carveout_set;
+}  // namespace
+
+int set_max_dynamic_smem(const void* func, size_t bytes, const char* name) {
+  int dev = 0;
+  OES_TRY_CUDA(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  size_t& have = g_smem_set[{dev, func}];
+  if (bytes <= have) return OES_OK;
+  const cudaError_t e =
+      cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  have = bytes;
+  return OES_OK;
+}
+
+int prefer_max_shared_carveout(const void* func, const char* name) {
+  int dev = 0;
+  OES_TRY_CUDA(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  bool& done = g_carveout_set[{dev, func}];
+  if (done) return OES_OK;
+  const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  done = true;
+  return OES_OK;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -53,6 +90,16 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                  CUtensorMapSwizzle swizzle) {
+  // the encoder is a driver call and needs a current context; a thread whose
+  // first CUDA call this is has none yet, so bind the current device's
+  // primary context once per thread
+  static thread_local bool bound = false;
+  if (!bound) {
+    int dev = 0;
+    OES_TRY_CUDA(cudaGetDevice(&dev));
+    OES_TRY_CUDA(cudaSetDevice(dev));
+    bound = true;
+  }
   auto fn = get_encode();
   if (!fn) {
     set_error("cuTensorMapEncodeTiled is not available from the driver");

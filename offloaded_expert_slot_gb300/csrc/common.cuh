@@ -36,6 +36,10 @@ int cuda_fail(cudaError_t e, const char* what);
   } while (0)
 
 int num_sms();  // SMs of the current device (cached per device)
+// Once per (device, kernel), thread-safe: raise the kernel's dynamic shared
+// memory limit to at least `bytes`; make it prefer the largest shared carveout.
+int set_max_dynamic_smem(const void* func, size_t bytes, const char* name);
+int prefer_max_shared_carveout(const void* func, const char* name);
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

@@ -1197,16 +1197,9 @@ int launch_gemm_tm(const GemmMaps& maps, const GemmParams& p0, cudaStream_t stre
     return rc;
   }
   p.tmem_cols = 512;
-  static bool configured = false;
-  if (!configured) {
-    // the largest dynamic size the kernel's own static shared memory leaves
-    cudaFuncAttributes fa{};
-    OES_TRY_CUDA(cudaFuncGetAttributes(&fa, grouped_gemm_tm_kernel<MODE, WF>));
-    OES_TRY_CUDA(cudaFuncSetAttribute(grouped_gemm_tm_kernel<MODE, WF>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      227 * 1024 - (int)fa.sharedSizeBytes));
-    configured = true;
-  }
+  if ((rc = set_max_dynamic_smem(reinterpret_cast<const void*>(grouped_gemm_tm_kernel<MODE, WF>),
+                                  smem, "grouped_gemm_tm_kernel: shared memory limit")))
+    return rc;
   grouped_gemm_tm_kernel<MODE, WF><<<num_sms(), gemm_threads_tm(WF), smem, stream>>>(maps, p);
   OES_CHECK_LAUNCH("grouped_gemm_tm_kernel");
   return OES_OK;
@@ -1223,16 +1216,9 @@ int launch_gemm(const GemmMaps& maps, const GemmParams& p0, int BN, cudaStream_t
   }
   p.tmem_cols = (MODE == 1) ? 4 * BN : 2 * BN;
   if (p.tmem_cols < 32) p.tmem_cols = 32;
-  static bool configured = false;
-  if (!configured) {
-    // the largest dynamic size the kernel's own static shared memory leaves
-    cudaFuncAttributes fa{};
-    OES_TRY_CUDA(cudaFuncGetAttributes(&fa, grouped_gemm_kernel<MODE, WF>));
-    OES_TRY_CUDA(cudaFuncSetAttribute(grouped_gemm_kernel<MODE, WF>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      227 * 1024 - (int)fa.sharedSizeBytes));
-    configured = true;
-  }
+  if ((rc = set_max_dynamic_smem(reinterpret_cast<const void*>(grouped_gemm_kernel<MODE, WF>), smem,
+                                  "grouped_gemm_kernel: shared memory limit")))
+    return rc;
   grouped_gemm_kernel<MODE, WF><<<num_sms(), gemm_threads(WF), smem, stream>>>(maps, p);
   OES_CHECK_LAUNCH("grouped_gemm_kernel");
   return OES_OK;

@@ -496,18 +496,16 @@ extern "C" int slot_cache_ensure_tagged(oes_slot_cache* c, int layer, const int3
   int spad = 2;
   while (spad < c->S) spad <<= 1;
   const size_t smem = (size_t)spad * 8;
-  static size_t configured_smem = 0;
-  if (smem > 48 * 1024 && smem > configured_smem) {
-    OES_TRY_CUDA(cudaFuncSetAttribute(ensure_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)smem));
-    configured_smem = smem;
-  }
+  int rc;
+  if (smem > 48 * 1024 &&
+      (rc = set_max_dynamic_smem(reinterpret_cast<const void*>(ensure_kernel), smem,
+                                 "ensure_kernel: shared memory limit")))
+    return rc;
   // the largest shared carveout, as for the copies (an ensure may run beside
   // the copies and the GEMM)
-  static const cudaError_t carve = cudaFuncSetAttribute(
-      ensure_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-      cudaSharedmemCarveoutMaxShared);
-  OES_REQUIRE(carve == cudaSuccess, "slot_cache_ensure: carveout attribute failed");
+  if ((rc = prefer_max_shared_carveout(reinterpret_cast<const void*>(ensure_kernel),
+                                       "ensure_kernel: carveout")))
+    return rc;
   ensure_kernel<<<1, kEnsureThreads, smem, stream>>>(view_of(c), layer, experts, n, record_stats,
                                                      tag, spad, miss, n_miss, status);
   OES_CHECK_LAUNCH("ensure_kernel");
@@ -568,10 +566,9 @@ extern "C" int slot_cache_copy_misses(const oes_expert_source* src, void* pool, 
   // the copies run beside kernels that need most of an SM's shared memory;
   // an SM changes its L1 / shared split only when idle, so the copy kernel
   // asks for the largest shared carveout and never shrinks it
-  static const cudaError_t carve = cudaFuncSetAttribute(
-      copy_misses_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-      cudaSharedmemCarveoutMaxShared);
-  OES_REQUIRE(carve == cudaSuccess, "slot_cache_copy_misses: carveout attribute failed");
+  if (const int rc = prefer_max_shared_carveout(reinterpret_cast<const void*>(copy_misses_kernel),
+                                                "copy_misses_kernel: carveout"))
+    return rc;
   const int grid = num_sms();
   copy_misses_kernel<<<grid, kCopyThreads, 0, stream>>>(
       src->dev_bases, src->L, src->E, src->row_bytes, static_cast<uint8_t*>(pool), S, miss, n_miss,

@@ -133,3 +133,47 @@ def test_largest_layer_32_queries():
     s = gpu_stream(w)
     assert torch.equal(s.out.view(torch.int16), r.out.view(torch.int16))
     w.close()
+
+
+def test_two_host_threads_two_caches():
+    """The library is re-entrant across caches: two host threads, each with
+    its own cache, pool and stream, run the slot path at the same time
+    (ctypes releases the interpreter lock) and each gets exactly the bytes a
+    lone run gives."""
+    import threading
+    lib()
+    cfgs = [small("thread_a", T=32, k=4, E=64, S=80, L=2, prefill=30, seed=2101),
+            small("thread_b", T=48, k=6, E=64, S=80, L=2, prefill=50, seed=2102)]
+    want = []
+    for cfg in cfgs:
+        w = Workload(cfg, gen_device="cpu")
+        r = Run(w)
+        oes.moe_layer_forward_slots(w.cache, w.src, w.pool, 0, r.desc, r.chunk, 1)
+        torch.cuda.synchronize()
+        want.append(r.out.view(torch.int16).clone())
+        w.close()
+    works = [Workload(cfg, gen_device="cpu") for cfg in cfgs]
+    runs = [Run(w) for w in works]
+    errors = []
+
+    def worker(i):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                oes.moe_layer_forward_slots(works[i].cache, works[i].src, works[i].pool, 0,
+                                            runs[i].desc, runs[i].chunk, 1)
+            s.synchronize()
+        except Exception as e:            # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for i in range(2):
+        assert int(runs[i].status.item()) == 0
+        assert torch.equal(runs[i].out.view(torch.int16), want[i]), i
+        works[i].close()
