@@ -800,6 +800,57 @@ def layer_sweep(args):
     oes.oes_expert_source_destroy(src)
 
 
+def decode_warm(args):
+    """The decode step with a warm cache: every expert the tokens route to is
+    already resident (the step is run once before timing and the cache is
+    not restored), so the step is routing, the ensures (all hits), align and
+    the grouped GEMM over the routed experts -- a weight stream from HBM.
+    Per decode width: eager and graph-replayed ms per step, the distinct
+    experts, their bytes, and that stream's fraction of the measured HBM
+    bandwidth.  One JSON line per width; not the headline."""
+    import torch
+    from offloaded_expert_slot_gb300 import build, oes
+    from offloaded_expert_slot_gb300.configs import scaled
+    build.build()
+    oes.load()
+    hbm = float(peaks()["hbm_gbs"])
+    base = CONFIGS[args.config]
+    for T in (1, 4, 8, 16, 32, 64):
+        cfg = scaled(base, T=T)
+        b = Bench(cfg, 0)
+
+        def step():
+            oes.moe_layer_forward_slots(b.cache, b.src, b.pool, cfg.layer, b.desc, b.chunk, 1)
+
+        step()                                        # loads the misses: warm from here on
+        torch.cuda.synchronize()
+        for _ in range(3):
+            step()
+        ms = b.timed(step, max(args.steps, 20))
+        g = torch.cuda.CUDAGraph()
+        st = torch.cuda.Stream()
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            with torch.cuda.graph(g, stream=st):
+                step()
+        torch.cuda.current_stream().wait_stream(st)
+        for _ in range(3):
+            g.replay()
+        gms = b.timed(g.replay, max(args.steps, 20))
+        assert int(b.status.item()) == 0, int(b.status.item())
+        off = oes.moe_layer_workspace_views(b.desc, T, cfg.k, b.ws)["d_count"] - b.ws.data_ptr()
+        D = int(b.ws[off:off + 4].view(torch.int32).item())
+        nbytes = D * cfg.row_bytes
+        print(json.dumps({"decode_warm": cfg.name, "T": T, "k": cfg.k, "distinct_experts": D,
+                          "expert_bytes": nbytes, "ms_eager": ms, "ms_graph": gms,
+                          "GB/s_graph": nbytes / gms / 1e6, "hbm_frac_graph": nbytes / gms / 1e6 / hbm,
+                          "routed_tokens_per_s_graph": T / gms * 1e3}), flush=True)
+        del g
+        b.close()
+        del b, step
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -811,9 +862,14 @@ def main():
                     help="bandwidth sweep of the routing and align kernels (not the headline)")
     ap.add_argument("--crossover", action="store_true",
                     help="slot path vs staged whole-layer path per chunk size (not the headline)")
+    ap.add_argument("--decode-warm", action="store_true",
+                    help="decode steps with every routed expert resident (GEMM-bound), per width")
     ap.add_argument("--layers", action="store_true",
                     help="every layer of the workload in turn: slot path, staged, streamed")
     args = ap.parse_args()
+    if args.decode_warm:
+        decode_warm(args)
+        return
     if args.layers:
         layer_sweep(args)
         return

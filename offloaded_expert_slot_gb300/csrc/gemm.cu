@@ -337,6 +337,28 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
   UnitRec* utab = reinterpret_cast<UnitRec*>(tmem_holder + 4);  // [kMaxUnitsPerCta]
 
+  const int nb = *p.n_post_pad / p.BN;
+  int total = nb * p.n_mtiles;
+  const uint32_t acc_cols = (MODE == 1) ? 2 * p.BN : p.BN;
+  __shared__ int s_scan[33];
+  const int dense = p.filter ? fill_filtered_units(p, nb, utab, s_scan) : -1;
+  if (dense >= 0) {
+    total = dense;
+  } else {
+    // every thread looks up one of this CTA's units (independent loads in
+    // parallel), so the roles below never wait on global memory for them
+    for (int i = threadIdx.x; i < kMaxUnitsPerCta; i += blockDim.x) {
+      const int u = blockIdx.x + i * gridDim.x;
+      if (u >= total) break;
+      const Unit t = unit_info(p, u, nb);
+      utab[i] = UnitRec{t.b, t.m, t.slot, t.nvalid};
+    }
+  }
+  __syncthreads();
+  // a CTA without units leaves before it sets up barriers or takes TMEM
+  // (a small or filtered launch leaves most CTAs idle)
+  if ((int)blockIdx.x >= total) return;
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
@@ -372,25 +394,6 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-
-  const int nb = *p.n_post_pad / p.BN;
-  int total = nb * p.n_mtiles;
-  const uint32_t acc_cols = (MODE == 1) ? 2 * p.BN : p.BN;
-  __shared__ int s_scan[33];
-  const int dense = p.filter ? fill_filtered_units(p, nb, utab, s_scan) : -1;
-  if (dense >= 0) {
-    total = dense;
-  } else {
-    // every thread looks up one of this CTA's units (independent loads in
-    // parallel), so the roles below never wait on global memory for them
-    for (int i = threadIdx.x; i < kMaxUnitsPerCta; i += blockDim.x) {
-      const int u = blockIdx.x + i * gridDim.x;
-      if (u >= total) break;
-      const Unit t = unit_info(p, u, nb);
-      utab[i] = UnitRec{t.b, t.m, t.slot, t.nvalid};
-    }
-  }
-  __syncthreads();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -695,6 +698,25 @@ __global__ void __maxnreg__(64)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
   UnitRec* utab = reinterpret_cast<UnitRec*>(tmem_holder + 4);
 
+  const int nb = *p.n_post_pad / p.BN;
+  int total = nb * p.n_mtiles;
+  __shared__ int s_scan[33];
+  const int dense = p.filter ? fill_filtered_units(p, nb, utab, s_scan) : -1;
+  if (dense >= 0) {
+    total = dense;
+  } else {
+    for (int i = threadIdx.x; i < kMaxUnitsPerCta; i += blockDim.x) {
+      const int u = blockIdx.x + i * gridDim.x;
+      if (u >= total) break;
+      const Unit t = unit_info(p, u, nb);
+      utab[i] = UnitRec{t.b, t.m, t.slot, t.nvalid};
+    }
+  }
+  __syncthreads();
+  // a CTA without units leaves before it sets up barriers or takes TMEM
+  // (a small or filtered launch leaves most CTAs idle)
+  if ((int)blockIdx.x >= total) return;
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
@@ -728,22 +750,6 @@ __global__ void __maxnreg__(64)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-
-  const int nb = *p.n_post_pad / p.BN;
-  int total = nb * p.n_mtiles;
-  __shared__ int s_scan[33];
-  const int dense = p.filter ? fill_filtered_units(p, nb, utab, s_scan) : -1;
-  if (dense >= 0) {
-    total = dense;
-  } else {
-    for (int i = threadIdx.x; i < kMaxUnitsPerCta; i += blockDim.x) {
-      const int u = blockIdx.x + i * gridDim.x;
-      if (u >= total) break;
-      const Unit t = unit_info(p, u, nb);
-      utab[i] = UnitRec{t.b, t.m, t.slot, t.nvalid};
-    }
-  }
-  __syncthreads();
 
   // weight rows of tile j: GEMM1 gate [128j, +128) and up [I + 128j, +128);
   // GEMM2 w2 rows [256j, +256)
