@@ -121,6 +121,7 @@ def test_align_past_1024_experts(E):
 
 
 @pytest.mark.parametrize("R,E,B", [(0, 5, 4), (1, 1, 1), (7, 3, 1), (100, 7, 3), (999, 64, 16),
+                                   (1024, 2100, 16), (1025, 2100, 16), (1000, 4096, 128),
                                    (3000, 1, 128), (4099, 4096, 16)])
 def test_align_edges_and_invalid_ids(R, E, B):
     lib()
