@@ -616,6 +616,10 @@ def crossover(args):
     base = CONFIGS[args.config]
     if base.wfmt == "bf16":
         base = scaled(base, L=8, distinct_source_layers=2)
+    else:
+        # only layers 0..7 are forwarded: 8 distinct sources, the pool's
+        # placement still spread over all of the workload's layers
+        base = scaled(base, distinct_source_layers=min(base.L, 8))
     base = scaled(base, prefill=base.S)
     n_layers = min(8, base.L)
     E, S, rb = base.E, base.S, base.row_bytes
@@ -764,8 +768,12 @@ def layer_sweep(args):
         e.record()
         return e
 
+    # warm-up: one untimed pass over every layer, so that each pinned source
+    # has been read by the GPU once before anything is timed
     reset()
-    oes.moe_layer_forward_slots(cache, src, pool, 0, desc, ch, 0)       # warm-up
+    for l in layers:
+        oes.moe_layer_forward_slots(cache, src, pool, l, desc, ch, 0)
+    torch.cuda.synchronize()
     reset()
     marks = [ev()]
     for l in layers:

@@ -248,8 +248,9 @@ int slot_cache_copy_misses(const oes_expert_source *src, void *pool, int S, cons
                            oes_stream_t stream);
 
 /* Copies all E rows of one layer into a contiguous device buffer (the
- * whole-layer stream of FreeToken PR #676, Problem) with one DMA copy.
- * dst: device [E, row_bytes]. */
+ * whole-layer stream of FreeToken PR #676, Problem), with the miss copies'
+ * SM-load kernel (one warp per SM) rather than a DMA copy.
+ * dst: device [E, row_bytes], 16-byte aligned. */
 int oes_copy_layer(const oes_expert_source *src, int layer, void *dst, oes_stream_t stream);
 
 /* ------------------------------------------------------------------ align */
@@ -464,8 +465,10 @@ int moe_layer_forward(oes_slot_cache *cache, const oes_expert_source *src, void 
 
 /* Prefill staging over a sequence of layers (vLLM fork PR #51, Details,
  * "Prefill staging"): two device buffers of one whole layer each alternate
- * by layer; the rows of layer i+1 are copied by DMA on a copy stream while
- * layer i computes, ordered by events; at the start of the step the
+ * by layer; the rows of layer i+1 are copied on a copy stream while layer i
+ * computes, ordered by events (the pages copy by DMA; here the miss copies'
+ * one-warp-per-SM kernel, which holds the host link's rate where DMA falls
+ * back over tens of GB of pinned source); at the start of the step the
  * placement tables are read back once and each layer's non-resident experts
  * become contiguous runs.  Resident experts are read from their slots and
  * their rows are never written.
@@ -496,13 +499,15 @@ int oes_stage_plan_layer(const oes_stage_plan *plan, int i, int *n_runs, int32_t
 
 /* Forwards the plan's n layers in order: layer i = plan layer i with chunk
  * chunks[i] (host array [n]; chunks run one after another on
- * compute_stream, so they may share x, out and workspace).  Per layer: DMA
- * copies of the runs into staging buffer i % 2 on copy_stream (after the
+ * compute_stream, so they may share x, out and workspace).  Per layer: the
+ * copy kernel moves the runs into staging buffer i % 2 on copy_stream (after the
  * compute of layer i-2 released that buffer, and after all work queued on
  * compute_stream before the call), then on compute_stream route -> align
  * -> wait for the copies -> grouped GEMM -> combine, with the plan's remap.
  * Each chunk's output equals moe_layer_forward_stream's for that layer and
  * chunk, byte for byte.  pool: device [S + 2E, row_bytes] as above.  The
+ * first call with a given source row size builds the plan's device copy
+ * tables (an allocation and a synchronous upload).  The
  * plan's events order the copies, so one plan feeds one runner at a time;
  * oes_stage_plan_destroy waits for the last runner's compute to finish. */
 int moe_layers_forward_staged(const oes_stage_plan *plan, const oes_expert_source *src, void *pool,

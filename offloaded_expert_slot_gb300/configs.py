@@ -93,8 +93,7 @@ C4 = LayerConfig(name="c4_nvfp4_prefill", T=600, k=10, E=512, H=2048, I=768, wfm
                  S=1100, L=2, prefill=800, query_width=128, logits="normal", seed=1004,
                  layer_input_scales=(2.0, 3.0), other_slot_input_scale=9.0)
 C5 = LayerConfig(name="c5_long_prefill", T=4096, k=10, E=512, H=2048, I=768, wfmt="nvfp4",
-                 S=1650, L=48, prefill=0, query_width=128, logits="normal", seed=1005,
-                 distinct_source_layers=4)
+                 S=1650, L=48, prefill=0, query_width=128, logits="normal", seed=1005)
 
 CONFIGS = {c.name: c for c in (C1, C2, C3, C4, C5)}
 

@@ -39,4 +39,15 @@ struct oes_expert_source {
 
 namespace oes {
 int tile_plan(int R, int E);
+
+// A contiguous run of bytes from a host-mapped source to device memory;
+// item0 = the run's first 4 KB item in its copy launch.
+struct CopyRun {
+  int64_t src_off, dst_off, bytes, item0;
+};
+int64_t copy_run_items(int64_t bytes);
+// Copies the runs (device [nruns]) or, when runs is null, the one run
+// (src_off, dst_off, bytes); nitems = the launch's 4 KB items in all.
+int launch_copy_runs(const void* src, void* dst, const CopyRun* runs, int nruns, int64_t src_off,
+                     int64_t dst_off, int64_t bytes, int64_t nitems, cudaStream_t stream);
 }  // namespace oes

@@ -333,7 +333,7 @@ extern "C" int moe_layer_forward(oes_slot_cache* cache, const oes_expert_source*
 
 // ------------------------------------------------------------------ staging
 // vLLM fork PR #51, Details ("Prefill staging"): whole-layer double buffer,
-// next-layer prefetch by DMA on a side stream, contiguous non-resident runs
+// next-layer prefetch on a side stream, contiguous non-resident runs
 // from one placement readback per step.
 
 struct oes_stage_plan {
@@ -343,6 +343,13 @@ struct oes_stage_plan {
   std::vector<int> rows;                               // [n] staged experts
   int32_t* e2s;                                        // device [n][E]
   cudaEvent_t entry, copied[2], done[2];
+  // the runs as copy-kernel tables, built by the first runner call for its
+  // source's row size: layer i's runs are run_tab[run_first[i] ...]
+  int64_t run_rb = 0;
+  std::vector<CopyRun> run_host;
+  std::vector<int> run_first, run_count;
+  std::vector<int64_t> run_items;
+  CopyRun* run_tab = nullptr;
 };
 
 namespace {
@@ -350,6 +357,7 @@ namespace {
 void destroy_plan(oes_stage_plan* p) {
   if (!p) return;
   cudaFree(p->e2s);
+  cudaFree(p->run_tab);
   for (cudaEvent_t e : {p->entry, p->copied[0], p->copied[1], p->done[0], p->done[1]})
     if (e) cudaEventDestroy(e);
   delete p;
@@ -478,6 +486,34 @@ extern "C" int moe_layers_forward_staged(const oes_stage_plan* p, const oes_expe
                                 &plans[i]);
     if (rc) return rc;
   }
+  auto* mp = const_cast<oes_stage_plan*>(p);  // the run tables are a cache of the plan
+  if (mp->run_rb != rb) {
+    mp->run_host.clear();
+    mp->run_first.assign(p->n, 0);
+    mp->run_count.assign(p->n, 0);
+    mp->run_items.assign(p->n, 0);
+    for (int i = 0; i < p->n; ++i) {
+      const int b = i & 1;
+      int64_t items = 0;
+      mp->run_first[i] = (int)mp->run_host.size();
+      for (const auto& r : p->runs[i]) {
+        const int64_t bytes = (int64_t)(r.second - r.first) * rb;
+        mp->run_host.push_back(CopyRun{(int64_t)r.first * rb,
+                                       ((int64_t)p->S + (int64_t)b * E + r.first) * rb, bytes, items});
+        items += copy_run_items(bytes);
+      }
+      mp->run_count[i] = (int)p->runs[i].size();
+      mp->run_items[i] = items;
+    }
+    cudaFree(mp->run_tab);
+    mp->run_tab = nullptr;
+    if (!mp->run_host.empty()) {
+      OES_TRY_CUDA(cudaMalloc(&mp->run_tab, mp->run_host.size() * sizeof(CopyRun)));
+      OES_TRY_CUDA(cudaMemcpy(mp->run_tab, mp->run_host.data(), mp->run_host.size() * sizeof(CopyRun),
+                              cudaMemcpyHostToDevice));
+    }
+    mp->run_rb = rb;
+  }
   OES_TRY_CUDA(cudaEventRecord(p->entry, compute_stream));
   OES_TRY_CUDA(cudaStreamWaitEvent(copy_stream, p->entry, 0));
   for (int i = 0; i < p->n; ++i) {
@@ -485,11 +521,11 @@ extern "C" int moe_layers_forward_staged(const oes_stage_plan* p, const oes_expe
     const oes_chunk* c = &chunks[i];
     // copy stream: this layer's runs into staging buffer b once layer i-2 let go of it
     if (i >= 2) OES_TRY_CUDA(cudaStreamWaitEvent(copy_stream, p->done[b], 0));
-    const uint8_t* host = static_cast<const uint8_t*>(src->host_bases[layer]);
-    for (const auto& r : p->runs[i])
-      OES_TRY_CUDA(cudaMemcpyAsync(base + ((int64_t)p->S + (int64_t)b * E + r.first) * rb,
-                                   host + (int64_t)r.first * rb, (size_t)(r.second - r.first) * rb,
-                                   cudaMemcpyDefault, copy_stream));
+    if (p->run_count[i] > 0) {
+      const int rc = launch_copy_runs(src->host_bases[layer], base, p->run_tab + p->run_first[i],
+                                      p->run_count[i], 0, 0, 0, p->run_items[i], copy_stream);
+      if (rc) return rc;
+    }
     OES_TRY_CUDA(cudaEventRecord(p->copied[b], copy_stream));
     // compute stream: route and align overlap the copies; the GEMM waits for them
     const int T = c->T, k = c->k, R = T * k;

@@ -291,7 +291,65 @@ __global__ void __launch_bounds__(kCopyThreads)
   }
 }
 
+// Contiguous host runs to device, with copy_misses_kernel's access pattern
+// (one warp per SM, 4 KB per item, eight 16-byte loads a lane in flight):
+// over this pool's host link SM loads keep their rate where DMA copies lose
+// up to a fifth of it once the pinned source spans tens of GB.  Runs from
+// `runs` (device [nruns]) or, when it is null, the single run `one`.
+__global__ void __launch_bounds__(kCopyThreads)
+    copy_runs_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                     const CopyRun* __restrict__ runs, int nruns, CopyRun one, int64_t nitems) {
+  const int64_t chunk = (int64_t)kCopyThreads * kCopyUnroll;  // 16-byte vectors per item
+  for (int64_t it = blockIdx.x; it < nitems; it += gridDim.x) {
+    CopyRun r = one;
+    if (runs) {
+      int lo = 0, hi = nruns - 1;  // last run whose first item <= it
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (runs[mid].item0 <= it) lo = mid;
+        else hi = mid - 1;
+      }
+      r = runs[lo];
+    }
+    const int64_t vecs = r.bytes >> 4;
+    const int64_t c0 = (it - r.item0) * chunk;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + r.src_off);
+    uint4* d4 = reinterpret_cast<uint4*>(dst + r.dst_off);
+    uint4 buf[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t v = c0 + u * kCopyThreads + threadIdx.x;
+      if (v < vecs) buf[u] = __ldcs(s4 + v);
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t v = c0 + u * kCopyThreads + threadIdx.x;
+      if (v < vecs) d4[v] = buf[u];
+    }
+  }
+}
+
 }  // namespace
+
+int64_t copy_run_items(int64_t bytes) {
+  const int64_t item = (int64_t)kCopyThreads * kCopyUnroll * 16;
+  return (bytes + item - 1) / item;
+}
+
+int launch_copy_runs(const void* src, void* dst, const CopyRun* runs, int nruns, int64_t src_off,
+                     int64_t dst_off, int64_t bytes, int64_t nitems, cudaStream_t stream) {
+  if (nitems <= 0) return OES_OK;
+  if (const int rc = prefer_max_shared_carveout(reinterpret_cast<const void*>(copy_runs_kernel),
+                                                "copy_runs_kernel: carveout"))
+    return rc;
+  const CopyRun one{src_off, dst_off, bytes, 0};
+  copy_runs_kernel<<<num_sms(), kCopyThreads, 0, stream>>>(static_cast<const uint8_t*>(src),
+                                                          static_cast<uint8_t*>(dst), runs, nruns,
+                                                          one, nitems);
+  OES_CHECK_LAUNCH("copy_runs_kernel");
+  return OES_OK;
+}
+
 }  // namespace oes
 
 using namespace oes;
@@ -581,7 +639,8 @@ extern "C" int oes_copy_layer(const oes_expert_source* src, int layer, void* dst
                               oes_stream_t stream) {
   OES_REQUIRE(src && dst, "oes_copy_layer: null pointer");
   OES_REQUIRE(layer >= 0 && layer < src->L, "oes_copy_layer: layer %d out of range", layer);
-  OES_TRY_CUDA(cudaMemcpyAsync(dst, src->host_bases[layer], (size_t)src->E * src->row_bytes,
-                               cudaMemcpyDefault, stream));
-  return OES_OK;
+  OES_REQUIRE(((uintptr_t)dst & 15) == 0, "oes_copy_layer: dst not 16-byte aligned");
+  const int64_t bytes = (int64_t)src->E * src->row_bytes;
+  return launch_copy_runs(src->host_bases[layer], dst, nullptr, 0, 0, 0, bytes,
+                          copy_run_items(bytes), stream);
 }
