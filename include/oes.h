@@ -163,10 +163,12 @@ int slot_cache_read_state(const oes_slot_cache *cache, int32_t *map, int32_t *sl
                           int64_t *decode_freq, oes_stream_t stream);
 
 /* Bytes of the cache's device tables, and asynchronous device-to-device
- * copies of them: snapshot saves every table (map, slots, timestamps,
- * clock, counters, decode_freq) into dst, restore puts such a snapshot
- * back.  dst / src: device buffers of slot_cache_state_bytes() bytes.  Used
- * to replay a query sequence from a known state without a host sync. */
+ * copies of them (one small kernel): snapshot saves every table (map, slots,
+ * timestamps, clock, counters, decode_freq, LRFU scores and pins, the chunk
+ * tag counter) into dst, restore puts such a snapshot back.  dst / src:
+ * 16-byte aligned device buffers of slot_cache_state_bytes() bytes (a
+ * multiple of 16).  Used to replay a query sequence from a known state
+ * without a host sync. */
 size_t slot_cache_state_bytes(const oes_slot_cache *cache);
 int slot_cache_snapshot(const oes_slot_cache *cache, void *dst, oes_stream_t stream);
 int slot_cache_restore(oes_slot_cache *cache, const void *src, oes_stream_t stream);

@@ -329,6 +329,26 @@ __global__ void __launch_bounds__(kCopyThreads)
   }
 }
 
+// Device-to-device copy of the cache's tables (snapshot / restore): a few
+// tens of KB, where a kernel launch beats a copy-engine transfer.
+__global__ void copy_tables_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                   int64_t n16) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16;
+       i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
+int copy_tables(const void* src, void* dst, size_t bytes, cudaStream_t stream) {
+  OES_REQUIRE((((uintptr_t)src | (uintptr_t)dst) & 15) == 0 && bytes % 16 == 0,
+              "slot cache snapshot/restore: buffers must be 16-byte aligned");
+  const int64_t n16 = (int64_t)(bytes / 16);
+  const int blocks = (int)std::min<int64_t>((n16 + 255) / 256, (int64_t)num_sms());
+  copy_tables_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(src),
+                                                  static_cast<uint4*>(dst), n16);
+  OES_CHECK_LAUNCH("copy_tables_kernel");
+  return OES_OK;
+}
+
 }  // namespace
 
 int64_t copy_run_items(int64_t bytes) {
@@ -391,8 +411,8 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   c->E = E;
   cudaGetDevice(&c->device);
   const size_t LE = (size_t)L * E;
-  const size_t bytes = LE * 4 + (size_t)S * 4 + (size_t)S * 8 + 8 * 8 + LE * 8 + (size_t)S * 8 +
-                       (size_t)S * 4 + 64;
+  const size_t bytes = (LE * 4 + (size_t)S * 4 + (size_t)S * 8 + 8 * 8 + LE * 8 + (size_t)S * 8 +
+                        (size_t)S * 4 + 64 + 15) / 16 * 16;
   c->block_bytes = bytes;
   c->side = nullptr;
   c->fork = c->join = nullptr;
@@ -524,14 +544,12 @@ extern "C" size_t slot_cache_state_bytes(const oes_slot_cache* c) { return c ? c
 
 extern "C" int slot_cache_snapshot(const oes_slot_cache* c, void* dst, oes_stream_t stream) {
   OES_REQUIRE(c && dst, "slot_cache_snapshot: null pointer");
-  OES_TRY_CUDA(cudaMemcpyAsync(dst, c->block, c->block_bytes, cudaMemcpyDeviceToDevice, stream));
-  return OES_OK;
+  return copy_tables(c->block, dst, c->block_bytes, stream);
 }
 
 extern "C" int slot_cache_restore(oes_slot_cache* c, const void* src, oes_stream_t stream) {
   OES_REQUIRE(c && src, "slot_cache_restore: null pointer");
-  OES_TRY_CUDA(cudaMemcpyAsync(c->block, src, c->block_bytes, cudaMemcpyDeviceToDevice, stream));
-  return OES_OK;
+  return copy_tables(src, c->block, c->block_bytes, stream);
 }
 
 extern "C" int slot_cache_layer_map(const oes_slot_cache* c, int layer, const int32_t** e2s) {
