@@ -212,3 +212,36 @@ def test_copy_misses_large_rows_and_offsets_past_2gib():
     oes.oes_expert_source_destroy(src)
     oes.slot_cache_destroy(cache)
     w.close()
+
+
+@pytest.mark.parametrize("policy", ["lru", "lrfu"])
+def test_largest_pool(policy):
+    """OES_MAX_SLOTS slots (the ensure kernel's 64 KB sort buffer, above the
+    default 48 KB shared-memory limit) over 4 layers of 4096 experts, half
+    pre-filled; random queries of up to 128 keys, bit-exact against the
+    oracle under LRU and LRFU."""
+    S, L, E = oes.OES_MAX_SLOTS, 4, 4096
+    g = np.random.default_rng(8192)
+    c = GpuCache(S, L, E)
+    n = S // 2
+    key = np.full(S, -1, np.int32)
+    ts = np.zeros(S, np.int64)
+    slots = g.permutation(S)[:n]
+    key[slots] = g.choice(L * E, size=n, replace=False)
+    ts[slots] = g.permutation(n) + 1
+    c.load(key, ts, n)
+    o = SlotCache.from_state(S, L, E, key, ts, n)
+    if policy == "lrfu":
+        oes.slot_cache_set_policy(c.h, oes.OES_POLICY_LRFU, 4)
+        o.set_policy("lrfu", 4)
+    for step in range(30):
+        layer = int(g.integers(0, L))
+        q = sorted(g.choice(E, size=int(g.integers(1, oes.OES_QUERY_MAX + 1)), replace=False).tolist())
+        s, m = c.ensure(layer, q, record_stats=True)
+        os_, om = o.ensure([layer * E + e for e in q], record_stats=True)
+        assert s == STATUS[os_] and m == [tuple(x) for x in om], step
+    assert_same(c, o)
+    if policy == "lrfu":
+        crf, pin = oes.slot_cache_read_lrfu(c.h, S)
+        assert [int(v) for v in crf] == o.crf
+    c.close()
