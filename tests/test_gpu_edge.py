@@ -177,3 +177,38 @@ def test_two_host_threads_two_caches():
         assert int(runs[i].status.item()) == 0
         assert torch.equal(runs[i].out.view(torch.int16), want[i]), i
         works[i].close()
+
+
+@pytest.mark.parametrize("wfmt,T", [("bf16", 8), ("bf16", 24), ("nvfp4", 8)],
+                         ids=["bf16_weight_major", "bf16_token_major", "nvfp4_weight_major"])
+def test_wide_layer(wfmt, T):
+    """H = 8192, I = 4096: 128 K chunks per GEMM1 tile and 64 (weight-major)
+    or 32 (token-major) output tiles in GEMM2, on 4 experts; every token
+    against the oracle, slot == stream.  The outputs here are about 3x the
+    workloads' (sums over 8192 and 4096 terms), so the max-abs bar scales
+    with them: the GPU rounds h, y and out to 16 bits (each within 2^-9 of
+    the value, NVFP4's h f16 and bf16 y), and h's rounding adds noise over
+    the 4096-term down projection, so max-abs <= 2^-7 * max|out| (rel-L2
+    keeps the layer bar)."""
+    from offloaded_expert_slot_gb300.configs import C4
+    lib()
+    base = C2 if wfmt == "bf16" else C4
+    cfg = scaled(base, name=f"wide_{wfmt}_{T}", T=T, k=2, E=4, H=8192, I=4096, S=6, L=1,
+                 prefill=0)
+    w = Workload(cfg, gen_device="cpu")
+    r = Run(w)
+    oes.moe_layer_forward_slots(w.cache, w.src, w.pool, 0, r.desc, r.chunk, 0)
+    torch.cuda.synchronize()
+    assert int(r.status.item()) == 0
+    assert oes.oes_tile_plan(T * 2, 4) == (128 if T == 24 else 16)
+    o, _oc = oracle_slots(w)
+    got = r.out.to(torch.float64).cpu().numpy()
+    want = o["out"]
+    err = float(np.abs(got - want).max())
+    rl2 = float(np.linalg.norm(got - want) / np.linalg.norm(want))
+    bar = 5e-3 if wfmt == "bf16" else 1e-2
+    assert np.isfinite(got).all()
+    assert err <= 2.0 ** -7 * np.abs(want).max() and rl2 <= bar, (err, np.abs(want).max(), rl2)
+    s = gpu_stream(w)
+    assert torch.equal(s.out.view(torch.int16), r.out.view(torch.int16))
+    w.close()
