@@ -1,7 +1,7 @@
 """Runs the slot path of one workload for a few steps, for a profiler.
 
     python -m offloaded_expert_slot_gb300.profile_case [--config NAME]
-        [--slots S --prefill P] [--steps N] [--warm]
+        [--slots S --prefill P] [--tokens T] [--steps N] [--warm]
 
 Each step restores the cache tables to the workload's seeded pre-fill and
 runs moe_layer_forward_slots on the default stream, as bench.py's timed
@@ -34,12 +34,15 @@ def main() -> int:
     ap.add_argument("--prefill", type=int, default=-1)
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--warm", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0)
     a = ap.parse_args()
     cfg = CONFIGS[a.config]
     if a.slots:
         cfg = scaled(cfg, S=a.slots)
     if a.prefill >= 0:
         cfg = scaled(cfg, prefill=a.prefill)
+    if a.tokens:
+        cfg = scaled(cfg, T=a.tokens)
     build.build()
     oes.load()
     rb, E = cfg.row_bytes, cfg.E
