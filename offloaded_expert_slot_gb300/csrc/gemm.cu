@@ -140,6 +140,30 @@ __device__ int fill_filtered_units(const GemmParams& p, int nb, UnitRec* utab, i
     const int e = p.block_expert[b];
     return e >= 0 && e < p.E && p.flags[e] == p.filter && p.sorted_ids[(int64_t)b * p.BN] < p.R;
   };
+  if (nb <= nthr) {
+    // one block per thread: count and rank from one round of loads
+    const bool sel = tid < nb && selected(tid);
+    const unsigned bal = __ballot_sync(0xffffffffu, sel);
+    if (lane == 0) s_scan[warp] = __popc(bal);
+    __syncthreads();
+    int off = 0, n = 0;
+    for (int i = 0; i < nw; ++i) {
+      if (i < warp) off += s_scan[i];
+      n += s_scan[i];
+    }
+    const int units = n * p.n_mtiles;
+    if (units > kMaxUnitsPerCta * (int)gridDim.x) return -1;
+    if (sel) {
+      const int g = off + __popc(bal & ((1u << lane) - 1u));
+      const int nvalid = block_nvalid(p, tid);
+      const int slot = p.e2s[p.block_expert[tid]];
+      for (int m = 0; m < p.n_mtiles; ++m) {
+        const int v = g * p.n_mtiles + m;
+        if (v % (int)gridDim.x == (int)blockIdx.x) utab[v / gridDim.x] = UnitRec{tid, m, slot, nvalid};
+      }
+    }
+    return units;
+  }
   int mine = 0;
   for (int b = tid; b < nb; b += nthr) mine += selected(b) ? 1 : 0;
 #pragma unroll
