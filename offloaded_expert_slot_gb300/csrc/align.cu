@@ -35,6 +35,7 @@ struct AlignWs {
 __global__ void __launch_bounds__(kAlignThreads)
     align_count_kernel(const int32_t* __restrict__ ids, int R, int E, int C, int ignore_invalid,
                        AlignWs ws, int32_t* __restrict__ status) {
+  pdl_begin();
   extern __shared__ int32_t hist[];
   const int g = blockIdx.x;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
@@ -53,6 +54,7 @@ __global__ void __launch_bounds__(kAlignThreads)
 
 __global__ void __launch_bounds__(1024)
     align_scan_kernel(int G, int E, int B, AlignWs ws, int32_t* __restrict__ n_post_pad) {
+  pdl_begin();
   extern __shared__ int32_t padded[];  // [E]
   __shared__ int warp_tot[32];
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, w = tid >> 5;
@@ -112,6 +114,7 @@ __global__ void __launch_bounds__(kAlignThreads)
     align_scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int B, int C, int G,
                          int64_t cap, AlignWs ws, int32_t* __restrict__ sorted_ids,
                          int32_t* __restrict__ block_expert) {
+  pdl_begin();
   extern __shared__ int32_t sm[];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   if ((int)blockIdx.x < G) {
@@ -193,6 +196,7 @@ __global__ void __launch_bounds__(1024)
                        int ignore_invalid, int32_t* __restrict__ sorted_ids,
                        int32_t* __restrict__ block_expert, int32_t* __restrict__ n_post_pad,
                        int32_t* __restrict__ status) {
+  pdl_begin();
   extern __shared__ int32_t sm[];
   int32_t* cnt = sm;           // [E]
   int32_t* off = sm + E;       // [E]
@@ -319,7 +323,7 @@ extern "C" int moe_align_block_size(const int32_t* ids, int R, int E, int B, int
   const int64_t cap = OES_ALIGN_CAPACITY(R, E, B);
   if (R <= kSmallR) {
     const size_t smem = ((size_t)2 * E + std::max(R, 1)) * 4;  // at most 36 KB
-    align_small_kernel<<<1, 1024, smem, stream>>>(ids, R, E, B, cap, ignore_invalid, sorted_ids,
+    launch_kernel(align_small_kernel, 1, 1024, smem, stream, ids, R, E, B, cap, ignore_invalid, sorted_ids,
                                                   block_expert, n_post_pad, status);
     OES_CHECK_LAUNCH("align_small_kernel");
     return OES_OK;
@@ -339,13 +343,13 @@ extern "C" int moe_align_block_size(const int32_t* ids, int R, int E, int B, int
                                         scat_smem, "align_scatter_kernel: shared memory limit");
     if (rc) return rc;
   }
-  align_count_kernel<<<G, kAlignThreads, hist_smem, stream>>>(ids, R, E, C, ignore_invalid, ws, status);
+  launch_kernel(align_count_kernel, G, kAlignThreads, hist_smem, stream, ids, R, E, C, ignore_invalid, ws, status);
   OES_CHECK_LAUNCH("align_count_kernel");
-  align_scan_kernel<<<1, 1024, hist_smem, stream>>>(G, E, B, ws, n_post_pad);
+  launch_kernel(align_scan_kernel, 1, 1024, hist_smem, stream, G, E, B, ws, n_post_pad);
   OES_CHECK_LAUNCH("align_scan_kernel");
   const int fill_ctas = (int)std::min<int64_t>(
       std::max<int64_t>(1, ceil_div64(cap / B, kAlignWarps * 4)), (int64_t)num_sms());
-  align_scatter_kernel<<<G + fill_ctas, kAlignThreads, scat_smem, stream>>>(
+  launch_kernel(align_scatter_kernel, G + fill_ctas, kAlignThreads, scat_smem, stream, 
       ids, R, E, B, C, G, cap, ws, sorted_ids, block_expert);
   OES_CHECK_LAUNCH("align_scatter_kernel");
   return OES_OK;

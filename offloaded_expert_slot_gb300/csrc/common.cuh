@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "oes.h"
 
 namespace oes {
@@ -43,6 +45,29 @@ int prefer_max_shared_carveout(const void* func, const char* name);
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Every kernel of the library is launched as a programmatic dependent of the
+// kernel before it on the stream: the launch may begin while that kernel is
+// still running, and the kernel's first statement, pdl_begin(), waits until
+// it has completed and its memory is visible.  So no kernel touches global
+// memory before its predecessor is done, and the launch latency between
+// dependent kernels (route -> distinct -> ensure -> ... -> combine) overlaps
+// the predecessor's tail.  Inside a captured graph the same order holds.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // cuTensorMapEncodeTiled, fetched through the runtime's driver entry point so
 // the library does not link libcuda.
 int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
@@ -56,6 +81,15 @@ __device__ __forceinline__ void set_status(int32_t* status, int32_t bits) {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// First statement of every kernel: wait for the previous kernel on the
+// stream to complete (a no-op for a launch that is not programmatic), then
+// let the next kernel on the stream be launched.  Its CTAs are released only
+// once every CTA of this grid has started, and they wait the same way.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ----- mbarrier

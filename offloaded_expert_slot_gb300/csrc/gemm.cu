@@ -339,6 +339,7 @@ __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 template <int MODE, int WF>
 __global__ void __launch_bounds__(gemm_threads(WF), 1)
     grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  pdl_begin();
   constexpr int kA = (MODE == 1) ? 2 : 1;  // weight tiles per stage (gate + up, or w2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
@@ -700,6 +701,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
 template <int MODE, int WF>
 __global__ void __maxnreg__(64)
     grouped_gemm_tm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
+  pdl_begin();
   constexpr int kN = 256;                  // weight rows per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
@@ -1039,6 +1041,7 @@ __global__ void __maxnreg__(64)
 // f16 copy of x for the NVFP4 path (its MMAs run on f16 operands).
 __global__ void x_to_f16_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ x16,
                                 int64_t n) {
+  pdl_begin();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
     const float f = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
@@ -1051,6 +1054,7 @@ __global__ void x_to_f16_kernel(const uint16_t* __restrict__ x, uint16_t* __rest
 // OES_DEV_BAD_ID and replaced by 1.
 __global__ void act_scale_kernel(const float* __restrict__ in13, const float* __restrict__ in2,
                                  int E, float* __restrict__ act, int32_t* __restrict__ status) {
+  pdl_begin();
   __shared__ float red[2][32];
   float m13 = -INFINITY, m2 = -INFINITY;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -1082,6 +1086,7 @@ __global__ void act_scale_kernel(const float* __restrict__ in13, const float* __
 // W4A4: x [T, H] bf16 -> x16 [T, H] f16 holding q * sf per block of 16 along H.
 __global__ void x_quant_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ x16,
                                int64_t nblk, const float* __restrict__ act) {
+  pdl_begin();
   const float a = act[0];
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nblk;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -1106,6 +1111,7 @@ __global__ void x_quant_kernel(const uint16_t* __restrict__ x, uint16_t* __restr
 __global__ void combine_kernel(const uint16_t* __restrict__ y, const float* __restrict__ w,
                                const int32_t* __restrict__ ids, int T, int k, int H, int E,
                                uint16_t* __restrict__ out) {
+  pdl_begin();
   const int vec = H / 8;
   const int64_t n = (int64_t)T * vec;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
@@ -1230,7 +1236,7 @@ int launch_gemm_tm(const GemmMaps& maps, const GemmParams& p0, cudaStream_t stre
   if ((rc = set_max_dynamic_smem(reinterpret_cast<const void*>(grouped_gemm_tm_kernel<MODE, WF>),
                                   smem, "grouped_gemm_tm_kernel: shared memory limit")))
     return rc;
-  grouped_gemm_tm_kernel<MODE, WF><<<num_sms(), gemm_threads_tm(WF), smem, stream>>>(maps, p);
+  launch_kernel(grouped_gemm_tm_kernel<MODE, WF>, num_sms(), gemm_threads_tm(WF), smem, stream, maps, p);
   OES_CHECK_LAUNCH("grouped_gemm_tm_kernel");
   return OES_OK;
 }
@@ -1249,7 +1255,7 @@ int launch_gemm(const GemmMaps& maps, const GemmParams& p0, int BN, cudaStream_t
   if ((rc = set_max_dynamic_smem(reinterpret_cast<const void*>(grouped_gemm_kernel<MODE, WF>), smem,
                                   "grouped_gemm_kernel: shared memory limit")))
     return rc;
-  grouped_gemm_kernel<MODE, WF><<<num_sms(), gemm_threads(WF), smem, stream>>>(maps, p);
+  launch_kernel(grouped_gemm_kernel<MODE, WF>, num_sms(), gemm_threads(WF), smem, stream, maps, p);
   OES_CHECK_LAUNCH("grouped_gemm_kernel");
   return OES_OK;
 }
@@ -1433,15 +1439,15 @@ int gemm_prepare_x(const GemmPlan& g, cudaStream_t stream) {
   if (g.empty || !g.wf) return OES_OK;
   const int64_t n = (int64_t)g.T * g.H;
   if (g.a4) {
-    act_scale_kernel<<<1, 256, 0, stream>>>(g.in13, g.in2, g.E, g.act, g.status);
+    launch_kernel(act_scale_kernel, 1, 256, 0, stream, g.in13, g.in2, g.E, g.act, g.status);
     OES_CHECK_LAUNCH("act_scale_kernel");
     const int64_t nblk = n / 16;
     const int blocks = (int)std::min<int64_t>(ceil_div64(nblk, 256), (int64_t)num_sms() * 8);
-    x_quant_kernel<<<blocks, 256, 0, stream>>>(g.x, g.x16, nblk, g.act);
+    launch_kernel(x_quant_kernel, blocks, 256, 0, stream, g.x, g.x16, nblk, g.act);
     OES_CHECK_LAUNCH("x_quant_kernel");
   } else {
     const int blocks = (int)std::min<int64_t>(ceil_div64(n, 256), (int64_t)num_sms() * 8);
-    x_to_f16_kernel<<<blocks, 256, 0, stream>>>(g.x, g.x16, n);
+    launch_kernel(x_to_f16_kernel, blocks, 256, 0, stream, g.x, g.x16, n);
     OES_CHECK_LAUNCH("x_to_f16_kernel");
   }
   return OES_OK;
@@ -1470,8 +1476,7 @@ int gemm_combine(const GemmPlan& g, const int32_t* ids, const float* weights, ui
   OES_REQUIRE(ids && weights && out && ((uintptr_t)out & 15) == 0,
               "moe_grouped_gemm_slots: ids, weights and a 16-byte aligned out are required");
   const int64_t nvec = (int64_t)g.T * (g.H / 8);
-  combine_kernel<<<(int)std::min<int64_t>(ceil_div64(nvec, 256), (int64_t)num_sms() * 8), 256, 0,
-                   stream>>>(g.y, weights, ids, g.T, g.k, g.H, g.E, out);
+  launch_kernel(combine_kernel, (int)std::min<int64_t>(ceil_div64(nvec, 256), (int64_t)num_sms() * 8), 256, 0, stream, g.y, weights, ids, g.T, g.k, g.H, g.E, out);
   OES_CHECK_LAUNCH("combine_kernel");
   return OES_OK;
 }

@@ -93,6 +93,7 @@ __global__ void group_flags_kernel(const int32_t* __restrict__ distinct, int n, 
                                    const int32_t* __restrict__ miss,
                                    const int32_t* __restrict__ n_miss, int Q,
                                    uint8_t* __restrict__ group) {
+  pdl_begin();
   for (int e = threadIdx.x; e < E; e += blockDim.x) group[e] = 0;
   __syncthreads();
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
@@ -110,6 +111,7 @@ __global__ void group_flags_kernel(const int32_t* __restrict__ distinct, int n, 
 }
 
 __global__ void iota_kernel(int32_t* a, int n) {
+  pdl_begin();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) a[i] = i;
 }
 
@@ -231,7 +233,7 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
     if ((rc = query(q, side))) return rc;
     OES_TRY_CUDA(cudaEventRecord(cache->ensured[q], side));
   }
-  group_flags_kernel<<<1, 1024, 0, side>>>(w.distinct, Lq, E, layer, w.miss, w.n_miss, Q,
+  launch_kernel(group_flags_kernel, 1, 1024, 0, side, w.distinct, Lq, E, layer, w.miss, w.n_miss, Q,
                                            w.resident);
   OES_CHECK_LAUNCH("group_flags_kernel");
   if ((rc = moe_align_block_size(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad,
@@ -299,7 +301,7 @@ extern "C" int moe_layer_forward_stream(const oes_expert_source* src, void* laye
     OES_TRY_CUDA(cudaEventCreateWithFlags(&copied, cudaEventDisableTiming));
     OES_TRY_CUDA(cudaEventRecord(copied, copy_stream));
   }
-  iota_kernel<<<ceil_div(E, 256), 256, 0, compute_stream>>>(w.e2s_identity, E);
+  launch_kernel(iota_kernel, ceil_div(E, 256), 256, 0, compute_stream, w.e2s_identity, E);
   OES_CHECK_LAUNCH("iota_kernel");
   if ((rc = route(d, c, w, compute_stream))) return rc;
   if ((rc = moe_align_block_size(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad,

@@ -17,6 +17,7 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t b) {
 // logits[t, e] = sum_h x[t, h] * gate[h, e]; one thread per (t, e), h in order.
 __global__ void gate_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gate,
                                    int T, int H, int E, float* __restrict__ logits) {
+  pdl_begin();
   const int t = blockIdx.y;
   for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x) {
     float acc = 0.f;
@@ -33,6 +34,7 @@ __global__ void gate_logits_kernel(const uint16_t* __restrict__ x, const uint16_
 template <int EPL>
 __global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                             int32_t* __restrict__ ids, float* __restrict__ weights) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
@@ -91,6 +93,7 @@ __global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int 
 __global__ void __launch_bounds__(1024)
     distinct_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ distinct,
                     int32_t* __restrict__ d_count) {
+  pdl_begin();
   extern __shared__ uint8_t flag[];
   __shared__ int warp_tot[32];
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -146,7 +149,7 @@ extern "C" int moe_gate_logits(const uint16_t* x, const uint16_t* gate, int T, i
               "moe_gate_logits: bad sizes T=%d H=%d E=%d", T, H, E);
   const int threads = E < 256 ? ((E + 31) / 32) * 32 : 256;
   dim3 grid(ceil_div(E, threads), T);
-  gate_logits_kernel<<<grid, threads, 0, stream>>>(x, gate, T, H, E, logits);
+  launch_kernel(gate_logits_kernel, grid, threads, 0, stream, x, gate, T, H, E, logits);
   OES_CHECK_LAUNCH("gate_logits_kernel");
   return OES_OK;
 }
@@ -160,7 +163,7 @@ extern "C" int moe_route_topk(const float* logits, int T, int E, int k, int32_t*
   const int threads = 128;
   const int blocks = (int)std::min<int64_t>(ceil_div64((int64_t)T * 32, threads), (int64_t)num_sms() * 16);
   const int epl = ceil_div(E, 32);
-#define OES_TOPK(N) topk_kernel<N><<<blocks, threads, 0, stream>>>(logits, T, E, k, ids, weights)
+#define OES_TOPK(N) launch_kernel(topk_kernel<N>, blocks, threads, 0, stream, logits, T, E, k, ids, weights)
   if (epl <= 1) OES_TOPK(1);
   else if (epl <= 2) OES_TOPK(2);
   else if (epl <= 4) OES_TOPK(4);
@@ -178,7 +181,7 @@ extern "C" int moe_distinct_experts(const int32_t* ids, int R, int E, int32_t* d
                                     int32_t* d_count, oes_stream_t stream) {
   OES_REQUIRE(d_count && (R == 0 || (ids && distinct)), "moe_distinct_experts: null pointer");
   OES_REQUIRE(R >= 0 && E >= 1 && E <= OES_MAX_EXPERTS, "moe_distinct_experts: bad R=%d E=%d", R, E);
-  distinct_kernel<<<1, 1024, E, stream>>>(ids, R, E, distinct, d_count);
+  launch_kernel(distinct_kernel, 1, 1024, E, stream, ids, R, E, distinct, d_count);
   OES_CHECK_LAUNCH("distinct_kernel");
   return OES_OK;
 }

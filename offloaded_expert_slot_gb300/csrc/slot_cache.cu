@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(kEnsureThreads)
     ensure_kernel(CacheView c, int layer, const int32_t* __restrict__ experts, int n,
                   int record_stats, int tag, int spad, int32_t* __restrict__ miss,
                   int32_t* __restrict__ n_miss, int32_t* __restrict__ status) {
+  pdl_begin();
   extern __shared__ uint64_t skey[];  // [spad]
   __shared__ int32_t qkey[OES_QUERY_MAX];
   __shared__ int32_t qslot[OES_QUERY_MAX];
@@ -261,6 +262,7 @@ __global__ void __launch_bounds__(kCopyThreads)
                        uint8_t* __restrict__ pool, int S, const int32_t* __restrict__ miss,
                        const int32_t* __restrict__ n_miss_p, int max_misses,
                        int32_t* __restrict__ status) {
+  pdl_begin();
   const int nm = min(*n_miss_p, max_misses);
   const int64_t vecs = row_bytes >> 4;
   const int64_t chunk = (int64_t)kCopyThreads * kCopyUnroll;
@@ -299,6 +301,7 @@ __global__ void __launch_bounds__(kCopyThreads)
 __global__ void __launch_bounds__(kCopyThreads)
     copy_runs_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
                      const CopyRun* __restrict__ runs, int nruns, CopyRun one, int64_t nitems) {
+  pdl_begin();
   const int64_t chunk = (int64_t)kCopyThreads * kCopyUnroll;  // 16-byte vectors per item
   for (int64_t it = blockIdx.x; it < nitems; it += gridDim.x) {
     CopyRun r = one;
@@ -333,6 +336,7 @@ __global__ void __launch_bounds__(kCopyThreads)
 // tens of KB, where a kernel launch beats a copy-engine transfer.
 __global__ void copy_tables_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                                    int64_t n16) {
+  pdl_begin();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n16;
        i += (int64_t)gridDim.x * blockDim.x)
     dst[i] = src[i];
@@ -343,7 +347,7 @@ int copy_tables(const void* src, void* dst, size_t bytes, cudaStream_t stream) {
               "slot cache snapshot/restore: buffers must be 16-byte aligned");
   const int64_t n16 = (int64_t)(bytes / 16);
   const int blocks = (int)std::min<int64_t>((n16 + 255) / 256, (int64_t)num_sms());
-  copy_tables_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(src),
+  launch_kernel(copy_tables_kernel, blocks, 256, 0, stream, static_cast<const uint4*>(src),
                                                   static_cast<uint4*>(dst), n16);
   OES_CHECK_LAUNCH("copy_tables_kernel");
   return OES_OK;
@@ -363,7 +367,7 @@ int launch_copy_runs(const void* src, void* dst, const CopyRun* runs, int nruns,
                                                 "copy_runs_kernel: carveout"))
     return rc;
   const CopyRun one{src_off, dst_off, bytes, 0};
-  copy_runs_kernel<<<num_sms(), kCopyThreads, 0, stream>>>(static_cast<const uint8_t*>(src),
+  launch_kernel(copy_runs_kernel, num_sms(), kCopyThreads, 0, stream, static_cast<const uint8_t*>(src),
                                                           static_cast<uint8_t*>(dst), runs, nruns,
                                                           one, nitems);
   OES_CHECK_LAUNCH("copy_runs_kernel");
@@ -582,7 +586,7 @@ extern "C" int slot_cache_ensure_tagged(oes_slot_cache* c, int layer, const int3
   if ((rc = prefer_max_shared_carveout(reinterpret_cast<const void*>(ensure_kernel),
                                        "ensure_kernel: carveout")))
     return rc;
-  ensure_kernel<<<1, kEnsureThreads, smem, stream>>>(view_of(c), layer, experts, n, record_stats,
+  launch_kernel(ensure_kernel, 1, kEnsureThreads, smem, stream, view_of(c), layer, experts, n, record_stats,
                                                      tag, spad, miss, n_miss, status);
   OES_CHECK_LAUNCH("ensure_kernel");
   return OES_OK;
@@ -646,7 +650,7 @@ extern "C" int slot_cache_copy_misses(const oes_expert_source* src, void* pool, 
                                                 "copy_misses_kernel: carveout"))
     return rc;
   const int grid = num_sms();
-  copy_misses_kernel<<<grid, kCopyThreads, 0, stream>>>(
+  launch_kernel(copy_misses_kernel, grid, kCopyThreads, 0, stream, 
       src->dev_bases, src->L, src->E, src->row_bytes, static_cast<uint8_t*>(pool), S, miss, n_miss,
       max_misses, status);
   OES_CHECK_LAUNCH("copy_misses_kernel");
