@@ -7,9 +7,10 @@
 // ignore_invalid_experts).
 //
 //   count:   CTA g histograms its contiguous range of routes -> cnt[g][e]
-//   scan:    one CTA: per expert, exclusive prefix over CTAs; padded sizes;
+//   scan:    one CTA: per expert, its total over CTAs; padded sizes;
 //            exclusive scan over experts -> expert offsets; cnt[g][e] becomes
-//            the first output position of CTA g's routes of expert e
+//            the first output position of CTA g's routes of expert e (the
+//            expert's offset plus its routes in CTAs before g)
 //   scatter: CTA g re-reads its range; each warp walks its 32-route groups
 //            in order and places them with __match_any_sync ranks, so routes
 //            of one expert keep ascending route order (bit-exact, stable);
@@ -24,6 +25,7 @@ namespace {
 
 constexpr int kAlignThreads = 256;  // 8 warps
 constexpr int kAlignWarps = kAlignThreads / 32;
+constexpr int kScanBatch = 8;   // per-CTA counts one scan thread loads at once
 
 struct AlignWs {
   int32_t* cnt;   // [G][E]
@@ -58,13 +60,16 @@ __global__ void __launch_bounds__(1024)
   extern __shared__ int32_t padded[];  // [E]
   __shared__ int warp_tot[32];
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, w = tid >> 5;
+  // column totals: the loads of a batch are issued together (one round
+  // trip per kScanBatch CTAs instead of one per CTA)
   for (int e = tid; e < E; e += nt) {
     int run = 0;
-    for (int g = 0; g < G; ++g) {
-      const size_t i = (size_t)g * E + e;
-      const int c = ws.cnt[i];
-      ws.cnt[i] = run;
-      run += c;
+    for (int g0 = 0; g0 < G; g0 += kScanBatch) {
+      int c[kScanBatch];
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j) c[j] = (g0 + j < G) ? ws.cnt[(size_t)(g0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j) run += c[j];
     }
     ws.tot[e] = run;
     padded[e] = (run + B - 1) / B * B;
@@ -104,9 +109,19 @@ __global__ void __launch_bounds__(1024)
     *ws.nblk = total / B;
   }
   __syncthreads();
+  // cnt[g][e] <- offset of expert e + routes of e in CTAs before g
   for (int e = tid; e < E; e += nt) {
-    const int base = ws.off[e];
-    for (int g = 0; g < G; ++g) ws.cnt[(size_t)g * E + e] += base;
+    int run = ws.off[e];
+    for (int g0 = 0; g0 < G; g0 += kScanBatch) {
+      int c[kScanBatch];
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j) c[j] = (g0 + j < G) ? ws.cnt[(size_t)(g0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j) {
+        if (g0 + j < G) ws.cnt[(size_t)(g0 + j) * E + e] = run;
+        run += c[j];
+      }
+    }
   }
 }
 
