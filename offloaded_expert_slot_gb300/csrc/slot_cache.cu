@@ -40,10 +40,10 @@ constexpr uint64_t kCrfSat = (1ull << 51) - 1;     // saturation; leaves 13 bits
 
 constexpr int kEnsureThreads = 1024;
 
-// One ensure query in one CTA.  Victims: the non-hit slots ordered by a
-// 64-bit key sorted with a shared-memory bitonic network.  LRU: key =
-// (timestamp << 16 | slot); empty slots have timestamp 0 and so come first,
-// in slot order.  LRFU (Lee et al., IEEE Trans. Computers 2001, with
+// One ensure query in one CTA.  Victims: the nmiss smallest 64-bit keys of
+// the non-hit slots, in ascending order, found by a radix select (no full
+// sort).  LRU: key = (timestamp << 16 | slot); empty slots have timestamp 0
+// and so come first, in slot order.  LRFU (Lee et al., IEEE Trans. Computers 2001, with
 // F(x) = (1 - 2^-k)^x): every slot's score decays once (crf -= crf >> k),
 // then key = (score << 13 | slot) over the slots that are neither hit nor
 // pinned to this query's tag, empty slots scoring 0; hits gain 1.0, fills
@@ -155,52 +155,117 @@ __global__ void __launch_bounds__(kEnsureThreads)
   const int nmiss = s_nmiss, nhit = s_nhit;
   const int slot_bits = lrfu ? 13 : 16;
 
-  // 3. key the evictable slots (LRU: timestamp, LRFU: decayed score) and,
-  // when there are misses, sort them ascending
-  for (int s = tid; s < spad; s += blockDim.x) {
-    uint64_t k = ~0ull;
-    if (s < c.S && !(hitmask[s >> 5] & (1u << (s & 31))) && !(use_tag && c.pin[s] == use_tag)) {
-      uint64_t v;
-      if (c.slot_key[s] < 0) {
-        v = 0;
-      } else if (lrfu) {
-        const uint64_t crf = c.crf[s];
-        v = min(c.lrfu_k ? crf - (crf >> c.lrfu_k) : crf, kCrfSat);
-      } else {
-        v = static_cast<uint64_t>(c.slot_ts[s]);
+  // 3. when there are misses: key the evictable slots (LRU: timestamp, LRFU:
+  // decayed score; empty slots 0; every key unique by its slot bits) and
+  // select the nmiss smallest keys, ascending, into vic[]: a radix select
+  // finds the nmiss-th smallest key 8 bits at a time from the top
+  // significant digit, then the keys at or below it are ranked by counting
+  __shared__ uint64_t vic[OES_QUERY_MAX];
+  __shared__ uint64_t vsel[OES_QUERY_MAX];
+  __shared__ int hist[256];
+  __shared__ uint32_t s_orw[2][32];
+  __shared__ uint64_t s_prefix;
+  __shared__ int s_need, s_nsel, s_hb;
+  if (nmiss > 0) {
+    uint64_t orv = 0;
+    int navail = 0;
+    for (int base = 0; base < c.S; base += blockDim.x) {
+      const int s = base + tid;
+      uint64_t k = ~0ull;
+      if (s < c.S && !(hitmask[s >> 5] & (1u << (s & 31))) && !(use_tag && c.pin[s] == use_tag)) {
+        uint64_t v;
+        if (c.slot_key[s] < 0) {
+          v = 0;
+        } else if (lrfu) {
+          const uint64_t crf = c.crf[s];
+          v = min(c.lrfu_k ? crf - (crf >> c.lrfu_k) : crf, kCrfSat);
+        } else {
+          v = static_cast<uint64_t>(c.slot_ts[s]);
+        }
+        k = (v << slot_bits) | static_cast<uint64_t>(s);
+        orv |= k;
       }
-      k = (v << slot_bits) | static_cast<uint64_t>(s);
-      atomicAdd(&s_navail, 1);
+      if (s < c.S) skey[s] = k;
+      navail += __popc(__ballot_sync(0xffffffffu, k != ~0ull));
     }
-    skey[s] = k;
-  }
-  __syncthreads();
-  if (nmiss > s_navail) {
+    const uint32_t olo = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(orv));
+    const uint32_t ohi = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(orv >> 32));
+    if (lane == 0) {
+      atomicAdd(&s_navail, navail);
+      s_orw[0][w] = olo;
+      s_orw[1][w] = ohi;
+    }
+    __syncthreads();
+    if (nmiss > s_navail) {
+      if (tid == 0) {
+        set_status(status, OES_DEV_CAPACITY);
+        *n_miss = 0;
+      }
+      return;
+    }
     if (tid == 0) {
-      set_status(status, OES_DEV_CAPACITY);
-      *n_miss = 0;
+      uint64_t o = 0;
+      for (int i = 0; i < (int)(blockDim.x >> 5); ++i)
+        o |= (static_cast<uint64_t>(s_orw[1][i]) << 32) | s_orw[0][i];
+      s_hb = o ? 63 - __clzll(static_cast<long long>(o)) : 0;
+      s_prefix = 0;
+      s_need = nmiss;
+      s_nsel = 0;
     }
-    return;
+    __syncthreads();
+    for (int d = (s_hb / 8) * 8; d >= 0; d -= 8) {
+      for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
+      __syncthreads();
+      const uint64_t prefix = s_prefix;
+      for (int base = 0; base < c.S; base += blockDim.x) {
+        const int s = base + tid;
+        int digit = -1;
+        if (s < c.S) {
+          const uint64_t k = skey[s];
+          if (k != ~0ull && (d + 8 >= 64 || (k >> (d + 8)) == (prefix >> (d + 8))))
+            digit = static_cast<int>((k >> d) & 255u);
+        }
+        const unsigned same = __match_any_sync(0xffffffffu, digit);
+        if (digit >= 0 && lane == __ffs(same) - 1) atomicAdd(&hist[digit], __popc(same));
+      }
+      __syncthreads();
+      if (w == 0) {
+        int h[8], sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          h[j] = hist[lane * 8 + j];
+          sum += h[j];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int x = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += x;
+        }
+        const int need = s_need;
+        const int excl = incl - sum;
+        if (excl < need && need <= incl) {  // the one lane whose bins hold rank `need`
+          int run = excl, j = 0;
+          while (j < 7 && run + h[j] < need) run += h[j++];
+          s_prefix = prefix | (static_cast<uint64_t>(lane * 8 + j) << d);
+          s_need = need - run;
+        }
+      }
+      __syncthreads();
+    }
+    const uint64_t tau = s_prefix;  // the nmiss-th smallest key
+    for (int s = tid; s < c.S; s += blockDim.x)
+      if (skey[s] <= tau) vsel[atomicAdd(&s_nsel, 1)] = skey[s];
+    __syncthreads();
+    if (tid < nmiss) {
+      const uint64_t k = vsel[tid];
+      int r = 0;
+      for (int j = 0; j < nmiss; ++j) r += vsel[j] < k;
+      vic[r] = k;
+    }
+    __syncthreads();
   }
   const int64_t clock_new = c.ctr[0] + 1;
-  if (nmiss > 0) {
-    for (int kk = 2; kk <= spad; kk <<= 1) {
-      for (int j = kk >> 1; j > 0; j >>= 1) {
-        for (int i = tid; i < spad; i += blockDim.x) {
-          const int ixj = i ^ j;
-          if (ixj > i) {
-            const uint64_t a = skey[i], b = skey[ixj];
-            const bool up = (i & kk) == 0;
-            if ((a > b) == up) {
-              skey[i] = b;
-              skey[ixj] = a;
-            }
-          }
-        }
-        __syncthreads();
-      }
-    }
-  }
 
   // LRFU: every slot decays by one query before the hits and fills
   if (lrfu && c.lrfu_k)
@@ -212,7 +277,7 @@ __global__ void __launch_bounds__(kEnsureThreads)
     const int k = qkey[tid];
     const int r = qrank[tid];
     if (r >= 0) {
-      const int v = static_cast<int>(skey[r] & ((1u << slot_bits) - 1u));
+      const int v = static_cast<int>(vic[r] & ((1u << slot_bits) - 1u));
       const int old = c.slot_key[v];
       if (old >= 0 && old < LE) {
         c.map[old] = -1;
