@@ -385,13 +385,17 @@ def gpu_launches(cfg, with_restore=True):
     """Kernels of liboes launched per step of the slot path."""
     R = cfg.T * cfg.k
     Q = (min(R, cfg.E) + 127) // 128
-    # topk, distinct, Q x (ensure, copy), group flags, align x3, gemm1/2 over
-    # the hits, gemm1/2 per query over its copied experts, combine
-    n = 1 + 1 + 2 * Q + 1 + 3 + 2 + 2 * Q + 1
+    align = 1 if R <= 1024 else 3       # one CTA up to 1024 routes, else count/scan/scatter
+    # topk, distinct, Q ensures, 2 copies per query (its misses in two parts),
+    # group flags, align, gemm1/2 over the hits, gemm1/2 per part of each
+    # query over its copied experts, combine
+    n = 1 + 1 + Q + 2 * Q + 1 + align + 2 + 4 * Q + 1
+    if with_restore:
+        n += 1                          # the step's restore of the cache tables
     if cfg.logits == "gate":
         n += 1
     if cfg.wfmt == "nvfp4":
-        n += 1                          # x -> f16
+        n += 2 if cfg.w4a4 else 1       # W4A4: activation scales and x quantised; else x -> f16
     return n
 
 

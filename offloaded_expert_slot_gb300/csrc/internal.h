@@ -23,11 +23,12 @@ struct oes_slot_cache {
   int policy, lrfu_k;    // OES_POLICY_*, LRFU decay shift
   // side stream and events of moe_layer_forward_slots: the later queries'
   // ensures and every GEMM run there while the misses are copied on the
-  // caller's stream; ensured[q] / copied[q] mark query q's ensure and copies
+  // caller's stream; ensured[q] marks query q's ensure, copied[2q + p] the
+  // copies of part p of its misses
   static constexpr int kMaxQueries = OES_MAX_EXPERTS / OES_QUERY_MAX;
   cudaStream_t side;
   cudaEvent_t fork, join;
-  cudaEvent_t ensured[kMaxQueries], copied[kMaxQueries];
+  cudaEvent_t ensured[kMaxQueries], copied[2 * kMaxQueries];
 };
 
 struct oes_expert_source {
@@ -39,6 +40,15 @@ struct oes_expert_source {
 
 namespace oes {
 int tile_plan(int R, int E);
+
+// The slot path copies a query's n misses in two parts, so that the GEMM over
+// the first part's experts runs while the last part is still being copied:
+// part 0 = misses [0, miss_split(n)), part 1 = the last min(n / 2, 16).
+__host__ __device__ inline int miss_split(int n) { return n - (n / 2 < 16 ? n / 2 : 16); }
+// slot_cache_copy_misses for part 0 or 1 of the query's misses (-1: all).
+int copy_misses_part(const oes_expert_source* src, void* pool, int S, const int32_t* miss,
+                     const int32_t* n_miss, int max_misses, int part, int32_t* status,
+                     cudaStream_t stream);
 
 // A contiguous run of bytes from a host-mapped source to device memory;
 // item0 = the run's first 4 KB item in its copy launch.

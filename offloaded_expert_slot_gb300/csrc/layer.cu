@@ -79,8 +79,9 @@ LayerWs carve_layer(void* base, const oes_layer_desc* d, int T, int k) {
 
 // group[e] of the chunk's experts, taken after every query of the chunk has
 // been ensured: kGroupHit for an expert that was a hit in its own query,
-// kGroupMiss0 + q for one that query q missed (0 for experts not in the
-// chunk).  A hit keeps its slot and bytes to the end of the chunk: its query
+// kGroupMiss0 + 2q + p for one that query q missed, p = 0 or 1 the part of
+// the query's misses its copy belongs to (miss_split; 0 for experts not in
+// the chunk).  A hit keeps its slot and bytes to the end of the chunk: its query
 // gives it a newer timestamp than any slot no query of the chunk has
 // touched, and since the pool holds all of the chunk's experts at once
 // (checked up front) every later query finds enough such older slots to
@@ -103,9 +104,10 @@ __global__ void group_flags_kernel(const int32_t* __restrict__ distinct, int n, 
   __syncthreads();
   for (int q = 0; q < Q; ++q) {
     const int m = min(n_miss[q], OES_QUERY_MAX);
+    const int split = miss_split(m);
     for (int i = threadIdx.x; i < m; i += blockDim.x) {
       const int e = miss[(q * OES_QUERY_MAX + i) * 3] - layer * E;
-      if (e >= 0 && e < E) group[e] = (uint8_t)(kGroupMiss0 + q);
+      if (e >= 0 && e < E) group[e] = (uint8_t)(kGroupMiss0 + 2 * q + (i >= split));
     }
   }
 }
@@ -197,9 +199,9 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
                                     q == 0 ? OES_TAG_NEW_CHUNK : OES_TAG_SAME_CHUNK, miss_of(q),
                                     w.n_miss + q, c->status, s);
   };
-  auto copy = [&](int q, cudaStream_t s) {
+  auto copy = [&](int q, int part, cudaStream_t s) {
     const int n = std::min(OES_QUERY_MAX, Lq - q * OES_QUERY_MAX);
-    return slot_cache_copy_misses(src, pool, cache->S, miss_of(q), w.n_miss + q, n, c->status, s);
+    return copy_misses_part(src, pool, cache->S, miss_of(q), w.n_miss + q, n, part, c->status, s);
   };
   // the GEMM is validated and its parameters built before anything is
   // launched: a call that fails here leaves the cache as it was
@@ -242,16 +244,21 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
   if ((rc = gemm_prepare_x(g, side))) return rc;
   if ((rc = gemm_run(g, kGroupHit, w.resident, side))) return rc;
   // caller's stream: each query's misses in query order, each query's copies
-  // after its own ensure; the side stream runs each query's copied experts
-  // once their copies are in
+  // after its own ensure, in two parts; the side stream runs each part's
+  // copied experts once its copies are in, so that after the last copy only
+  // the GEMM over the last part (at most 16 experts) remains
   for (int q = 0; q < Q; ++q) {
     if (q > 0) OES_TRY_CUDA(cudaStreamWaitEvent(stream, cache->ensured[q], 0));
-    if ((rc = copy(q, stream))) return rc;
-    OES_TRY_CUDA(cudaEventRecord(cache->copied[q], stream));
+    for (int p = 0; p < 2; ++p) {
+      if ((rc = copy(q, p, stream))) return rc;
+      OES_TRY_CUDA(cudaEventRecord(cache->copied[2 * q + p], stream));
+    }
   }
   for (int q = 0; q < Q; ++q) {
-    OES_TRY_CUDA(cudaStreamWaitEvent(side, cache->copied[q], 0));
-    if ((rc = gemm_run(g, kGroupMiss0 + q, w.resident, side))) return rc;
+    for (int p = 0; p < 2; ++p) {
+      OES_TRY_CUDA(cudaStreamWaitEvent(side, cache->copied[2 * q + p], 0));
+      if ((rc = gemm_run(g, kGroupMiss0 + 2 * q + p, w.resident, side))) return rc;
+    }
   }
   OES_TRY_CUDA(cudaEventRecord(cache->join, side));
   OES_TRY_CUDA(cudaStreamWaitEvent(stream, cache->join, 0));

@@ -325,16 +325,18 @@ constexpr int kCopyUnroll = 8;
 __global__ void __launch_bounds__(kCopyThreads)
     copy_misses_kernel(const uint8_t* const* __restrict__ bases, int L, int E, int64_t row_bytes,
                        uint8_t* __restrict__ pool, int S, const int32_t* __restrict__ miss,
-                       const int32_t* __restrict__ n_miss_p, int max_misses,
+                       const int32_t* __restrict__ n_miss_p, int max_misses, int part,
                        int32_t* __restrict__ status) {
   pdl_begin();
   const int nm = min(*n_miss_p, max_misses);
+  // part 0 / 1: the misses before / from miss_split(nm); -1: all of them
+  const int i0 = part == 1 ? miss_split(nm) : 0, i1 = part == 0 ? miss_split(nm) : nm;
   const int64_t vecs = row_bytes >> 4;
   const int64_t chunk = (int64_t)kCopyThreads * kCopyUnroll;
   const int64_t per_row = (vecs + chunk - 1) / chunk;
-  const int64_t total = (int64_t)nm * per_row;
+  const int64_t total = (int64_t)(i1 - i0) * per_row;
   for (int64_t it = blockIdx.x; it < total; it += gridDim.x) {
-    const int i = static_cast<int>(it / per_row);
+    const int i = i0 + static_cast<int>(it / per_row);
     const int64_t c0 = (it % per_row) * chunk;
     const int key = miss[3 * i], slot = miss[3 * i + 1];
     if (key < 0 || key >= L * E || slot < 0 || slot >= S) {
@@ -447,7 +449,8 @@ using namespace oes;
 static int release_cache(oes_slot_cache* c) {
   for (int q = 0; q < oes_slot_cache::kMaxQueries; ++q) {
     if (c->ensured[q]) cudaEventDestroy(c->ensured[q]);
-    if (c->copied[q]) cudaEventDestroy(c->copied[q]);
+    if (c->copied[2 * q]) cudaEventDestroy(c->copied[2 * q]);
+    if (c->copied[2 * q + 1]) cudaEventDestroy(c->copied[2 * q + 1]);
   }
   if (c->join) cudaEventDestroy(c->join);
   if (c->fork) cudaEventDestroy(c->fork);
@@ -485,7 +488,8 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   c->block_bytes = bytes;
   c->side = nullptr;
   c->fork = c->join = nullptr;
-  for (int q = 0; q < oes_slot_cache::kMaxQueries; ++q) c->ensured[q] = c->copied[q] = nullptr;
+  for (int q = 0; q < oes_slot_cache::kMaxQueries; ++q)
+    c->ensured[q] = c->copied[2 * q] = c->copied[2 * q + 1] = nullptr;
   c->block = nullptr;
   cudaError_t e = cudaMalloc(&c->block, bytes);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking);
@@ -493,7 +497,8 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->join, cudaEventDisableTiming);
   for (int q = 0; q < oes_slot_cache::kMaxQueries && e == cudaSuccess; ++q) {
     e = cudaEventCreateWithFlags(&c->ensured[q], cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->copied[q], cudaEventDisableTiming);
+    for (int p = 0; p < 2 && e == cudaSuccess; ++p)
+      e = cudaEventCreateWithFlags(&c->copied[2 * q + p], cudaEventDisableTiming);
   }
   if (e != cudaSuccess) {
     release_cache(c);
@@ -700,9 +705,10 @@ extern "C" int oes_expert_source_destroy(oes_expert_source* s) {
   return OES_OK;
 }
 
-extern "C" int slot_cache_copy_misses(const oes_expert_source* src, void* pool, int S,
-                                      const int32_t* miss, const int32_t* n_miss, int max_misses,
-                                      int32_t* status, oes_stream_t stream) {
+namespace oes {
+int copy_misses_part(const oes_expert_source* src, void* pool, int S, const int32_t* miss,
+                     const int32_t* n_miss, int max_misses, int part, int32_t* status,
+                     cudaStream_t stream) {
   OES_REQUIRE(src && pool && miss && n_miss, "slot_cache_copy_misses: null pointer");
   OES_REQUIRE(S >= 1 && max_misses >= 0 && max_misses <= OES_QUERY_MAX,
               "slot_cache_copy_misses: bad S=%d max_misses=%d", S, max_misses);
@@ -715,11 +721,18 @@ extern "C" int slot_cache_copy_misses(const oes_expert_source* src, void* pool, 
                                                 "copy_misses_kernel: carveout"))
     return rc;
   const int grid = num_sms();
-  launch_kernel(copy_misses_kernel, grid, kCopyThreads, 0, stream, 
-      src->dev_bases, src->L, src->E, src->row_bytes, static_cast<uint8_t*>(pool), S, miss, n_miss,
-      max_misses, status);
+  launch_kernel(copy_misses_kernel, grid, kCopyThreads, 0, stream, src->dev_bases, src->L, src->E,
+                src->row_bytes, static_cast<uint8_t*>(pool), S, miss, n_miss, max_misses, part,
+                status);
   OES_CHECK_LAUNCH("copy_misses_kernel");
   return OES_OK;
+}
+}  // namespace oes
+
+extern "C" int slot_cache_copy_misses(const oes_expert_source* src, void* pool, int S,
+                                      const int32_t* miss, const int32_t* n_miss, int max_misses,
+                                      int32_t* status, oes_stream_t stream) {
+  return copy_misses_part(src, pool, S, miss, n_miss, max_misses, -1, status, stream);
 }
 
 extern "C" int oes_copy_layer(const oes_expert_source* src, int layer, void* dst,
