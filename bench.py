@@ -39,11 +39,15 @@ from offloaded_expert_slot_gb300.configs import CONFIGS  # noqa: E402
 DEFAULT_CONFIG = "c2_decode_width"
 METRIC = "routed tokens/s per MoE layer (1xGB300)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) per copy_misses_kernel launch on the decode-width
-# workload, from one ncu capture of the current kernel (one warp per SM):
-# 0.05 MB read + 123.2 MB written.  Valid only for that workload and kernel.
-COPY_TRAFFIC_WORKLOAD = "c2_decode_width"
-COPY_TRAFFIC_PER_LAUNCH = 123.26e6
+# DRAM bytes (read + write) on the decode-width workload from one ncu
+# capture of the current kernels, of the launches the breakdown times
+# (`python bench.py --breakdown --steps 2`, profiles/launch_list_c2_decode_width.md):
+# per whole-query copy_misses_kernel launch (three a step, the third query
+# empty) 0.1 MB read + 123.9 MB written; per step the grouped GEMM (GEMM1,
+# GEMM2, combine) 2342.5 MB.  Valid only for that workload and these kernels.
+TRAFFIC_WORKLOAD = "c2_decode_width"
+COPY_TRAFFIC_PER_LAUNCH = 123.96e6
+GEMM_TRAFFIC_PER_STEP = 2342.5e6
 
 
 def peaks():
@@ -485,12 +489,13 @@ def gpu_arm(args, cfg):
     gemm_hbm = g["GB/s"]
     roof_gemm = {"kernel": "grouped_gemm (gemm1 + gemm2 + combine)", "bound": "hbm",
                  "achieved": gemm_hbm, "peak": hbm, "unit": "GB/s", "frac": gemm_hbm / hbm,
-                 "traffic": None, "peak_source": pk["source"],
+                 "traffic": GEMM_TRAFFIC_PER_STEP if cfg.name == TRAFFIC_WORKLOAD else None,
+                 "peak_source": pk["source"],
                  "algorithmic_bytes": step_bytes["gemm"], "launch_ms": bd["gemm"]}
     if dom == "copy":
         c = kernels["copy"]
         q = info["queries"]
-        traffic = COPY_TRAFFIC_PER_LAUNCH if cfg.name == COPY_TRAFFIC_WORKLOAD else None
+        traffic = COPY_TRAFFIC_PER_LAUNCH if cfg.name == TRAFFIC_WORKLOAD else None
         roofline = {"kernel": "copy_misses_kernel", "bound": "host_link", "achieved": c["GB/s"],
                     "peak": link, "unit": "GB/s", "frac": c["frac"], "traffic": traffic,
                     "traffic_note": "DRAM read + write per launch from one ncu capture; the rows "
@@ -863,6 +868,21 @@ def decode_warm(args):
         torch.cuda.empty_cache()
 
 
+def breakdown_only(args):
+    """The per-step breakdown of bench.py's timed step alone: route, distinct,
+    each query's ensure and whole-query copy, align and the grouped GEMM as
+    separate calls on one stream (the launches the roofline line times), one
+    JSON line of per-kernel milliseconds."""
+    import torch
+    from offloaded_expert_slot_gb300 import build
+    build.build()
+    cfg = CONFIGS[args.config]
+    b = Bench(cfg, 0)
+    bd, info = b.breakdown(max(1, args.steps))
+    torch.cuda.synchronize()
+    print(json.dumps({"breakdown": cfg.name, "ms": bd, **info}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -878,7 +898,13 @@ def main():
                     help="decode steps with every routed expert resident (GEMM-bound), per width")
     ap.add_argument("--layers", action="store_true",
                     help="every layer of the workload in turn: slot path, staged, streamed")
+    ap.add_argument("--breakdown", action="store_true",
+                    help="only the per-step breakdown (each step's kernels as separate calls, "
+                         "timed with events), for a profiler")
     args = ap.parse_args()
+    if args.breakdown:
+        breakdown_only(args)
+        return
     if args.decode_warm:
         decode_warm(args)
         return
