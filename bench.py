@@ -389,11 +389,13 @@ def gpu_launches(cfg, with_restore=True):
     """Kernels of liboes launched per step of the slot path."""
     R = cfg.T * cfg.k
     Q = (min(R, cfg.E) + 127) // 128
+    Lq = min(R, cfg.E)
     align = 1 if R <= 1024 else 3       # one CTA up to 1024 routes, else count/scan/scatter
-    # topk, distinct, Q ensures, 2 copies per query (its misses in two parts),
-    # group flags, align, gemm1/2 over the hits, gemm1/2 per part of each
-    # query over its copied experts, combine
-    n = 1 + 1 + Q + 2 * Q + 1 + align + 2 + 4 * Q + 1
+    # a query of more than 32 ids copies its misses in two parts
+    parts = sum(2 if min(128, Lq - 128 * q) > 32 else 1 for q in range(Q))
+    # topk, distinct, Q ensures, a copy per part, group flags, align,
+    # gemm1/2 over the hits, gemm1/2 per part over its copied experts, combine
+    n = 1 + 1 + Q + parts + 1 + align + 2 + 2 * parts + 1
     if with_restore:
         n += 1                          # the step's restore of the cache tables
     if cfg.logits == "gate":

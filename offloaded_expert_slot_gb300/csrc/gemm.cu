@@ -340,6 +340,8 @@ template <int MODE, int WF>
 __global__ void __launch_bounds__(gemm_threads(WF), 1)
     grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   pdl_begin();
+  // a filtered launch over a group with no experts has nothing to do
+  if (p.filter && p.gcount && p.gcount[p.filter] == 0) return;
   constexpr int kA = (MODE == 1) ? 2 : 1;  // weight tiles per stage (gate + up, or w2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
@@ -702,6 +704,8 @@ template <int MODE, int WF>
 __global__ void __maxnreg__(64)
     grouped_gemm_tm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
   pdl_begin();
+  // a filtered launch over a group with no experts has nothing to do
+  if (p.filter && p.gcount && p.gcount[p.filter] == 0) return;
   constexpr int kN = 256;                  // weight rows per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
@@ -1455,11 +1459,13 @@ int gemm_prepare_x(const GemmPlan& g, cudaStream_t stream) {
 
 // GEMM1 then GEMM2 over the blocks `filter` selects (flags: device [E]
 // group of each expert; filter 0 = every block).
-int gemm_run(const GemmPlan& g, int filter, const uint8_t* flags, cudaStream_t stream) {
+int gemm_run(const GemmPlan& g, int filter, const uint8_t* flags, const int32_t* gcount,
+             cudaStream_t stream) {
   if (g.empty) return OES_OK;
   GemmParams p1 = g.p1, p2 = g.p2;
   p1.filter = p2.filter = filter;
   p1.flags = p2.flags = flags;
+  p1.gcount = p2.gcount = gcount;
   const int B = p1.BN;
   int rc;
   if (g.tm) rc = g.wf ? launch_gemm_tm<1, 1>(g.m1, p1, stream) : launch_gemm_tm<1, 0>(g.m1, p1, stream);
@@ -1495,6 +1501,6 @@ extern "C" int moe_grouped_gemm_slots(const oes_routed_experts* v, const uint16_
                         workspace_bytes, status, &g);
   if (rc) return rc;
   if ((rc = gemm_prepare_x(g, stream))) return rc;
-  if ((rc = gemm_run(g, 0, nullptr, stream))) return rc;
+  if ((rc = gemm_run(g, 0, nullptr, nullptr, stream))) return rc;
   return gemm_combine(g, ids, weights, out, stream);
 }

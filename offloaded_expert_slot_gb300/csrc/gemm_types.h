@@ -23,6 +23,7 @@ struct GemmParams {
   const int32_t* n_post_pad;
   const int32_t* e2s;
   const uint8_t* flags;  // [E] group of each expert (filtered launches)
+  const int32_t* gcount;  // [groups] experts in each group, or null
   int filter;            // 0 all blocks; g > 0 the blocks of experts with flags[e] == g
   int a4;                // W4A4: x and h hold NVFP4-quantised activations
   const float* act;      // W4A4: device [2] activation scales of GEMM1, GEMM2
@@ -60,7 +61,8 @@ int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
 // the x kernels of a prepared GEMM (NVFP4 weights), on `stream`
 int gemm_prepare_x(const GemmPlan& plan, cudaStream_t stream);
 // filter: 0 every block; g > 0 the blocks of experts with flags[e] == g
-int gemm_run(const GemmPlan& plan, int filter, const uint8_t* flags, cudaStream_t stream);
+int gemm_run(const GemmPlan& plan, int filter, const uint8_t* flags, const int32_t* gcount,
+             cudaStream_t stream);
 int gemm_combine(const GemmPlan& plan, const int32_t* ids, const float* weights, uint16_t* out,
                  cudaStream_t stream);
 

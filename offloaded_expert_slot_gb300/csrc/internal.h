@@ -41,10 +41,18 @@ struct oes_expert_source {
 namespace oes {
 int tile_plan(int R, int E);
 
-// The slot path copies a query's n misses in two parts, so that the GEMM over
-// the first part's experts runs while the last part is still being copied:
-// part 0 = misses [0, miss_split(n)), part 1 = the last min(n / 2, 16).
+// The slot path copies the n misses of a query of more than kSplitIds ids in
+// two parts, so that the GEMM over the first part's experts runs while the
+// last part is still being copied: part 0 = misses [0, miss_split(n)),
+// part 1 = the last min(n / 2, 16).  A smaller query's GEMM is one wave of
+// CTAs either way, and its misses go in one part.
+constexpr int kSplitIds = 32;
 __host__ __device__ inline int miss_split(int n) { return n - (n / 2 < 16 ? n / 2 : 16); }
+// Expert groups of the slot path's filtered GEMM launches: 0 not in the
+// chunk, kGroupHit a hit in its own query, kGroupMiss0 + 2q + p missed in
+// part p of query q's misses.
+constexpr int kGroupHit = 1, kGroupMiss0 = 2;
+constexpr int kGroups = kGroupMiss0 + 2 * (OES_MAX_EXPERTS / OES_QUERY_MAX);
 // slot_cache_copy_misses for part 0 or 1 of the query's misses (-1: all).
 int copy_misses_part(const oes_expert_source* src, void* pool, int S, const int32_t* miss,
                      const int32_t* n_miss, int max_misses, int part, int32_t* status,

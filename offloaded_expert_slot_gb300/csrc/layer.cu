@@ -31,6 +31,7 @@ struct LayerWs {
   int32_t* n_post_pad;
   int32_t* e2s_identity;
   uint8_t* resident;  // [E] group of each of the chunk's experts (hit, or missed in query q)
+  int32_t* gcount;    // [kGroups] experts in each group
   void* align_ws;
   size_t align_bytes;
   void* gemm_ws;
@@ -64,6 +65,7 @@ LayerWs carve_layer(void* base, const oes_layer_desc* d, int T, int k) {
   w.n_post_pad = static_cast<int32_t*>(take(4));
   w.e2s_identity = static_cast<int32_t*>(take((size_t)E * 4));
   w.resident = static_cast<uint8_t*>(take((size_t)E));
+  w.gcount = static_cast<int32_t*>(take((size_t)kGroups * 4));
   w.align_bytes = moe_align_workspace_size(R, E, B);
   w.align_ws = take(w.align_bytes);
   oes_routed_experts v{};
@@ -88,14 +90,15 @@ LayerWs carve_layer(void* base, const oes_layer_desc* d, int T, int k) {
 // evict.  An expert resident before the chunk but belonging to a later query
 // has no such guarantee: an earlier query may evict it, and it is then a
 // miss of its own query like any other.
-constexpr int kGroupHit = 1, kGroupMiss0 = 2;
 
 __global__ void group_flags_kernel(const int32_t* __restrict__ distinct, int n, int E, int layer,
                                    const int32_t* __restrict__ miss,
                                    const int32_t* __restrict__ n_miss, int Q,
-                                   uint8_t* __restrict__ group) {
+                                   uint8_t* __restrict__ group, int32_t* __restrict__ gcount) {
   pdl_begin();
+  __shared__ int32_t cnt[kGroups];
   for (int e = threadIdx.x; e < E; e += blockDim.x) group[e] = 0;
+  for (int g = threadIdx.x; g < kGroups; g += blockDim.x) cnt[g] = 0;
   __syncthreads();
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const int e = distinct[i];
@@ -104,12 +107,22 @@ __global__ void group_flags_kernel(const int32_t* __restrict__ distinct, int n, 
   __syncthreads();
   for (int q = 0; q < Q; ++q) {
     const int m = min(n_miss[q], OES_QUERY_MAX);
-    const int split = miss_split(m);
+    const int nq = min(OES_QUERY_MAX, n - q * OES_QUERY_MAX);
+    const int split = nq > kSplitIds ? miss_split(m) : m;
     for (int i = threadIdx.x; i < m; i += blockDim.x) {
       const int e = miss[(q * OES_QUERY_MAX + i) * 3] - layer * E;
       if (e >= 0 && e < E) group[e] = (uint8_t)(kGroupMiss0 + 2 * q + (i >= split));
     }
   }
+  // experts per group: a filtered GEMM launch over an empty group returns
+  // before it deals out units
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int g = group[e];
+    if (g) atomicAdd(&cnt[g], 1);
+  }
+  __syncthreads();
+  for (int g = threadIdx.x; g < kGroups; g += blockDim.x) gcount[g] = cnt[g];
 }
 
 __global__ void iota_kernel(int32_t* a, int n) {
@@ -236,28 +249,32 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
     OES_TRY_CUDA(cudaEventRecord(cache->ensured[q], side));
   }
   launch_kernel(group_flags_kernel, 1, 1024, 0, side, w.distinct, Lq, E, layer, w.miss, w.n_miss, Q,
-                                           w.resident);
+                w.resident, w.gcount);
   OES_CHECK_LAUNCH("group_flags_kernel");
   if ((rc = moe_align_block_size(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad,
                                  c->status, w.align_ws, w.align_bytes, side)))
     return rc;
   if ((rc = gemm_prepare_x(g, side))) return rc;
-  if ((rc = gemm_run(g, kGroupHit, w.resident, side))) return rc;
+  if ((rc = gemm_run(g, kGroupHit, w.resident, w.gcount, side))) return rc;
   // caller's stream: each query's misses in query order, each query's copies
-  // after its own ensure, in two parts; the side stream runs each part's
-  // copied experts once its copies are in, so that after the last copy only
-  // the GEMM over the last part (at most 16 experts) remains
+  // after its own ensure, in two parts when it has more than kSplitIds ids;
+  // the side stream runs each part's copied experts once its copies are in,
+  // so that after the last copy only the GEMM over the last part (at most 16
+  // experts, or a small query's misses) remains
+  auto parts = [&](int q) {
+    return std::min(OES_QUERY_MAX, Lq - q * OES_QUERY_MAX) > kSplitIds ? 2 : 1;
+  };
   for (int q = 0; q < Q; ++q) {
     if (q > 0) OES_TRY_CUDA(cudaStreamWaitEvent(stream, cache->ensured[q], 0));
-    for (int p = 0; p < 2; ++p) {
-      if ((rc = copy(q, p, stream))) return rc;
+    for (int p = 0; p < parts(q); ++p) {
+      if ((rc = copy(q, parts(q) == 2 ? p : -1, stream))) return rc;
       OES_TRY_CUDA(cudaEventRecord(cache->copied[2 * q + p], stream));
     }
   }
   for (int q = 0; q < Q; ++q) {
-    for (int p = 0; p < 2; ++p) {
+    for (int p = 0; p < parts(q); ++p) {
       OES_TRY_CUDA(cudaStreamWaitEvent(side, cache->copied[2 * q + p], 0));
-      if ((rc = gemm_run(g, kGroupMiss0 + 2 * q + p, w.resident, side))) return rc;
+      if ((rc = gemm_run(g, kGroupMiss0 + 2 * q + p, w.resident, w.gcount, side))) return rc;
     }
   }
   OES_TRY_CUDA(cudaEventRecord(cache->join, side));
@@ -319,7 +336,7 @@ extern "C" int moe_layer_forward_stream(const oes_expert_source* src, void* laye
     OES_TRY_CUDA(cudaStreamWaitEvent(compute_stream, copied, 0));
     OES_TRY_CUDA(cudaEventDestroy(copied));
   }
-  if ((rc = gemm_run(g, 0, nullptr, compute_stream))) return rc;
+  if ((rc = gemm_run(g, 0, nullptr, nullptr, compute_stream))) return rc;
   return gemm_combine(g, w.ids, w.w, c->out, compute_stream);
 }
 
@@ -548,7 +565,7 @@ extern "C" int moe_layers_forward_staged(const oes_stage_plan* p, const oes_expe
       if (!rc) rc = gemm_prepare_x(plans[i], compute_stream);
       if (rc) return rc;
       OES_TRY_CUDA(cudaStreamWaitEvent(compute_stream, p->copied[b], 0));
-      if ((rc = gemm_run(plans[i], 0, nullptr, compute_stream))) return rc;
+      if ((rc = gemm_run(plans[i], 0, nullptr, nullptr, compute_stream))) return rc;
       if ((rc = gemm_combine(plans[i], w.ids, w.w, c->out, compute_stream))) return rc;
     } else {
       OES_TRY_CUDA(cudaStreamWaitEvent(compute_stream, p->copied[b], 0));
