@@ -412,8 +412,12 @@ int moe_layer_workspace_views(const oes_layer_desc *layer, int T, int k, void *w
  * (record_stats as given) in order -> align -> grouped GEMM over `pool`
  * through the layer's remap: the experts that were hits run at once on the
  * cache's side stream while each query's misses are copied, in query order,
- * on `stream`; the copied experts run after their copies.  The number of
- * queries is ceil(min(T*k, E) / OES_QUERY_MAX), known on the host.  All
+ * on `stream`; the copied experts run after their copies.  A query of more
+ * than 32 ids copies its misses in two launches (the last min(n/2, 16) of
+ * its n misses second), and the GEMM over each part's experts starts when
+ * that part is in, so after the last copy at most 16 experts' GEMM remains.
+ * The number of queries is ceil(min(T*k, E) / OES_QUERY_MAX), known on the
+ * host.  All
  * ensures go before the copies: ensure reads no pool bytes, and with the
  * chunk fitting the pool no query evicts a slot an earlier query touched,
  * so the tables, the slots written and the bytes are those of ensuring and
