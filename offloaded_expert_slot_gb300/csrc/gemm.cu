@@ -1112,6 +1112,7 @@ __global__ void x_quant_kernel(const uint16_t* __restrict__ x, uint16_t* __restr
 }
 
 // out[t, :] = sum_{j=0..k-1} w[t, j] * y[t*k + j, :], fp32 in j order -> bf16.
+constexpr int kCombineBatch = 8;
 __global__ void combine_kernel(const uint16_t* __restrict__ y, const float* __restrict__ w,
                                const int32_t* __restrict__ ids, int T, int k, int H, int E,
                                uint16_t* __restrict__ out) {
@@ -1123,16 +1124,33 @@ __global__ void combine_kernel(const uint16_t* __restrict__ y, const float* __re
     const int t = static_cast<int>(i / vec);
     const int c = static_cast<int>(i % vec);
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int j = 0; j < k; ++j) {
-      const int e = ids[(int64_t)t * k + j];
-      if (e < 0 || e >= E) continue;
-      const float wj = w[(int64_t)t * k + j];
-      const uint4 v = *reinterpret_cast<const uint4*>(y + ((int64_t)t * k + j) * H + c * 8);
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    // eight routes' rows are loaded together (every y row exists, so the
+    // loads need not wait for the ids), then added in j order, skipping
+    // routes outside [0, E)
+    for (int j0 = 0; j0 < k; j0 += kCombineBatch) {
+      uint4 v[kCombineBatch];
+      float wj[kCombineBatch];
+      bool ok[kCombineBatch];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc[2 * q] = fmaf(wj, __uint_as_float(u[q] << 16), acc[2 * q]);
-        acc[2 * q + 1] = fmaf(wj, __uint_as_float(u[q] & 0xFFFF0000u), acc[2 * q + 1]);
+      for (int b = 0; b < kCombineBatch; ++b) {
+        const int j = j0 + b;
+        ok[b] = false;
+        if (j < k) {
+          const int e = ids[(int64_t)t * k + j];
+          ok[b] = e >= 0 && e < E;
+          wj[b] = w[(int64_t)t * k + j];
+          v[b] = *reinterpret_cast<const uint4*>(y + ((int64_t)t * k + j) * H + c * 8);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kCombineBatch; ++b) {
+        if (!ok[b]) continue;
+        const uint32_t u[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[2 * q] = fmaf(wj[b], __uint_as_float(u[q] << 16), acc[2 * q]);
+          acc[2 * q + 1] = fmaf(wj[b], __uint_as_float(u[q] & 0xFFFF0000u), acc[2 * q + 1]);
+        }
       }
     }
     uint4 o;
