@@ -27,7 +27,7 @@
  *     which say so.
  *   - The return value reports what the host can check before launching:
  *     OES_OK, OES_ERR_INVALID_ARG (null pointer, size out of range, buffer
- *     too small), OES_ERR_UNSUPPORTED (a size this build does not handle),
+ *     too small), OES_ERR_UNSUPPORTED (a size the library does not handle),
  *     OES_ERR_CAPACITY (a chunk the pool cannot hold), OES_ERR_CUDA (a CUDA
  *     call or launch failed; oes_last_error() has the message).  On any
  *     error nothing more is launched.

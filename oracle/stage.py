@@ -4,9 +4,10 @@ Test infrastructure only.  vLLM fork PR #51, Details ("Prefill staging"):
 one placement readback per step turns each layer's experts without a slot
 into maximal contiguous runs; those rows are copied into a whole-layer
 staging buffer (two buffers, alternating by layer); experts with a slot are
-read from the pool and their rows are never written.  Its test checks that
-staging happened (layers staged, rows copied, resident rows untouched) and
-that the output equals the unstaged read byte for byte.
+read from the pool and their rows are never written.  Its test counts the
+layers that went through a staging buffer and the rows that moved, checks
+that rows already in the pool kept their bytes, and compares the output
+with the unstaged read byte for byte.
 
 Readings: with skip_resident off every expert is staged (the whole-layer
 stream with next-layer prefetch); an expert's weights come from its slot

@@ -165,6 +165,24 @@ def test_medium_layers_match_oracle_and_stream(cfg):
     w.close()
 
 
+@pytest.mark.parametrize("prefill", [47, 46, 45, 30, 0])
+def test_two_part_copies(prefill):
+    """One query of 48 ids, more than the 32 above which a query's misses are
+    copied in two launches (the last min(n/2, 16) second), each with its own
+    GEMM: 1, 2, 3, 18 and 48 misses put the split at its edges (an empty
+    second part, a one-miss part, a full 16-miss part)."""
+    lib()
+    cfg = scaled(C2, name=f"split_bf16_p{prefill}", T=40, k=6, E=48, H=128, I=128, S=60, L=1,
+                 prefill=prefill)
+    w = Workload(cfg, gen_device="cpu")
+    o, _ = oracle_slots(w)
+    assert len(o["distinct"]) == 48 and (np.asarray(o["distinct"]) >= 0).all()
+    r = full_check(w)
+    st = oes.slot_cache_read_state(w.cache, cfg.S, cfg.L, cfg.E)
+    assert int((st["slot_key"] >= 0).sum()) == 48           # prefill + misses, all of layer 0
+    w.close()
+
+
 def test_full_pool_two_queries():
     """Every slot full and two queries: query 1's misses evict the oldest
     slots, some holding experts of query 2 that were resident before the

@@ -1,8 +1,9 @@
 """Pins for the oracle's prefill staging (CPU only).
 
 * The hand case in tests/golden/stage_hand.json (vLLM fork PR #51, Details
-  and its staging test: two layers staged, eight rows copied, resident rows
-  untouched), with and without skipping resident experts.
+  and its staging test: both layers go through a buffer, 8 rows move, rows
+  already in the pool keep their bytes), with and without skipping resident
+  experts.
 * Brute force: on random placements the runs are ascending, disjoint,
   maximal, and cover exactly the experts without a slot.
 * The staged layer equals the streamed layer when every slot holds its
