@@ -21,13 +21,15 @@ struct oes_slot_cache {
   uint64_t* crf;         // [S] LRFU score of each slot, Q32.32
   int32_t* pin;          // [S] LRFU pin tag of each slot, 0 = none
   int policy, lrfu_k;    // OES_POLICY_*, LRFU decay shift
-  // side stream and events of moe_layer_forward_slots: the later queries'
-  // ensures and every GEMM run there while the misses are copied on the
-  // caller's stream; ensured[q] marks query q's ensure, copied[2q + p] the
-  // copies of part p of its misses
+  // streams and events of moe_layer_forward_slots: the later queries'
+  // ensures, the align and the GEMM over the hits run on `side`, the GEMM
+  // over each part of each query's copied experts on `gemm`, while the
+  // misses are copied on the caller's stream; ensured[q] marks query q's
+  // ensure, copied[2q + p] the copies of part p of its misses, prepared the
+  // align and the GEMMs' x, join / gjoin the ends of side / gemm
   static constexpr int kMaxQueries = OES_MAX_EXPERTS / OES_QUERY_MAX;
-  cudaStream_t side;
-  cudaEvent_t fork, join;
+  cudaStream_t side = nullptr, gemm = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, prepared = nullptr, gjoin = nullptr;
   cudaEvent_t ensured[kMaxQueries], copied[2 * kMaxQueries];
 };
 

@@ -255,12 +255,14 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
                                  c->status, w.align_ws, w.align_bytes, side)))
     return rc;
   if ((rc = gemm_prepare_x(g, side))) return rc;
+  OES_TRY_CUDA(cudaEventRecord(cache->prepared, side));
   if ((rc = gemm_run(g, kGroupHit, w.resident, w.gcount, side))) return rc;
+  OES_TRY_CUDA(cudaEventRecord(cache->join, side));
   // caller's stream: each query's misses in query order, each query's copies
   // after its own ensure, in two parts when it has more than kSplitIds ids;
-  // the side stream runs each part's copied experts once its copies are in,
-  // so that after the last copy only the GEMM over the last part (at most 16
-  // experts, or a small query's misses) remains
+  // each part's copied experts run once its copies are in, so that after the
+  // last copy only the GEMM over the last part (at most 16 experts, or a
+  // small query's misses) remains
   auto parts = [&](int q) {
     return std::min(OES_QUERY_MAX, Lq - q * OES_QUERY_MAX) > kSplitIds ? 2 : 1;
   };
@@ -271,14 +273,20 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
       OES_TRY_CUDA(cudaEventRecord(cache->copied[2 * q + p], stream));
     }
   }
+  // the gemm stream: each part's copied experts after the align and that
+  // part's copies, beside the GEMM over the hits (empty parts, as in a warm
+  // decode step, then cost the side stream nothing)
+  cudaStream_t gs = cache->gemm;
+  OES_TRY_CUDA(cudaStreamWaitEvent(gs, cache->prepared, 0));
   for (int q = 0; q < Q; ++q) {
     for (int p = 0; p < parts(q); ++p) {
-      OES_TRY_CUDA(cudaStreamWaitEvent(side, cache->copied[2 * q + p], 0));
-      if ((rc = gemm_run(g, kGroupMiss0 + 2 * q + p, w.resident, w.gcount, side))) return rc;
+      OES_TRY_CUDA(cudaStreamWaitEvent(gs, cache->copied[2 * q + p], 0));
+      if ((rc = gemm_run(g, kGroupMiss0 + 2 * q + p, w.resident, w.gcount, gs))) return rc;
     }
   }
-  OES_TRY_CUDA(cudaEventRecord(cache->join, side));
+  OES_TRY_CUDA(cudaEventRecord(cache->gjoin, gs));
   OES_TRY_CUDA(cudaStreamWaitEvent(stream, cache->join, 0));
+  OES_TRY_CUDA(cudaStreamWaitEvent(stream, cache->gjoin, 0));
   return gemm_combine(g, w.ids, w.w, c->out, stream);
 }
 

@@ -454,7 +454,10 @@ static int release_cache(oes_slot_cache* c) {
   }
   if (c->join) cudaEventDestroy(c->join);
   if (c->fork) cudaEventDestroy(c->fork);
+  if (c->prepared) cudaEventDestroy(c->prepared);
+  if (c->gjoin) cudaEventDestroy(c->gjoin);
   if (c->side) cudaStreamDestroy(c->side);
+  if (c->gemm) cudaStreamDestroy(c->gemm);
   cudaError_t e = c->block ? cudaFree(c->block) : cudaSuccess;
   delete c;
   if (e != cudaSuccess) return cuda_fail(e, "cudaFree(slot cache tables)");
@@ -493,8 +496,11 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   c->block = nullptr;
   cudaError_t e = cudaMalloc(&c->block, bytes);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->gemm, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->fork, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->join, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->prepared, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->gjoin, cudaEventDisableTiming);
   for (int q = 0; q < oes_slot_cache::kMaxQueries && e == cudaSuccess; ++q) {
     e = cudaEventCreateWithFlags(&c->ensured[q], cudaEventDisableTiming);
     for (int p = 0; p < 2 && e == cudaSuccess; ++p)
