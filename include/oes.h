@@ -415,7 +415,8 @@ int moe_layer_workspace_views(const oes_layer_desc *layer, int T, int k, void *w
  * on `stream`; the copied experts run after their copies.  A query of more
  * than 32 ids copies its misses in two launches (the last min(n/2, 16) of
  * its n misses second), and the GEMM over each part's experts starts when
- * that part is in, so after the last copy at most 16 experts' GEMM remains.
+ * that part is in (on a second side stream of the cache, beside the GEMM
+ * over the hits), so after the last copy at most 16 experts' GEMM remains.
  * The number of queries is ceil(min(T*k, E) / OES_QUERY_MAX), known on the
  * host.  All
  * ensures go before the copies: ensure reads no pool bytes, and with the
