@@ -22,14 +22,16 @@ struct oes_slot_cache {
   int32_t* pin;          // [S] LRFU pin tag of each slot, 0 = none
   int policy, lrfu_k;    // OES_POLICY_*, LRFU decay shift
   // streams and events of moe_layer_forward_slots: the later queries'
-  // ensures, the align and the GEMM over the hits run on `side`, the GEMM
-  // over each part of each query's copied experts on `gemm`, while the
-  // misses are copied on the caller's stream; ensured[q] marks query q's
-  // ensure, copied[2q + p] the copies of part p of its misses, prepared the
-  // align and the GEMMs' x, join / gjoin the ends of side / gemm
+  // ensures, the group flags and the GEMM over the hits run on `side`; the
+  // align, the GEMMs' x and the GEMM over each part of each query's copied
+  // experts on `gemm`; the misses are copied on the caller's stream.
+  // routed marks the routing, ensured[q] query q's ensure, flagged the
+  // group flags, copied[2q + p] the copies of part p of query q's misses,
+  // prepared the align and x, join / gjoin the ends of side / gemm
   static constexpr int kMaxQueries = OES_MAX_EXPERTS / OES_QUERY_MAX;
   cudaStream_t side = nullptr, gemm = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr, prepared = nullptr, gjoin = nullptr;
+  cudaEvent_t routed = nullptr, flagged = nullptr;
   cudaEvent_t ensured[kMaxQueries], copied[2 * kMaxQueries];
 };
 

@@ -236,13 +236,23 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
     return rc;
   // caller's stream: route, distinct experts, the first query
   if ((rc = route(d, c, w, stream))) return rc;
+  OES_TRY_CUDA(cudaEventRecord(cache->routed, stream));
   if ((rc = moe_distinct_experts(w.ids, R, E, w.distinct, w.d_count, stream))) return rc;
   if ((rc = query(0, stream))) return rc;
   OES_TRY_CUDA(cudaEventRecord(cache->fork, stream));
+  // gemm stream: the align and the GEMMs' x, which need only the routes, run
+  // while the queries are ensured
+  cudaStream_t gs = cache->gemm;
+  OES_TRY_CUDA(cudaStreamWaitEvent(gs, cache->routed, 0));
+  if ((rc = moe_align_block_size(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad,
+                                 c->status, w.align_ws, w.align_bytes, gs)))
+    return rc;
+  if ((rc = gemm_prepare_x(g, gs))) return rc;
+  OES_TRY_CUDA(cudaEventRecord(cache->prepared, gs));
   // side stream: the later queries in order (ensure reads no pool bytes, and
   // with the chunk fitting the pool no query evicts a slot an earlier query
-  // touched, so a query's copies may trail the later ensures), then the
-  // expert groups, the align and the GEMM over the hits
+  // touched, so a query's copies may trail the later ensures), the expert
+  // groups, then the GEMM over the hits once the align is done
   OES_TRY_CUDA(cudaStreamWaitEvent(side, cache->fork, 0));
   for (int q = 1; q < Q; ++q) {
     if ((rc = query(q, side))) return rc;
@@ -251,11 +261,8 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
   launch_kernel(group_flags_kernel, 1, 1024, 0, side, w.distinct, Lq, E, layer, w.miss, w.n_miss, Q,
                 w.resident, w.gcount);
   OES_CHECK_LAUNCH("group_flags_kernel");
-  if ((rc = moe_align_block_size(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad,
-                                 c->status, w.align_ws, w.align_bytes, side)))
-    return rc;
-  if ((rc = gemm_prepare_x(g, side))) return rc;
-  OES_TRY_CUDA(cudaEventRecord(cache->prepared, side));
+  OES_TRY_CUDA(cudaEventRecord(cache->flagged, side));
+  OES_TRY_CUDA(cudaStreamWaitEvent(side, cache->prepared, 0));
   if ((rc = gemm_run(g, kGroupHit, w.resident, w.gcount, side))) return rc;
   OES_TRY_CUDA(cudaEventRecord(cache->join, side));
   // caller's stream: each query's misses in query order, each query's copies
@@ -273,11 +280,10 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
       OES_TRY_CUDA(cudaEventRecord(cache->copied[2 * q + p], stream));
     }
   }
-  // the gemm stream: each part's copied experts after the align and that
-  // part's copies, beside the GEMM over the hits (empty parts, as in a warm
-  // decode step, then cost the side stream nothing)
-  cudaStream_t gs = cache->gemm;
-  OES_TRY_CUDA(cudaStreamWaitEvent(gs, cache->prepared, 0));
+  // the gemm stream: each part's copied experts after the group flags and
+  // that part's copies, beside the GEMM over the hits (empty parts, as in a
+  // warm decode step, then cost the side stream nothing)
+  OES_TRY_CUDA(cudaStreamWaitEvent(gs, cache->flagged, 0));
   for (int q = 0; q < Q; ++q) {
     for (int p = 0; p < parts(q); ++p) {
       OES_TRY_CUDA(cudaStreamWaitEvent(gs, cache->copied[2 * q + p], 0));

@@ -456,6 +456,8 @@ static int release_cache(oes_slot_cache* c) {
   if (c->fork) cudaEventDestroy(c->fork);
   if (c->prepared) cudaEventDestroy(c->prepared);
   if (c->gjoin) cudaEventDestroy(c->gjoin);
+  if (c->routed) cudaEventDestroy(c->routed);
+  if (c->flagged) cudaEventDestroy(c->flagged);
   if (c->side) cudaStreamDestroy(c->side);
   if (c->gemm) cudaStreamDestroy(c->gemm);
   cudaError_t e = c->block ? cudaFree(c->block) : cudaSuccess;
@@ -501,6 +503,8 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->join, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->prepared, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->gjoin, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->routed, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->flagged, cudaEventDisableTiming);
   for (int q = 0; q < oes_slot_cache::kMaxQueries && e == cudaSuccess; ++q) {
     e = cudaEventCreateWithFlags(&c->ensured[q], cudaEventDisableTiming);
     for (int p = 0; p < 2 && e == cudaSuccess; ++p)
