@@ -411,24 +411,25 @@ int moe_layer_workspace_views(const oes_layer_desc *layer, int T, int k, void *w
  * (FreeToken PR #676, Solution): route (or gate logits + route) -> distinct
  * experts -> the queries of OES_QUERY_MAX distinct experts, each ensured
  * (record_stats as given) in order -> align -> grouped GEMM over `pool`
- * through the layer's remap: the experts that were hits run at once on the
- * cache's side stream while each query's misses are copied, in query order,
- * on `stream`; the copied experts run after their copies.  A query of more
+ * through the layer's remap -> combine.  The number of queries is
+ * ceil(min(T*k, E) / OES_QUERY_MAX), known on the host.
+ * Schedule: each query's misses are copied on `stream`, in query order,
+ * after that query's ensure.  The cache's side stream runs the later
+ * ensures, the expert groups and then the GEMM over the experts that were
+ * hits; a second side stream runs the align (right after routing) and the
+ * GEMM over each query's copied experts once they are in.  A query of more
  * than 32 ids copies its misses in two launches (the last min(n/2, 16) of
- * its n misses second), and the GEMM over each part's experts starts when
- * that part is in (on a second side stream of the cache, beside the GEMM
- * over the hits), so after the last copy at most 16 experts' GEMM remains.
- * The number of queries is ceil(min(T*k, E) / OES_QUERY_MAX), known on the
- * host.  All
- * ensures go before the copies: ensure reads no pool bytes, and with the
- * chunk fitting the pool no query evicts a slot an earlier query touched,
- * so the tables, the slots written and the bytes are those of ensuring and
+ * its n misses second), each part with its own GEMM, so that after the last
+ * copy at most 16 experts' GEMM remains.  The later ensures may run before
+ * earlier copies finish: ensure reads no pool bytes, and with the chunk
+ * fitting the pool no query evicts a slot an earlier query touched, so the
+ * tables, the slots written and the bytes are those of ensuring and
  * copying query by query.
  * The pool must hold every expert the chunk needs at once (the author's
  * reply on FreeToken PR #676): with min(T*k, E) > S this returns
  * OES_ERR_CAPACITY and launches nothing; the caller streams the layer.
  * The call makes no host synchronisation and no allocation, and its side
- * stream forks from and joins `stream` through events.  So a decode step
+ * streams fork from and join `stream` through events.  So a decode step
  * (record_stats = 1) can be captured from `stream` into a CUDA graph and
  * replayed on new tokens written into the same x / logits buffers.  The
  * first call with a given shape sets one-time kernel attributes, so run it
