@@ -46,6 +46,24 @@ def test_topk_ties_and_wide_experts():
         np.testing.assert_allclose(w, ow, rtol=2e-6, atol=1e-7)
 
 
+def test_topk_signed_zeros_infinities_and_k16():
+    """The per-logit ordering the kernel keys on: -0 ties with +0 (lower id
+    first), -inf ranks below every finite logit and gets weight 0; and k = 16,
+    the largest k of the candidate-filter path, on 512 and 33 experts."""
+    lib()
+    g = np.random.default_rng(12)
+    for E, k in [(512, 10), (512, 16), (33, 16), (33, 3)]:
+        vals = np.array([-np.inf, -0.0, 0.0, -1.0, 0.5, 2.0], dtype=np.float32)
+        logits = vals[g.integers(0, len(vals), size=(40, E))]
+        logits[::3] = g.standard_normal((logits[::3].shape[0], E)).astype(np.float32)
+        logits[1] = -np.inf                      # fewer finite logits than k: -inf ones
+        logits[1, g.choice(E, 2, replace=False)] = [1.0, -0.0]   # are taken in id order
+        ids, w = gpu_route(logits, k)
+        oids, ow = route_topk(logits, k)
+        assert np.array_equal(ids, oids), (E, k)
+        np.testing.assert_allclose(w, ow, rtol=2e-6, atol=1e-7)
+
+
 def test_gate_logits_tiny_workload():
     """The tiny workload's router: bf16 gate, fp32 sums; the top-2 decision
     is compared where its margin exceeds the fp32 rounding of the sums."""
