@@ -339,7 +339,7 @@ __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 template <int MODE, int WF>
 __global__ void __launch_bounds__(gemm_threads(WF), 1)
     grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
-  pdl_begin();
+  pdl_wait();
   // a filtered launch over a group with no experts has nothing to do
   if (p.filter && p.gcount && p.gcount[p.filter] == 0) return;
   constexpr int kA = (MODE == 1) ? 2 : 1;  // weight tiles per stage (gate + up, or w2)
@@ -703,7 +703,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
 template <int MODE, int WF>
 __global__ void __maxnreg__(64)
     grouped_gemm_tm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
-  pdl_begin();
+  pdl_wait();
   // a filtered launch over a group with no experts has nothing to do
   if (p.filter && p.gcount && p.gcount[p.filter] == 0) return;
   constexpr int kN = 256;                  // weight rows per tile
@@ -1045,7 +1045,7 @@ __global__ void __maxnreg__(64)
 // f16 copy of x for the NVFP4 path (its MMAs run on f16 operands).
 __global__ void x_to_f16_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ x16,
                                 int64_t n) {
-  pdl_begin();
+  pdl_wait();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
     const float f = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
@@ -1090,7 +1090,7 @@ __global__ void act_scale_kernel(const float* __restrict__ in13, const float* __
 // W4A4: x [T, H] bf16 -> x16 [T, H] f16 holding q * sf per block of 16 along H.
 __global__ void x_quant_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ x16,
                                int64_t nblk, const float* __restrict__ act) {
-  pdl_begin();
+  pdl_wait();
   const float a = act[0];
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nblk;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -1116,7 +1116,7 @@ constexpr int kCombineBatch = 8;
 __global__ void combine_kernel(const uint16_t* __restrict__ y, const float* __restrict__ w,
                                const int32_t* __restrict__ ids, int T, int k, int H, int E,
                                uint16_t* __restrict__ out) {
-  pdl_begin();
+  pdl_wait();
   const int vec = H / 8;
   const int64_t n = (int64_t)T * vec;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;

@@ -500,6 +500,7 @@ extern "C" int moe_layers_forward_staged(const oes_stage_plan* p, const oes_expe
     int rc = check_chunk(d, &chunks[i]);
     if (rc) return rc;
   }
+  const PlainLaunches plain;  // no programmatic launches in the staged sequence
   const int E = p->E;
   const int64_t rb = src->row_bytes;
   uint8_t* base = static_cast<uint8_t*>(pool);

@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(kCopyThreads)
                        uint8_t* __restrict__ pool, int S, const int32_t* __restrict__ miss,
                        const int32_t* __restrict__ n_miss_p, int max_misses, int part,
                        int32_t* __restrict__ status) {
-  pdl_begin();
+  pdl_wait();
   const int nm = min(*n_miss_p, max_misses);
   // part 0 / 1: the misses before / from miss_split(nm); -1: all of them
   const int i0 = part == 1 ? miss_split(nm) : 0, i1 = part == 0 ? miss_split(nm) : nm;
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kCopyThreads)
 __global__ void __launch_bounds__(kCopyThreads)
     copy_runs_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
                      const CopyRun* __restrict__ runs, int nruns, CopyRun one, int64_t nitems) {
-  pdl_begin();
+  pdl_wait();
   const int64_t chunk = (int64_t)kCopyThreads * kCopyUnroll;  // 16-byte vectors per item
   for (int64_t it = blockIdx.x; it < nitems; it += gridDim.x) {
     CopyRun r = one;
