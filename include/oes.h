@@ -331,10 +331,9 @@ typedef struct {
 /* Tile plan (FreeToken PR #676, Solution: nvfp4_moe.prefill_config sizes
  * the tiles by routes per expert of the layer, never per slot): the block
  * size B shared by moe_align_block_size and the GEMM, a function of R and
- * the layer's E only: 16 when ceil(R / E) <= 2 and 32 when it is <= 8
- * (the weight-major kernel, 128 weight rows x the block's routes rounded up
- * to 16 per MMA), else 128 (the token-major kernel, 128 routes x 256 weight
- * rows per MMA). */
+ * the layer's E only: 16 when ceil(R / E) <= 8 (the weight-major kernel,
+ * 128 weight rows x 16 routes per MMA), else 128 (the token-major kernel,
+ * 128 routes x 256 weight rows per MMA). */
 int oes_tile_plan(int R, int E, int *block);
 
 /* Workspace bytes of moe_grouped_gemm_slots for T tokens at top-k. */

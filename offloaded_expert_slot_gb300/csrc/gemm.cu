@@ -1285,12 +1285,10 @@ int launch_gemm(const GemmMaps& maps, const GemmParams& p0, int BN, cudaStream_t
 }  // namespace
 
 int tile_plan(int R, int E) {
-  // routes per expert of the LAYER: up to 8, blocks of 16 (up to 2) or 32
-  // routes on the weight-major kernel, so that an expert that skewed routing
-  // gives up to 32 routes is one block and its weights stream once; more,
-  // blocks of 128 routes on the token-major one
+  // routes per expert of the LAYER: up to 8, blocks of 16 routes on the
+  // weight-major kernel; more, blocks of 128 routes on the token-major one
   const int per = (R + E - 1) / std::max(E, 1);
-  return per <= 2 ? 16 : (per <= 8 ? 32 : 128);
+  return per <= 8 ? 16 : 128;
 }
 
 }  // namespace oes

@@ -56,15 +56,14 @@ def test_tile_plan_uses_the_layers_expert_count(lib):
     of the layer, never of the slot pool.  At 600 tokens x
     top-10 the layer's 512 experts get 11.7 routes each (blocks of 128 routes,
     token-major kernel); sizing by the 1100 slots would give 5.5 (blocks of
-    32, weight-major kernel).  Up to 2 routes per expert: blocks of 16."""
+    16, weight-major kernel)."""
     assert oes.oes_tile_plan(600 * 10, 512) == 128
-    assert oes.oes_tile_plan(600 * 10, 1100) == 32
+    assert oes.oes_tile_plan(600 * 10, 1100) == 16
     assert oes.oes_tile_plan(4096 * 10, 512) == 128
     assert oes.oes_tile_plan(32 * 10, 512) == 16
-    assert oes.oes_tile_plan(200 * 10, 512) == 32
-    assert oes.oes_tile_plan(16 * 2, 8) == 32
-    for R, E, want in [(2 * 512, 512, 16), (2 * 512 + 1, 512, 32), (8 * 512, 512, 32),
-                       (8 * 512 + 1, 512, 128), (0, 5, 16)]:
+    assert oes.oes_tile_plan(200 * 10, 512) == 16
+    assert oes.oes_tile_plan(16 * 2, 8) == 16
+    for R, E, want in [(8 * 512, 512, 16), (8 * 512 + 1, 512, 128), (0, 5, 16)]:
         assert oes.oes_tile_plan(R, E) == want
 
 

@@ -200,7 +200,7 @@ def test_wide_layer(wfmt, T):
     oes.moe_layer_forward_slots(w.cache, w.src, w.pool, 0, r.desc, r.chunk, 0)
     torch.cuda.synchronize()
     assert int(r.status.item()) == 0
-    assert oes.oes_tile_plan(T * 2, 4) == (128 if T == 24 else 32)
+    assert oes.oes_tile_plan(T * 2, 4) == (128 if T == 24 else 16)
     o, _oc = oracle_slots(w)
     got = r.out.to(torch.float64).cpu().numpy()
     want = o["out"]

@@ -28,7 +28,7 @@ MEDIUM_BF16 = scaled(C2, name="medium_bf16", T=96, k=4, E=16, H=256, I=192, S=40
 MEDIUM_NVFP4 = scaled(C4, name="medium_nvfp4", T=96, k=4, E=16, H=256, I=192, S=40, L=2, prefill=20)
 WIDE_BLOCKS = scaled(C2, name="wide_blocks_bf16", T=160, k=8, E=12, H=128, I=128, S=30, L=2,
                      prefill=10)
-# few routes per expert: blocks of 32 on the weight-major kernel, ragged I
+# few routes per expert: blocks of 16 on the weight-major kernel, ragged I
 MEDIUM_SWAP_BF16 = scaled(C2, name="medium_swap_bf16", T=40, k=3, E=16, H=256, I=192, S=40, L=2,
                           prefill=20)
 MEDIUM_SWAP_NVFP4 = scaled(C4, name="medium_swap_nvfp4", T=40, k=3, E=16, H=256, I=192, S=40,
@@ -159,7 +159,7 @@ def test_medium_layers_match_oracle_and_stream(cfg):
     (token-major for many routes per expert, weight-major for few)."""
     lib()
     R = cfg.T * cfg.k
-    assert oes.oes_tile_plan(R, cfg.E) == (32 if "swap" in cfg.name else 128)
+    assert oes.oes_tile_plan(R, cfg.E) == (16 if "swap" in cfg.name else 128)
     w = Workload(cfg, gen_device="cpu")
     full_check(w)
     w.close()

@@ -58,7 +58,7 @@ def test_w4a4_gemm_steps(cfg):
     ids, wts = i32(R), torch.empty(R, dtype=torch.float32, device="cuda")
     oes.moe_route_topk(w.logits, T, E, k, ids, wts)
     B = oes.oes_tile_plan(R, E)
-    assert B == (128 if cfg is W4A4_TM else 32)
+    assert B == (128 if cfg is W4A4_TM else 16)
     cap = oes.align_capacity(R, E, B)
     srt, be, npp, st = i32(cap), i32(cap // B), i32(1), status()
     awsb = oes.moe_align_workspace_size(R, E, B)
