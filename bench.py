@@ -43,11 +43,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture of the current kernels, of the launches the breakdown times
 # (`python bench.py --breakdown --steps 2`, profiles/launch_list_c2_decode_width.md):
 # per whole-query copy_misses_kernel launch (three a step, the third query
-# empty) 0.2 MB read + 123.7 MB written; per step the grouped GEMM (GEMM1,
-# GEMM2, combine) 2342.6 MB.  Valid only for that workload and these kernels.
+# empty) 0.1 MB read + 123.7 MB written; per step the grouped GEMM (GEMM1,
+# GEMM2, combine) 2342.5 MB.  Valid only for that workload and these kernels.
 TRAFFIC_WORKLOAD = "c2_decode_width"
-COPY_TRAFFIC_PER_LAUNCH = 123.93e6
-GEMM_TRAFFIC_PER_STEP = 2342.6e6
+COPY_TRAFFIC_PER_LAUNCH = 123.77e6
+GEMM_TRAFFIC_PER_STEP = 2342.5e6
 
 
 def peaks():
