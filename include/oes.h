@@ -140,7 +140,12 @@ int moe_distinct_experts(const int32_t *ids, int R, int E, int32_t *distinct, in
  * slot_key [S] (key of each slot or -1), slot_ts [S] (timestamp of the query
  * that last touched the slot; 0 = empty), a clock (last timestamp handed
  * out), counters hits / misses / evictions and decode_freq [L*E].
- * The slot pool itself (S rows of expert bytes) belongs to the caller. */
+ * The slot pool itself (S rows of expert bytes) belongs to the caller.
+ * A handle also owns the two side streams and the events of
+ * moe_layer_forward_slots.  Calls on one handle are ordered by the caller:
+ * they must not overlap in time from different host threads, and their
+ * device work follows the order of the streams they are given (the tables
+ * are one state).  Different handles are independent. */
 typedef struct oes_slot_cache oes_slot_cache;
 
 /* Allocates the tables (cudaMalloc, synchronous) on the current device and
