@@ -125,7 +125,8 @@ def oracle_sample(cfg, rin, source_row, prefill, n_tokens, seed):
     cache = SlotCache.from_state(cfg.S, cfg.L, cfg.E, prefill["slot_key"], prefill["slot_ts"],
                                  prefill["clock"])
     toks = np.random.default_rng(seed).choice(cfg.T, n_tokens, replace=False)
-    block = 16 if cfg.T * cfg.k <= 16 * cfg.E else 128
+    per = -(-(cfg.T * cfg.k) // cfg.E)           # the library's tile plan: routes per expert
+    block = 16 if per <= 8 else 128
     t0 = time.perf_counter()
     forward_slots(cfg, rin, source_row, cache, pool, block=block, tokens=toks)
     return time.perf_counter() - t0
@@ -149,11 +150,11 @@ def lazy_source(cfg, needed):
 def reference_arm(args, cfg):
     """The CPU oracle as the reference implementation, on the host cores."""
     from offloaded_expert_slot_gb300.inputs import pool_prefill, router_inputs
-    from oracle.distinct import distinct_experts
-    from oracle.router import route_topk
+    from oracle.router import gate_logits, route_topk
     rin = router_inputs(cfg)
     prefill = pool_prefill(cfg)
-    ids, _ = route_topk(rin["logits"], cfg.k)
+    logits = rin["logits"] if rin["logits"] is not None else gate_logits(rin["x"], rin["gate"])
+    ids, _ = route_topk(logits, cfg.k)
     n_tok = min(cfg.T, 8)
     needed = {(cfg.layer, int(e)) for e in np.unique(ids)}
     src = lazy_source(cfg, needed)
