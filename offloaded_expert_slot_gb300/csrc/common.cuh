@@ -182,9 +182,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
 __device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
 // The mbarrier gets one arrival (counted in its expected arrivals) once every
 // cp.async this thread issued before has completed; the thread does not wait.
 __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
