@@ -152,6 +152,9 @@ typedef struct oes_slot_cache oes_slot_cache;
  * sets every slot empty.  1 <= S <= OES_MAX_SLOTS, 1 <= E <= OES_MAX_EXPERTS,
  * L >= 1, L * E < 2^31. */
 int slot_cache_create(int S, int L, int E, oes_slot_cache **out);
+/* Waits for the handle's two side streams, then frees its tables, streams and
+ * events.  Work the caller queued on its own streams that uses the handle must
+ * have finished (or be synchronised) first.  A null handle is a no-op. */
 int slot_cache_destroy(oes_slot_cache *cache);
 
 /* Replaces the state: slot_key / slot_ts host [S] (slot_ts 0 for an empty

@@ -32,7 +32,7 @@ struct oes_slot_cache {
   cudaStream_t side = nullptr, gemm = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr, prepared = nullptr, gjoin = nullptr;
   cudaEvent_t routed = nullptr, flagged = nullptr;
-  cudaEvent_t ensured[kMaxQueries], copied[2 * kMaxQueries];
+  cudaEvent_t ensured[kMaxQueries] = {}, copied[2 * kMaxQueries] = {};
 };
 
 struct oes_expert_source {

@@ -491,10 +491,6 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   const size_t bytes = (LE * 4 + (size_t)S * 4 + (size_t)S * 8 + 8 * 8 + LE * 8 + (size_t)S * 8 +
                         (size_t)S * 4 + 64 + 15) / 16 * 16;
   c->block_bytes = bytes;
-  c->side = nullptr;
-  c->fork = c->join = nullptr;
-  for (int q = 0; q < oes_slot_cache::kMaxQueries; ++q)
-    c->ensured[q] = c->copied[2 * q] = c->copied[2 * q + 1] = nullptr;
   c->block = nullptr;
   cudaError_t e = cudaMalloc(&c->block, bytes);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking);
@@ -543,7 +539,9 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
 
 extern "C" int slot_cache_destroy(oes_slot_cache* c) {
   if (!c) return OES_OK;
+  // the handle's own streams may still run kernels that read the tables
   if (c->side) cudaStreamSynchronize(c->side);
+  if (c->gemm) cudaStreamSynchronize(c->gemm);
   return release_cache(c);
 }
 
