@@ -79,3 +79,55 @@ def test_demand_token_dispatch_rule(lib):
     from conftest import GOLDEN
     for c in json.load(open(os.path.join(GOLDEN, "demand_dispatch.json")))["cases"]:
         assert oes.oes_takes_slot_path(c["T"], c["k"], c["E"], c["S"], c["N"]) == c["slots"], c
+
+
+def test_null_handles_destroy_as_no_ops(lib):
+    oes.slot_cache_destroy(None)
+    oes.oes_expert_source_destroy(None)
+    oes.oes_stage_plan_destroy(None)
+
+
+def _invalid(fn, *args, **kw):
+    with pytest.raises(oes.OesError) as e:
+        fn(*args, **kw)
+    assert e.value.code == oes.OES_ERR_INVALID_ARG, e.value
+    return str(e.value)
+
+
+def test_handle_and_layer_argument_checks(lib):
+    """Checks that the library takes on the host, before any device work: the
+    addresses below are never dereferenced."""
+    A = 1 << 20                                    # a fake, 256-byte aligned address
+    # slot cache: L * E must stay below 2^31, E within OES_MAX_EXPERTS
+    _invalid(oes.slot_cache_create, 16, 1 << 20, 4096)
+    _invalid(oes.slot_cache_create, 16, 1, oes.OES_MAX_EXPERTS + 1)
+    _invalid(oes.slot_cache_create, 16, 0, 8)
+    # expert source: row size a positive multiple of 16, bases non-null and aligned
+    _invalid(oes.oes_expert_source_create, [A, A], 8, 24)
+    _invalid(oes.oes_expert_source_create, [A, A], 8, 0)
+    msg = _invalid(oes.oes_expert_source_create, [A, A + 8], 8, 64)
+    assert "layer 1" in msg
+    _invalid(oes.oes_expert_source_create, [A, 0], 8, 64)
+    # stage plan and its per-layer query need a plan
+    _invalid(oes.oes_stage_plan_create, None, [0], 0, stream=0)
+    _invalid(oes.oes_stage_plan_layer, None, 0, 8)
+    # a whole-layer chunk is validated before the cache, source or pool
+    desc = oes.layer_desc(8, 64, 32, oes.OES_WFMT_BF16)
+    need = oes.moe_layer_workspace_size(desc, 4, 2)
+    assert need > 0 and need % 256 == 0
+    ok = dict(x=A, T=4, k=2, out=A, status=A, workspace=A, workspace_bytes=need, logits=A)
+    for bad in [dict(workspace_bytes=need - 1), dict(workspace=A + 16), dict(k=9), dict(k=0),
+                dict(T=-1), dict(x=None), dict(logits=None), dict(out=None)]:
+        ch = oes.chunk(**{**ok, **bad})
+        msg = _invalid(oes.moe_layer_forward_slots, A, A, A, 0, desc, ch, False, stream=0)
+        assert "layer forward" in msg, bad
+        _invalid(oes.moe_layer_forward_stream, A, A, 0, desc, ch, copy_stream=0,
+                 compute_stream=0)
+    ch = oes.chunk(**ok)
+    msg = _invalid(oes.moe_layer_forward_slots, None, A, A, 0, desc, ch, False, stream=0)
+    assert "moe_layer_forward_slots" in msg
+    msg = _invalid(oes.moe_layer_forward_stream, None, A, 0, desc, ch, copy_stream=0,
+                   compute_stream=0)
+    assert "moe_layer_forward_stream" in msg
+    _invalid(oes.moe_layers_forward_staged, None, A, A, desc, [ch], copy_stream=0,
+             compute_stream=0)
