@@ -114,15 +114,20 @@ const char *oes_last_error(void);
 int moe_gate_logits(const uint16_t *x, const uint16_t *gate, int T, int H, int E, float *logits,
                     oes_stream_t stream);
 
+/* Router logit types of moe_route_topk. */
+enum { OES_LOGITS_F32 = 0, OES_LOGITS_BF16 = 1 };
+
 /* Top-k routing (FreeToken PR #676, Problem and Solution: each token routes
  * to k experts; the workloads fix softmax-renormalised top-k).  For each
  * token t: ids[t, 0..k-1] = the k largest logits[t, :] in descending order,
  * ties to the lower expert id; weights[t, j] = softmax over the k selected
  * logits (equal to the full softmax renormalised over the top k).
- * logits: device [T, E] fp32, finite; ids: device [T, k] int32; weights:
- * device [T, k] fp32.  1 <= k <= min(E, OES_MAX_TOPK), E <= OES_MAX_EXPERTS. */
-int moe_route_topk(const float *logits, int T, int E, int k, int32_t *ids, float *weights,
-                   oes_stream_t stream);
+ * logits: device [T, E] of `dtype` (OES_LOGITS_F32, or OES_LOGITS_BF16 as
+ * uint16_t bit patterns, widened exactly to fp32 before any comparison), not
+ * NaN (-inf is allowed); ids: device [T, k] int32; weights: device [T, k]
+ * fp32.  1 <= k <= min(E, OES_MAX_TOPK), E <= OES_MAX_EXPERTS. */
+int moe_route_topk(const void *logits, int dtype, int T, int E, int k, int32_t *ids,
+                   float *weights, oes_stream_t stream);
 
 /* The chunk's distinct experts as a sorted list of fixed length (FreeToken
  * PR #676, Solution: the list's length does not depend on the routing, so
@@ -162,6 +167,13 @@ int slot_cache_destroy(oes_slot_cache *cache);
  * 2^47; rebuilds map, zeroes the counters.  Synchronous. */
 int slot_cache_load_state(oes_slot_cache *cache, const int32_t *slot_key, const int64_t *slot_ts,
                           int64_t clock);
+
+/* Puts the handle back in the state slot_cache_create leaves: every slot
+ * empty, clock 0, counters, decode frequencies, LRFU scores, pins and the
+ * chunk tag counter zero.  The policy stays as set.  Three memsets on
+ * `stream`, ordered after the handle's earlier calls on it; no host
+ * synchronisation, so a graph may capture it. */
+int slot_cache_reset(oes_slot_cache *cache, oes_stream_t stream);
 
 /* Copies the state to host arrays (any may be NULL): map [L*E], slot_key
  * [S], slot_ts [S], clock [1], counters [3] = hits, misses, evictions,

@@ -152,7 +152,7 @@ int route(const oes_layer_desc* d, const oes_chunk* c, const LayerWs& w, cudaStr
     if (rc) return rc;
     logits = w.logits;
   }
-  return moe_route_topk(logits, c->T, d->E, c->k, w.ids, w.w, s);
+  return moe_route_topk(logits, OES_LOGITS_F32, c->T, d->E, c->k, w.ids, w.w, s);
 }
 
 }  // namespace

@@ -28,22 +28,25 @@ __global__ void gate_logits_kernel(const uint16_t* __restrict__ x, const uint16_
   }
 }
 
-// One warp per token.  Lane l holds logits l, l+32, ...; k rounds of a
-// warp-wide arg-max (larger value first, ties to the lower id); a selected
-// entry is replaced by NaN, which loses every comparison.
-template <int EPL>
-__global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+__device__ __forceinline__ float load_logit(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float load_logit(const uint16_t* p) { return bf16_to_f32(__ldg(p)); }
+
+// One warp per token.  Lane l holds logits l, l+32, ... widened to fp32 (bf16
+// exactly); k rounds of a warp-wide arg-max (larger value first, ties to the
+// lower id); a selected entry is replaced by NaN, which loses every comparison.
+template <int EPL, typename LT>
+__global__ void topk_kernel(const LT* __restrict__ logits, int T, int E, int k,
                             int32_t* __restrict__ ids, float* __restrict__ weights) {
   pdl_begin();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
-    const float* row = logits + (size_t)t * E;
+    const LT* row = logits + (size_t)t * E;
     float v[EPL];
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {
       const int e = lane + 32 * j;
-      v[j] = (e < E) ? __ldg(row + e) : -INFINITY;
+      v[j] = (e < E) ? load_logit(row + e) : -INFINITY;
     }
     float my_v = 0.f;  // lane j keeps round j's winner
     int my_e = 0;
@@ -154,16 +157,15 @@ extern "C" int moe_gate_logits(const uint16_t* x, const uint16_t* gate, int T, i
   return OES_OK;
 }
 
-extern "C" int moe_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* weights,
-                              oes_stream_t stream) {
-  OES_REQUIRE(logits && ids && weights, "moe_route_topk: null pointer");
-  OES_REQUIRE(T >= 0 && E >= 1 && E <= OES_MAX_EXPERTS, "moe_route_topk: bad T=%d E=%d", T, E);
-  OES_REQUIRE(k >= 1 && k <= E && k <= OES_MAX_TOPK, "moe_route_topk: bad k=%d (E=%d)", k, E);
-  if (T == 0) return OES_OK;
+namespace {
+template <typename LT>
+void launch_topk(const LT* logits, int T, int E, int k, int32_t* ids, float* weights,
+                 cudaStream_t stream) {
   const int threads = 128;
   const int blocks = (int)std::min<int64_t>(ceil_div64((int64_t)T * 32, threads), (int64_t)num_sms() * 16);
   const int epl = ceil_div(E, 32);
-#define OES_TOPK(N) launch_kernel(topk_kernel<N>, blocks, threads, 0, stream, logits, T, E, k, ids, weights)
+#define OES_TOPK(N) \
+  launch_kernel(topk_kernel<N, LT>, blocks, threads, 0, stream, logits, T, E, k, ids, weights)
   if (epl <= 1) OES_TOPK(1);
   else if (epl <= 2) OES_TOPK(2);
   else if (epl <= 4) OES_TOPK(4);
@@ -173,6 +175,21 @@ extern "C" int moe_route_topk(const float* logits, int T, int E, int k, int32_t*
   else if (epl <= 64) OES_TOPK(64);
   else OES_TOPK(128);
 #undef OES_TOPK
+}
+}  // namespace
+
+extern "C" int moe_route_topk(const void* logits, int dtype, int T, int E, int k, int32_t* ids,
+                              float* weights, oes_stream_t stream) {
+  OES_REQUIRE(logits && ids && weights, "moe_route_topk: null pointer");
+  OES_REQUIRE(dtype == OES_LOGITS_F32 || dtype == OES_LOGITS_BF16,
+              "moe_route_topk: unknown logits type %d", dtype);
+  OES_REQUIRE(T >= 0 && E >= 1 && E <= OES_MAX_EXPERTS, "moe_route_topk: bad T=%d E=%d", T, E);
+  OES_REQUIRE(k >= 1 && k <= E && k <= OES_MAX_TOPK, "moe_route_topk: bad k=%d (E=%d)", k, E);
+  if (T == 0) return OES_OK;
+  if (dtype == OES_LOGITS_F32)
+    launch_topk(static_cast<const float*>(logits), T, E, k, ids, weights, stream);
+  else
+    launch_topk(static_cast<const uint16_t*>(logits), T, E, k, ids, weights, stream);
   OES_CHECK_LAUNCH("topk_kernel");
   return OES_OK;
 }

@@ -493,6 +493,7 @@ extern "C" int slot_cache_create(int S, int L, int E, oes_slot_cache** out) {
   c->block_bytes = bytes;
   c->block = nullptr;
   cudaError_t e = cudaMalloc(&c->block, bytes);
+  if (e == cudaSuccess) e = cudaMemset(c->block, 0, bytes);  // slack bytes included
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->gemm, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->fork, cudaEventDisableTiming);
@@ -573,6 +574,20 @@ extern "C" int slot_cache_load_state(oes_slot_cache* c, const int32_t* slot_key,
   OES_TRY_CUDA(cudaMemcpy(c->ctr, ctr, sizeof(ctr), cudaMemcpyHostToDevice));
   OES_TRY_CUDA(cudaMemset(c->decode_freq, 0, LE * 8));
   return reset_lrfu(c, slot_key);
+}
+
+extern "C" int slot_cache_reset(oes_slot_cache* c, oes_stream_t stream) {
+  OES_REQUIRE(c, "slot_cache_reset: null cache");
+  const int64_t LE = (int64_t)c->L * c->E;
+  uint8_t* base = static_cast<uint8_t*>(c->block);
+  uint8_t* map = reinterpret_cast<uint8_t*>(c->map);
+  uint8_t* pin = reinterpret_cast<uint8_t*>(c->pin);
+  // slot_ts, counters, decode_freq and LRFU scores precede the map; map and
+  // slot_key are adjacent and become -1; the pins and the block's slack zero
+  OES_TRY_CUDA(cudaMemsetAsync(base, 0, (size_t)(map - base), stream));
+  OES_TRY_CUDA(cudaMemsetAsync(map, 0xff, (size_t)(LE + c->S) * 4, stream));
+  OES_TRY_CUDA(cudaMemsetAsync(pin, 0, c->block_bytes - (size_t)(pin - base), stream));
+  return OES_OK;
 }
 
 extern "C" int slot_cache_set_policy(oes_slot_cache* c, int policy, int lrfu_k) {

@@ -23,6 +23,7 @@ from . import build as _build
 OES_OK, OES_ERR_INVALID_ARG, OES_ERR_UNSUPPORTED, OES_ERR_CUDA, OES_ERR_CAPACITY = range(5)
 OES_DEV_CAPACITY, OES_DEV_BAD_ID, OES_DEV_TIMEOUT = 1, 2, 4
 OES_WFMT_BF16, OES_WFMT_NVFP4, OES_WFMT_NVFP4_W4A4 = 0, 1, 2
+OES_LOGITS_F32, OES_LOGITS_BF16 = 0, 1
 OES_POLICY_LRU, OES_POLICY_LRFU = 0, 1
 OES_LRFU_MAX_K = 18
 OES_QUERY_MAX = 128
@@ -68,10 +69,11 @@ _vp, _i, _i64, _sz = C.c_void_p, C.c_int, C.c_int64, C.c_size_t
 _SIGS = {
     "oes_last_error": (C.c_char_p, []),
     "moe_gate_logits": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
-    "moe_route_topk": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp]),
+    "moe_route_topk": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp]),
     "moe_distinct_experts": (_i, [_vp, _i, _i, _vp, _vp, _vp]),
     "slot_cache_create": (_i, [_i, _i, _i, C.POINTER(_vp)]),
     "slot_cache_destroy": (_i, [_vp]),
+    "slot_cache_reset": (_i, [_vp, _vp]),
     "slot_cache_load_state": (_i, [_vp, _vp, _vp, _i64]),
     "slot_cache_read_state": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "slot_cache_layer_map": (_i, [_vp, _i, C.POINTER(_vp)]),
@@ -171,8 +173,25 @@ def moe_gate_logits(x, gate, T, H, E, logits, stream=None):
     _call("moe_gate_logits", _ptr(x), _ptr(gate), T, H, E, _ptr(logits), _stream(stream))
 
 
-def moe_route_topk(logits, T, E, k, ids, weights, stream=None):
-    _call("moe_route_topk", _ptr(logits), T, E, k, _ptr(ids), _ptr(weights), _stream(stream))
+def _logits_type(logits) -> int:
+    """fp32 arrays are fp32 logits; bf16 arrays and 16-bit integer arrays (bf16
+    bit patterns) are bf16; a raw address is fp32 unless dtype says otherwise."""
+    if logits is None or isinstance(logits, int):
+        return OES_LOGITS_F32
+    name = str(getattr(logits, "dtype", "")).replace("torch.", "")
+    if name == "float32":
+        return OES_LOGITS_F32
+    if name in ("bfloat16", "int16", "uint16"):
+        return OES_LOGITS_BF16
+    raise TypeError(f"moe_route_topk: logits of dtype {name!r}; expected fp32 or bf16 (bit patterns)")
+
+
+def moe_route_topk(logits, T, E, k, ids, weights, stream=None, dtype=None):
+    """dtype: OES_LOGITS_*, or None to take it from the logits array."""
+    if dtype is None:
+        dtype = _logits_type(logits)
+    _call("moe_route_topk", _ptr(logits), dtype, T, E, k, _ptr(ids), _ptr(weights),
+          _stream(stream))
 
 
 def moe_distinct_experts(ids, R, E, distinct, d_count, stream=None):
@@ -188,6 +207,10 @@ def slot_cache_create(S, L, E) -> int:
 
 def slot_cache_destroy(cache):
     _call("slot_cache_destroy", cache)
+
+
+def slot_cache_reset(cache, stream=None):
+    _call("slot_cache_reset", cache, _stream(stream))
 
 
 def slot_cache_load_state(cache, slot_key, slot_ts, clock):

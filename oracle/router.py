@@ -7,7 +7,9 @@ renormalised top-k".  Readings taken where the pages are silent:
     expert id;
   * softmax over all E experts, keep the top k, divide by their sum -- which
     equals a softmax over the k selected logits -- computed in fp64 and
-    stored as fp32.
+    stored as fp32;
+  * bf16 logits are widened to fp32 (exact: bf16 is fp32's upper half) and
+    routed the same way.
 """
 from __future__ import annotations
 
@@ -36,3 +38,8 @@ def route_topk(logits: np.ndarray, k: int):
         ex = np.exp(sel - sel.max())
         w[t] = (ex / ex.sum()).astype(np.float32)
     return ids, w
+
+
+def route_topk_bf16(logit_bits: np.ndarray, k: int):
+    """route_topk on bf16 logits given as uint16 bit patterns [T, E]."""
+    return route_topk(bf16_to_f64(logit_bits).astype(np.float32), k)

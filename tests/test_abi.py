@@ -38,6 +38,9 @@ def test_host_argument_checks(lib):
         oes.moe_route_topk(16, 4, 8, 9, 16, 16, stream=0)     # k > E
     assert e.value.code == oes.OES_ERR_INVALID_ARG
     with pytest.raises(oes.OesError) as e:
+        oes.moe_route_topk(16, 4, 8, 2, 16, 16, stream=0, dtype=7)   # unknown logits type
+    assert e.value.code == oes.OES_ERR_INVALID_ARG
+    with pytest.raises(oes.OesError) as e:
         oes.slot_cache_create(0, 1, 8)
     assert e.value.code == oes.OES_ERR_INVALID_ARG
     with pytest.raises(oes.OesError) as e:
@@ -81,8 +84,25 @@ def test_demand_token_dispatch_rule(lib):
         assert oes.oes_takes_slot_path(c["T"], c["k"], c["E"], c["S"], c["N"]) == c["slots"], c
 
 
+def test_logits_type_follows_the_array():
+    """The binding names the logits type from the array: fp32, or bf16 given as
+    bf16 or as its 16-bit patterns; any other type is refused before a call."""
+    import numpy as np
+    import torch
+    assert oes._logits_type(np.zeros(2, np.float32)) == oes.OES_LOGITS_F32
+    assert oes._logits_type(torch.zeros(2)) == oes.OES_LOGITS_F32
+    for a in (np.zeros(2, np.uint16), torch.zeros(2, dtype=torch.bfloat16),
+              torch.zeros(2, dtype=torch.int16)):
+        assert oes._logits_type(a) == oes.OES_LOGITS_BF16
+    for a in (torch.zeros(2, dtype=torch.float16), np.zeros(2, np.float64)):
+        with pytest.raises(TypeError):
+            oes._logits_type(a)
+
+
 def test_null_handles_destroy_as_no_ops(lib):
     oes.slot_cache_destroy(None)
+    with pytest.raises(oes.OesError):
+        oes.slot_cache_reset(None, stream=0)
     oes.oes_expert_source_destroy(None)
     oes.oes_stage_plan_destroy(None)
 

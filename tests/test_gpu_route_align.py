@@ -11,7 +11,7 @@ from offloaded_expert_slot_gb300.configs import C1, C2, C3, C4, C5, C5B
 from offloaded_expert_slot_gb300.inputs import router_inputs, uniform_routes
 from oracle.align import moe_align_block_size as oracle_align
 from oracle.distinct import distinct_experts
-from oracle.router import gate_logits, route_topk
+from oracle.router import gate_logits, route_topk, route_topk_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -62,6 +62,35 @@ def test_topk_signed_zeros_infinities_and_k16():
         oids, ow = route_topk(logits, k)
         assert np.array_equal(ids, oids), (E, k)
         np.testing.assert_allclose(w, ow, rtol=2e-6, atol=1e-7)
+
+
+def test_topk_bf16_logits():
+    """bf16 logits route as their exact fp32 widening: ids bit-exact against
+    the oracle, weights within its bound, and both identical bit for bit to the
+    fp32 call on the widened values.  Truncated normals give many ties; -inf
+    and -0 are mixed in.  One case passes a torch.bfloat16 tensor."""
+    lib()
+    g = np.random.default_rng(13)
+    for E, k in [(8, 2), (33, 16), (512, 10), (2100, 32), (4096, 8)]:
+        f = g.standard_normal((37, E)).astype(np.float32)
+        bits = (f.view(np.uint32) >> 16).astype(np.uint16)
+        bits[::5, ::7] = 0xff80
+        bits[1::5, ::3] = 0x8000
+        T = bits.shape[0]
+        ids, w = i32(T * k), f32(T * k)
+        dev = bits16(bits)
+        if E == 512:
+            oes.moe_route_topk(dev.view(torch.bfloat16), T, E, k, ids, w)
+        else:
+            oes.moe_route_topk(dev, T, E, k, ids, w, dtype=oes.OES_LOGITS_BF16)
+        torch.cuda.synchronize()
+        gi, gw = ids.cpu().numpy().reshape(T, k), w.cpu().numpy().reshape(T, k)
+        oids, ow = route_topk_bf16(bits, k)
+        assert np.array_equal(gi, oids), (E, k)
+        np.testing.assert_allclose(gw, ow, rtol=2e-6, atol=1e-7)
+        wide = (bits.astype(np.uint32) << 16).view(np.float32)
+        fi, fw = gpu_route(wide, k)
+        assert np.array_equal(gi, fi) and np.array_equal(gw.view(np.uint32), fw.view(np.uint32))
 
 
 def test_gate_logits_tiny_workload():

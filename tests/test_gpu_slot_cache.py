@@ -245,3 +245,55 @@ def test_largest_pool(policy):
         crf, pin = oes.slot_cache_read_lrfu(c.h, S)
         assert [int(v) for v in crf] == o.crf
     c.close()
+
+
+@pytest.mark.parametrize("policy", ["lru", "lrfu"])
+def test_reset_returns_the_created_state(policy):
+    """slot_cache_reset, queued on the stream after queries that were not
+    waited for, leaves every table byte as slot_cache_create does (the
+    snapshot of a fresh handle with the same policy); the policy stays, and
+    queries after it follow the oracle from an empty cache."""
+    g = np.random.default_rng(910 + (policy == "lrfu"))
+    S, L, E = 40, 2, 64
+    c = GpuCache(S, L, E)
+    fresh = oes.slot_cache_create(S, L, E)
+    if policy == "lrfu":
+        oes.slot_cache_set_policy(c.h, oes.OES_POLICY_LRFU, 3)
+        oes.slot_cache_set_policy(fresh, oes.OES_POLICY_LRFU, 3)
+
+    def queries(n):
+        out = []
+        for _ in range(n):
+            w = int(g.integers(0, S + 1))
+            out.append((int(g.integers(0, L)), sorted(g.choice(E, size=w, replace=False).tolist()),
+                        bool(g.random() < 0.5)))
+        return out
+
+    keep = []
+    for layer, q, rs in queries(6):                         # queued, not waited for
+        dev = cuda(np.asarray(q, dtype=np.int32)) if q else 0
+        keep.append(dev)
+        oes.slot_cache_ensure(c.h, layer, dev, len(q), rs, c.miss, c.n_miss, c.status)
+    oes.slot_cache_reset(c.h)
+    nb = oes.slot_cache_state_bytes(c.h)
+    a = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    b = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    oes.slot_cache_snapshot(c.h, a)
+    oes.slot_cache_snapshot(fresh, b)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    st = c.state()
+    assert (st["map"] == -1).all() and (st["slot_key"] == -1).all() and st["clock"] == 0
+    o = SlotCache(S, L, E)
+    if policy == "lrfu":
+        o.set_policy("lrfu", 3)
+    for layer, q, rs in queries(12):
+        s_, m = c.ensure(layer, q, record_stats=rs)
+        os_, om = o.ensure([layer * E + e for e in q], record_stats=rs)
+        assert s_ == STATUS[os_] and m == [tuple(x) for x in om]
+    assert_same(c, o)
+    if policy == "lrfu":
+        crf, pin = oes.slot_cache_read_lrfu(c.h, S)
+        assert [int(v) for v in crf] == o.crf and [int(v) for v in pin] == o.pin
+    oes.slot_cache_destroy(fresh)
+    c.close()

@@ -10,7 +10,7 @@ import pytest
 from conftest import GOLDEN
 from oracle.distinct import distinct_experts
 from oracle.numerics import bf16_to_f64
-from oracle.router import gate_logits, route_topk
+from oracle.router import gate_logits, route_topk, route_topk_bf16
 
 
 def test_router_hand_cases():
@@ -19,6 +19,22 @@ def test_router_hand_cases():
         ids, w = route_topk(np.array([c["logits"]], dtype=np.float32), c["k"])
         assert ids[0].tolist() == c["ids"]
         np.testing.assert_allclose(w[0], c["w"], rtol=1e-7, atol=0)
+
+
+def test_router_bf16_logits_hand_case():
+    """bf16 bit patterns with known values: 0x4000 = 2, 0x3f80 = 1, 0x3fc0 =
+    1.5, 0x0000 = +0, 0x8000 = -0, 0xbf80 = -1, 0xc000 = -2, 0xff80 = -inf.
+    Ordering by the raw (signed or unsigned) bits would put the negatives in
+    the wrong place; -0 ties with +0 and the lower id wins."""
+    bits = np.array([[0xbf80, 0x8000, 0x4000, 0x0000, 0xff80, 0x3fc0, 0xc000, 0x3f80]],
+                    dtype=np.uint16)
+    ids, w = route_topk_bf16(bits, 6)
+    assert ids[0].tolist() == [2, 5, 7, 1, 3, 0]
+    v = np.array([2.0, 1.5, 1.0, 0.0, 0.0, -1.0])
+    want = np.exp(v - 2.0) / np.exp(v - 2.0).sum()
+    np.testing.assert_allclose(w[0], want, rtol=1e-7, atol=0)
+    ids, w = route_topk_bf16(bits, 8)
+    assert ids[0].tolist() == [2, 5, 7, 1, 3, 0, 6, 4] and w[0, 7] == 0.0
 
 
 @pytest.mark.parametrize("seed", range(20))
