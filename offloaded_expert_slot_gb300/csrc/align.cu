@@ -19,6 +19,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "internal.h"
 
 namespace oes {
 namespace {
@@ -55,11 +56,13 @@ __global__ void __launch_bounds__(kAlignThreads)
 }
 
 __global__ void __launch_bounds__(1024)
-    align_scan_kernel(int G, int E, int B, AlignWs ws, int32_t* __restrict__ n_post_pad) {
+    align_scan_kernel(int G, int E, int B, AlignWs ws, int32_t* __restrict__ n_post_pad,
+                      int32_t* __restrict__ zero, int nzero) {
   pdl_begin();
   extern __shared__ int32_t padded[];  // [E]
   __shared__ int warp_tot[32];
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, w = tid >> 5;
+  for (int i = tid; i < nzero; i += nt) zero[i] = 0;
   // column totals: the loads of a batch are issued together (one round
   // trip per kScanBatch CTAs instead of one per CTA)
   for (int e = tid; e < E; e += nt) {
@@ -210,8 +213,9 @@ __global__ void __launch_bounds__(1024)
     align_small_kernel(const int32_t* __restrict__ ids, int R, int E, int B, int64_t cap,
                        int ignore_invalid, int32_t* __restrict__ sorted_ids,
                        int32_t* __restrict__ block_expert, int32_t* __restrict__ n_post_pad,
-                       int32_t* __restrict__ status) {
+                       int32_t* __restrict__ status, int32_t* __restrict__ zero, int nzero) {
   pdl_begin();
+  for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
   extern __shared__ int32_t sm[];
   int32_t* cnt = sm;           // [E]
   int32_t* off = sm + E;       // [E]
@@ -325,8 +329,17 @@ extern "C" int moe_align_block_size(const int32_t* ids, int R, int E, int B, int
                                     int32_t* sorted_ids, int32_t* block_expert, int32_t* n_post_pad,
                                     int32_t* status, void* workspace, size_t workspace_bytes,
                                     oes_stream_t stream) {
+  return align_run(ids, R, E, B, ignore_invalid, sorted_ids, block_expert, n_post_pad, status,
+                   workspace, workspace_bytes, nullptr, 0, stream);
+}
+
+namespace oes {
+int align_run(const int32_t* ids, int R, int E, int B, int ignore_invalid, int32_t* sorted_ids,
+              int32_t* block_expert, int32_t* n_post_pad, int32_t* status, void* workspace,
+              size_t workspace_bytes, int32_t* zero, int nzero, cudaStream_t stream) {
   OES_REQUIRE(n_post_pad && workspace && (R == 0 || (ids && sorted_ids && block_expert)),
               "moe_align_block_size: null pointer");
+  OES_REQUIRE(nzero >= 0 && (nzero == 0 || zero), "moe_align_block_size: bad words to zero");
   OES_REQUIRE(R >= 0 && R < (1 << 30) && E >= 1 && E <= OES_MAX_EXPERTS && B >= 1 && B <= 1024,
               "moe_align_block_size: bad R=%d E=%d B=%d", R, E, B);
   OES_REQUIRE(((uintptr_t)workspace & 15) == 0, "moe_align_block_size: workspace not 16-byte aligned");
@@ -339,7 +352,7 @@ extern "C" int moe_align_block_size(const int32_t* ids, int R, int E, int B, int
   if (R <= kSmallR) {
     const size_t smem = ((size_t)2 * E + std::max(R, 1)) * 4;  // at most 36 KB
     launch_kernel(align_small_kernel, 1, 1024, smem, stream, ids, R, E, B, cap, ignore_invalid, sorted_ids,
-                                                  block_expert, n_post_pad, status);
+                  block_expert, n_post_pad, status, zero, nzero);
     OES_CHECK_LAUNCH("align_small_kernel");
     return OES_OK;
   }
@@ -360,7 +373,7 @@ extern "C" int moe_align_block_size(const int32_t* ids, int R, int E, int B, int
   }
   launch_kernel(align_count_kernel, G, kAlignThreads, hist_smem, stream, ids, R, E, C, ignore_invalid, ws, status);
   OES_CHECK_LAUNCH("align_count_kernel");
-  launch_kernel(align_scan_kernel, 1, 1024, hist_smem, stream, G, E, B, ws, n_post_pad);
+  launch_kernel(align_scan_kernel, 1, 1024, hist_smem, stream, G, E, B, ws, n_post_pad, zero, nzero);
   OES_CHECK_LAUNCH("align_scan_kernel");
   const int fill_ctas = (int)std::min<int64_t>(
       std::max<int64_t>(1, ceil_div64(cap / B, kAlignWarps * 4)), (int64_t)num_sms());
@@ -369,6 +382,7 @@ extern "C" int moe_align_block_size(const int32_t* ids, int R, int E, int B, int
   OES_CHECK_LAUNCH("align_scatter_kernel");
   return OES_OK;
 }
+}  // namespace oes
 
 // ------------------------------------------------------ no-allocation variant
 // Scratch for moe_align_block_size_noalloc: one fixed buffer per GPU that

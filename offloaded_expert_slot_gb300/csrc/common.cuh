@@ -232,6 +232,12 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// Device-scope acquire-release atomic add on global memory; returns the old value.
+__device__ __forceinline__ int32_t atom_add_acq_rel_gpu(int32_t* ptr, int32_t v) {
+  int32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+  return old;
+}
 // 32 lanes x 16 columns of 32-bit values: thread i of the warp gets row
 // (lane base + i), columns col..col+15.
 __device__ __forceinline__ void tmem_ld_16(uint32_t taddr, uint32_t (&r)[16]) {

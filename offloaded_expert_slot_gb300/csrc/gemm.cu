@@ -72,7 +72,7 @@ constexpr int kTmConvWarps = 16;
 __host__ __device__ constexpr int gemm_threads_tm(int wf) { return 32 * (wf ? kTmConvW0 + kTmConvWarps : 12); }
 
 struct Unit {
-  int b, m, slot, nvalid;
+  int b, m, h, slot, nvalid;  // h: the unit's K half (0 unless the tile's K is split)
   bool skip;
 };
 
@@ -81,12 +81,15 @@ constexpr int kFiltered = -2;  // Unit::slot of a block another launch computes
 // Which block / tile a unit is, the slot of its expert, and how many of the
 // block's entries are real routes (padding, value R, only at the end).
 __device__ __forceinline__ Unit unit_info(const GemmParams& p, int u, int nb) {
-  // tile index fastest: the units of one block run on neighbouring CTAs at
-  // the same time, so the block's token rows (GEMM1) or h rows (GEMM2) are
-  // read from DRAM once and then served from L2 for its other tiles
+  // tile index fastest (after the K half): the units of one block run on
+  // neighbouring CTAs at the same time, so the block's token rows (GEMM1) or
+  // h rows (GEMM2) are read from DRAM once and then served from L2 for its
+  // other tiles
   Unit t;
-  t.b = u / p.n_mtiles;
-  t.m = u % p.n_mtiles;
+  const int upb = p.n_mtiles * p.ks;  // units per block
+  t.b = u / upb;
+  t.m = (u % upb) / p.ks;
+  t.h = (u % upb) % p.ks;
   const int e = p.block_expert[t.b];
   const bool valid_e = e >= 0 && e < p.E;
   const bool filtered = p.filter && valid_e && p.flags[e] != p.filter;
@@ -109,7 +112,13 @@ __device__ __forceinline__ Unit unit_info(const GemmParams& p, int u, int nb) {
 
 __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
 
-struct UnitRec {  // shared-memory copy of a Unit
+// K chunks [kc_lo, kc_hi) of a unit: all of the tile's, or those of its half
+__device__ __forceinline__ int kc_lo(const GemmParams& p, const Unit& t) { return t.h * p.n_kc / p.ks; }
+__device__ __forceinline__ int kc_hi(const GemmParams& p, const Unit& t) {
+  return (t.h + 1) * p.n_kc / p.ks;
+}
+
+struct UnitRec {  // shared-memory copy of a Unit; m holds tile * ks + K half
   int b, m, slot, nvalid;
 };
 
@@ -128,7 +137,8 @@ __device__ __forceinline__ int block_nvalid(const GemmParams& p, int b) {
 
 // A filtered launch deals out only the units of the selected blocks, densely,
 // so that its CTAs get equal shares: the selected block of rank g (blocks in
-// order) owns units g * n_mtiles + m (tile fastest, as everywhere), and this
+// order) owns units g * upb + m, upb = n_mtiles * ks (tile fastest after the
+// K half, as everywhere), and this
 // CTA takes every gridDim.x-th of them into its table.  Every CTA computes the
 // same ranks.  Returns the number of units, or -1 when this CTA's share would
 // not fit the table (the caller then numbers units as an unfiltered launch and
@@ -151,14 +161,15 @@ __device__ int fill_filtered_units(const GemmParams& p, int nb, UnitRec* utab, i
       if (i < warp) off += s_scan[i];
       n += s_scan[i];
     }
-    const int units = n * p.n_mtiles;
+    const int upb = p.n_mtiles * p.ks;
+    const int units = n * upb;
     if (units > kMaxUnitsPerCta * (int)gridDim.x) return -1;
     if (sel) {
       const int g = off + __popc(bal & ((1u << lane) - 1u));
       const int nvalid = block_nvalid(p, tid);
       const int slot = p.e2s[p.block_expert[tid]];
-      for (int m = 0; m < p.n_mtiles; ++m) {
-        const int v = g * p.n_mtiles + m;
+      for (int m = 0; m < upb; ++m) {
+        const int v = g * upb + m;
         if (v % (int)gridDim.x == (int)blockIdx.x) utab[v / gridDim.x] = UnitRec{tid, m, slot, nvalid};
       }
     }
@@ -176,7 +187,8 @@ __device__ int fill_filtered_units(const GemmParams& p, int nb, UnitRec* utab, i
     s_scan[32] = n;
   }
   __syncthreads();
-  const int units = s_scan[32] * p.n_mtiles;
+  const int upb = p.n_mtiles * p.ks;
+  const int units = s_scan[32] * upb;
   __syncthreads();
   if (units > kMaxUnitsPerCta * (int)gridDim.x) return -1;
   int base = 0;
@@ -195,8 +207,8 @@ __device__ int fill_filtered_units(const GemmParams& p, int nb, UnitRec* utab, i
       const int g = off + __popc(bal & ((1u << lane) - 1u));
       const int nvalid = block_nvalid(p, b);
       const int slot = p.e2s[p.block_expert[b]];
-      for (int m = 0; m < p.n_mtiles; ++m) {
-        const int v = g * p.n_mtiles + m;
+      for (int m = 0; m < upb; ++m) {
+        const int v = g * upb + m;
         if (v % (int)gridDim.x == (int)blockIdx.x) utab[v / gridDim.x] = UnitRec{b, m, slot, nvalid};
       }
     }
@@ -213,7 +225,8 @@ __device__ __forceinline__ Unit my_unit(const GemmParams& p, const UnitRec* tab,
     const UnitRec r = tab[idx];
     Unit t;
     t.b = r.b;
-    t.m = r.m;
+    t.m = r.m / p.ks;
+    t.h = r.m % p.ks;
     t.slot = r.slot;
     t.nvalid = r.nvalid;
     t.skip = t.slot < 0 || t.slot >= p.S || t.nvalid == 0;
@@ -336,6 +349,38 @@ __device__ __forceinline__ void convert_row(const uint8_t* q, uint32_t scales, u
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
+// GEMM1 epilogue of weight row i for routes c0 .. c0 + C - 1 of the unit's
+// block: h = silu(g gs) * (u gs) from the fp32 sums g and u, stored as 16-bit
+// h.  W4A4 quantises h per 16 rows, one row a lane: all 32 lanes take part.
+template <int WF, int C>
+__device__ __forceinline__ void store_h(const GemmParams& p, const Unit& t, int i, int c0,
+                                        const float (&g)[C], const float (&v)[C], float gs) {
+  if (WF && p.a4) {
+#pragma unroll
+    for (int j = 0; j < C; ++j) {
+      const int n = c0 + j;
+      const bool keep = i < p.I && n < t.nvalid;
+      const float hv = keep ? silu(g[j] * gs) * (v[j] * gs) : 0.0f;
+      const uint16_t hb = quant_lane_act(hv, p.act[1]);
+      if (keep) p.h[((int64_t)t.b * p.BN + n) * p.I + i] = hb;
+    }
+  } else if (i < p.I) {
+#pragma unroll
+    for (int j = 0; j < C; ++j) {
+      const int n = c0 + j;
+      if (n < t.nvalid) {
+        const float gv = g[j] * gs;
+        const float uv = v[j] * gs;
+        const float hv = silu(gv) * uv;
+        uint16_t hb;
+        if (WF) hb = __half_as_ushort(__float2half_rn(hv));
+        else hb = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+        p.h[((int64_t)t.b * p.BN + n) * p.I + i] = hb;
+      }
+    }
+  }
+}
+
 template <int MODE, int WF>
 __global__ void __launch_bounds__(gemm_threads(WF), 1)
     grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
@@ -365,7 +410,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
   UnitRec* utab = reinterpret_cast<UnitRec*>(tmem_holder + 4);  // [kMaxUnitsPerCta]
 
   const int nb = *p.n_post_pad / p.BN;
-  int total = nb * p.n_mtiles;
+  int total = nb * p.n_mtiles * p.ks;
   const uint32_t acc_cols = (MODE == 1) ? 2 * p.BN : p.BN;
   __shared__ int s_scan[33];
   const int dense = p.filter ? fill_filtered_units(p, nb, utab, s_scan) : -1;
@@ -378,7 +423,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
       const int u = blockIdx.x + i * gridDim.x;
       if (u >= total) break;
       const Unit t = unit_info(p, u, nb);
-      utab[i] = UnitRec{t.b, t.m, t.slot, t.nvalid};
+      utab[i] = UnitRec{t.b, t.m * p.ks + t.h, t.slot, t.nvalid};
     }
   }
   __syncthreads();
@@ -431,7 +476,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
         const Unit t = my_unit(p, utab, ui, u, nb);
         if (t.skip) continue;
         const int row0 = t.m * kTileM;
-        for (int kc = 0; kc < p.n_kc && ok; ++kc) {
+        for (int kc = kc_lo(p, t), ke = kc_hi(p, t); kc < ke && ok; ++kc) {
           if (!WF) {
             ok = mbar_wait(&empty[s], ph ^ 1, p.status);
             if (!ok) break;
@@ -476,7 +521,8 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + a * acc_cols;
-        for (int kc = 0; kc < p.n_kc; ++kc) {
+        const int k0 = kc_lo(p, t), k1 = kc_hi(p, t);
+        for (int kc = k0; kc < k1; ++kc) {
           ok = mbar_wait(&full[s], ph, p.status);
           if (!ok) break;
           tc_fence_after();
@@ -488,7 +534,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
           const uint64_t bd = smem_desc_sw128(A + a_bytes);
 #pragma unroll
           for (int kk = 0; kk < kChunkK / 16; ++kk) {
-            const uint32_t acc = (kc | kk) ? 1u : 0u;
+            const uint32_t acc = (kc != k0 || kk) ? 1u : 0u;
             tc_mma_f16(d0, ad + 2 * kk, bd + 2 * kk, idesc, acc);
             if (MODE == 1) tc_mma_f16(d0 + p.BN, ud + 2 * kk, bd + 2 * kk, idesc, acc);
           }
@@ -509,7 +555,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
       for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
         const Unit t = my_unit(p, utab, ui, u, nb);
         if (t.skip) continue;
-        for (int kc = 0; kc < p.n_kc; ++kc) {
+        for (int kc = kc_lo(p, t), ke = kc_hi(p, t); kc < ke; ++kc) {
           ok = mbar_wait(&empty[s], ph ^ 1, p.status);
           if (!ok) break;
           uint8_t* B = stages + s * stage_bytes + a_bytes;
@@ -540,7 +586,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
           const int tk = (n < t.nvalid) ? p.sorted_ids[(int64_t)t.b * p.BN + n] / p.k : 0;
           src_off[j] = (int64_t)tk * p.H * 2 + c * 16;
         }
-        for (int kc = 0; kc < p.n_kc; ++kc) {
+        for (int kc = kc_lo(p, t), ke = kc_hi(p, t); kc < ke; ++kc) {
           if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, p.status);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
@@ -587,6 +633,54 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
       if (WF && p.a4) gs *= p.act[MODE - 1];
       const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16) + a * acc_cols;
       const int N = round16(t.nvalid);
+      if (MODE == 1 && p.ks == 2) {
+        // K split: each epilogue warp puts its 32 rows of this half's fp32
+        // sums in the tile's part and counts itself in; the warp of the
+        // second half to get there adds half 0's and half 1's sums and
+        // writes those rows of h.  No warp waits for another.
+        const int64_t tile = (int64_t)t.b * p.n_mtiles + t.m;
+        const int64_t hsz = 2 * (int64_t)p.BN * kTileM;  // gate and up sums of one half
+        const float* const tp = p.part + tile * 2 * hsz + row;  // this lane's row, half 0
+        float* wg = p.part + (tile * 2 + t.h) * hsz + row;
+        float* wu = wg + (int64_t)p.BN * kTileM;
+#pragma unroll 1
+        for (int c0 = 0; c0 < N; c0 += 16, wg += 16 * kTileM, wu += 16 * kTileM) {
+          uint32_t g[16], v[16];
+          tmem_ld_16(tl + c0, g);
+          tmem_ld_16(tl + p.BN + c0, v);
+          tc_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            wg[j * kTileM] = __uint_as_float(g[j]);
+            wu[j * kTileM] = __uint_as_float(v[j]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[a]);  // the accumulator is free again
+        ++use[a];
+        a ^= 1;
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atom_add_acq_rel_gpu(p.tcount + tile * 4 + q, 1) == 1;
+        if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+        __threadfence();
+        const int64_t uo = (int64_t)p.BN * kTileM;
+#pragma unroll 1
+        for (int c0 = 0; c0 < N; c0 += 8) {  // 8 routes at a time: fewer loads in flight
+          const float* r0 = tp + (int64_t)c0 * kTileM;
+          const float* r1 = r0 + hsz;
+          float gf[8], vf[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            gf[j] = __ldcg(r0 + j * kTileM) + __ldcg(r1 + j * kTileM);
+            vf[j] = __ldcg(r0 + uo + j * kTileM) + __ldcg(r1 + uo + j * kTileM);
+          }
+          store_h<WF, 8>(p, t, t.m * kTileM + row, c0, gf, vf, gs);
+        }
+        continue;
+      }
       for (int c0 = 0; c0 < N; c0 += 16) {
         uint32_t g[16];
         tmem_ld_16(tl + c0, g);
@@ -594,33 +688,13 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
           uint32_t v[16];
           tmem_ld_16(tl + p.BN + c0, v);
           tc_wait_ld();
-          const int i = t.m * kTileM + row;
-          if (WF && p.a4) {
-            // W4A4: a block of 16 along I is 16 consecutive lanes
+          float gf[16], vf[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int n = c0 + j;
-              const bool keep = i < p.I && n < t.nvalid;
-              const float hv = keep ? silu(__uint_as_float(g[j]) * gs) * (__uint_as_float(v[j]) * gs)
-                                    : 0.0f;
-              const uint16_t hb = quant_lane_act(hv, p.act[1]);
-              if (keep) p.h[((int64_t)t.b * p.BN + n) * p.I + i] = hb;
-            }
-          } else if (i < p.I) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int n = c0 + j;
-              if (n < t.nvalid) {
-                const float gv = __uint_as_float(g[j]) * gs;
-                const float uv = __uint_as_float(v[j]) * gs;
-                const float hv = silu(gv) * uv;
-                uint16_t hb;
-                if (WF) hb = __half_as_ushort(__float2half_rn(hv));
-                else hb = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
-                p.h[((int64_t)t.b * p.BN + n) * p.I + i] = hb;
-              }
-            }
+          for (int j = 0; j < 16; ++j) {
+            gf[j] = __uint_as_float(g[j]);
+            vf[j] = __uint_as_float(v[j]);
           }
+          store_h<WF, 16>(p, t, t.m * kTileM + row, c0, gf, vf, gs);
         } else {
           tc_wait_ld();
           const int col = t.m * kTileM + row;
@@ -656,7 +730,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
     for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
       const Unit t = my_unit(p, utab, ui, u, nb);
       if (t.skip) continue;
-      for (int kc = 0; kc < p.n_kc; ++kc) {
+      for (int kc = kc_lo(p, t), ke = kc_hi(p, t); kc < ke; ++kc) {
         ok = mbar_wait(&rfull[r], rph, p.status) && mbar_wait(&empty[s], ph ^ 1, p.status);
         if (!ok) break;
         const uint8_t* Q = raw + r * raw_stage;
@@ -729,7 +803,7 @@ __global__ void __maxnreg__(64)
   UnitRec* utab = reinterpret_cast<UnitRec*>(tmem_holder + 4);
 
   const int nb = *p.n_post_pad / p.BN;
-  int total = nb * p.n_mtiles;
+  int total = nb * p.n_mtiles * p.ks;
   __shared__ int s_scan[33];
   const int dense = p.filter ? fill_filtered_units(p, nb, utab, s_scan) : -1;
   if (dense >= 0) {
@@ -739,7 +813,7 @@ __global__ void __maxnreg__(64)
       const int u = blockIdx.x + i * gridDim.x;
       if (u >= total) break;
       const Unit t = unit_info(p, u, nb);
-      utab[i] = UnitRec{t.b, t.m, t.slot, t.nvalid};
+      utab[i] = UnitRec{t.b, t.m * p.ks + t.h, t.slot, t.nvalid};
     }
   }
   __syncthreads();
@@ -1193,9 +1267,21 @@ struct Ws {
   uint16_t* h;
   uint16_t* y;
   uint16_t* x16;
-  float* act;  // W4A4: the layer's two activation scales
+  float* act;        // W4A4: the layer's two activation scales
+  float* part;       // GEMM1 K split: fp32 sums of each tile's halves
+  int32_t* tcount;   // GEMM1 K split: halves finished per tile and epilogue warp
   size_t bytes;
 };
+
+// GEMM1 tiles of the largest routing a chunk of R routes can have (blocks of
+// 16, the weight-major kernel), if few enough that splitting their K range
+// could pay: then the workspace holds the split's sums.  0 otherwise.
+constexpr int64_t kSplitMaxTiles = 128;
+int64_t split_tiles(int64_t R, int E, int I, int B) {
+  if (B != 16 || R == 0) return 0;
+  const int64_t tiles = OES_ALIGN_CAPACITY(R, E, B) / B * ((I + kTileM - 1) / kTileM);
+  return tiles <= kSplitMaxTiles ? tiles : 0;
+}
 
 Ws carve(void* base, int T, int k, int E, int H, int I, int B, int wfmt) {
   Ws w{};
@@ -1212,6 +1298,11 @@ Ws carve(void* base, int T, int k, int E, int H, int I, int B, int wfmt) {
   if (wfmt != OES_WFMT_BF16) off += up((size_t)T * H * 2);
   w.act = reinterpret_cast<float*>(p + off);
   if (wfmt == OES_WFMT_NVFP4_W4A4) off += 256;
+  const int64_t st = split_tiles(R, E, I, B);
+  w.part = reinterpret_cast<float*>(p + off);
+  off += up((size_t)st * 2 * 2 * B * kTileM * 4);
+  w.tcount = reinterpret_cast<int32_t*>(p + off);
+  off += up((size_t)st * 4 * 4);
   w.bytes = off + 256;
   return w;
 }
@@ -1438,6 +1529,7 @@ int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
   p.E = E;
   p.S = S;
   p.up_row0 = I;
+  p.ks = 1;
   p.xg = xb;
   p.a4 = a4;
   p.act = ws.act;
@@ -1452,6 +1544,18 @@ int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
   g->p2 = p;
   g->p2.n_mtiles = g->tm ? ceil_div(H, 256) : ceil_div(H, kTileM);
   g->p2.n_kc = I / kChunkK;
+  // GEMM1's K split: when the tiles of the largest routing this chunk can
+  // have fill at most half the SMs (a one-token decode), each tile's K range
+  // is shared by two CTAs.  Decided from the plan alone, so every launch of
+  // a call, and the slot and streamed paths, split alike.
+  const int64_t st = split_tiles(R, E, I, B);
+  g->split_tiles = 0;
+  if (!g->tm && st > 0 && st * 2 <= num_sms() && g->p1.n_kc >= 2) {
+    g->split_tiles = (int)st;
+    g->p1.ks = 2;
+    g->p1.part = ws.part;
+    g->p1.tcount = ws.tcount;
+  }
   return OES_OK;
 }
 
@@ -1518,6 +1622,8 @@ extern "C" int moe_grouped_gemm_slots(const oes_routed_experts* v, const uint16_
   int rc = gemm_prepare(v, x, T, k, sorted_ids, block_expert, n_post_pad, B, workspace,
                         workspace_bytes, status, &g);
   if (rc) return rc;
+  const SplitCounters sc = split_counters(g);
+  if (sc.n > 0) OES_TRY_CUDA(cudaMemsetAsync(sc.ptr, 0, (size_t)sc.n * 4, stream));
   if ((rc = gemm_prepare_x(g, stream))) return rc;
   if ((rc = gemm_run(g, 0, nullptr, nullptr, stream))) return rc;
   return gemm_combine(g, ids, weights, out, stream);

@@ -32,6 +32,9 @@ struct GemmParams {
   int64_t scal_off;  // NVFP4: byte offset of the fp32 scalars in a row
   int R, k, BN, H, I, E, S;
   int n_mtiles, n_kc, up_row0;  // up_row0: first up row of w13 (= I)
+  int ks;          // K splits of a tile: 1, or 2 (GEMM1 of the weight-major kernel)
+  float* part;     // ks = 2: fp32 gate and up sums of each half of each tile [tiles][2][2][BN][128]
+  int32_t* tcount;  // ks = 2: halves finished per tile and epilogue warp [tiles][4], zero before GEMM1
   int NS, NR;                   // pipeline depths
   uint32_t tmem_cols;
   const uint16_t* xg;  // GEMM1: token rows to gather, [T, H] (bf16, or f16 for NVFP4)
@@ -45,6 +48,7 @@ struct GemmPlan {
   GemmMaps m1, m2;
   GemmParams p1, p2;
   bool empty, tm;
+  int split_tiles;  // > 0: GEMM1 splits K over this many tiles at most
   int wf, a4, T, k, H, E;
   uint16_t* y;
   const uint16_t* x;        // the chunk's x (bf16)
@@ -60,6 +64,17 @@ int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
                  int B, void* workspace, size_t workspace_bytes, int32_t* status, GemmPlan* plan);
 // the x kernels of a prepared GEMM (NVFP4 weights), on `stream`
 int gemm_prepare_x(const GemmPlan& plan, cudaStream_t stream);
+// The int32 words GEMM1's K split needs zeroed before the plan's first
+// gemm_run (none when it does not split); a composite call has its align
+// zero them.
+struct SplitCounters {
+  int32_t* ptr;
+  int n;
+};
+inline SplitCounters split_counters(const GemmPlan& plan) {
+  if (plan.empty || plan.split_tiles <= 0) return {nullptr, 0};
+  return {plan.p1.tcount, plan.split_tiles * 4};
+}
 // filter: 0 every block; g > 0 the blocks of experts with flags[e] == g
 int gemm_run(const GemmPlan& plan, int filter, const uint8_t* flags, const int32_t* gcount,
              cudaStream_t stream);

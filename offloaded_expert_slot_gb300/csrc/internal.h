@@ -44,6 +44,12 @@ struct oes_expert_source {
 
 namespace oes {
 int tile_plan(int R, int E);
+// moe_align_block_size, which also zeroes nzero int32 words at `zero` (device)
+// in one of its kernels: a composite call clears the GEMM's K-split counters
+// there instead of in a memset of its own.
+int align_run(const int32_t* ids, int R, int E, int B, int ignore_invalid, int32_t* sorted_ids,
+              int32_t* block_expert, int32_t* n_post_pad, int32_t* status, void* workspace,
+              size_t workspace_bytes, int32_t* zero, int nzero, cudaStream_t stream);
 
 // The slot path copies the n misses of a query of more than kSplitIds ids in
 // two parts, so that the GEMM over the first part's experts runs while the

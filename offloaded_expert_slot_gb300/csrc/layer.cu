@@ -244,8 +244,9 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
   // while the queries are ensured
   cudaStream_t gs = cache->gemm;
   OES_TRY_CUDA(cudaStreamWaitEvent(gs, cache->routed, 0));
-  if ((rc = moe_align_block_size(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad,
-                                 c->status, w.align_ws, w.align_bytes, gs)))
+  const SplitCounters sc = split_counters(g);
+  if ((rc = align_run(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad, c->status,
+                      w.align_ws, w.align_bytes, sc.ptr, sc.n, gs)))
     return rc;
   if ((rc = gemm_prepare_x(g, gs))) return rc;
   OES_TRY_CUDA(cudaEventRecord(cache->prepared, gs));
@@ -342,8 +343,9 @@ extern "C" int moe_layer_forward_stream(const oes_expert_source* src, void* laye
   launch_kernel(iota_kernel, ceil_div(E, 256), 256, 0, compute_stream, w.e2s_identity, E);
   OES_CHECK_LAUNCH("iota_kernel");
   if ((rc = route(d, c, w, compute_stream))) return rc;
-  if ((rc = moe_align_block_size(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad,
-                                 c->status, w.align_ws, w.align_bytes, compute_stream)))
+  const SplitCounters sc = split_counters(g);
+  if ((rc = align_run(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad, c->status,
+                      w.align_ws, w.align_bytes, sc.ptr, sc.n, compute_stream)))
     return rc;
   if ((rc = gemm_prepare_x(g, compute_stream))) return rc;  // overlaps the layer copy
   if (copied) {
@@ -574,9 +576,10 @@ extern "C" int moe_layers_forward_staged(const oes_stage_plan* p, const oes_expe
       const LayerWs w = carve_layer(c->workspace, d, T, k);
       const int B = tile_plan(R, E);
       int rc = route(d, c, w, compute_stream);
+      const SplitCounters sc = split_counters(plans[i]);
       if (!rc)
-        rc = moe_align_block_size(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad,
-                                  c->status, w.align_ws, w.align_bytes, compute_stream);
+        rc = align_run(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad, c->status,
+                       w.align_ws, w.align_bytes, sc.ptr, sc.n, compute_stream);
       if (!rc) rc = gemm_prepare_x(plans[i], compute_stream);
       if (rc) return rc;
       OES_TRY_CUDA(cudaStreamWaitEvent(compute_stream, p->copied[b], 0));

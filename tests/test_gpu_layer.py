@@ -267,6 +267,25 @@ def test_workload_layers(cfg, tokens):
     w.close()
 
 
+@pytest.mark.parametrize("cfg", [scaled(C2, name="one_token_bf16", T=1),
+                                 scaled(C4, name="one_token_nvfp4", T=1),
+                                 scaled(C2, name="two_tokens_bf16", T=2)], ids=lambda c: c.name)
+def test_few_token_decode(cfg):
+    """One token x top-10 over the decode-width layer (512 experts, hidden
+    2048, intermediate 768): GEMM1's 60 tiles fill at most half the SMs, so
+    each tile's K range is shared by two CTAs and the second to finish writes
+    h.  Two tokens (120 tiles) take whole tiles.  Either way slot == stream
+    byte for byte and the output follows the oracle; a second, warm call (every
+    expert a hit, the GEMM over the hits alone) gives the same bytes."""
+    lib()
+    w = Workload(cfg)
+    first = full_check(w)
+    warm = gpu_slots(w)
+    assert int(warm.status.item()) == 0
+    assert torch.equal(warm.out.view(torch.int16), first.out.view(torch.int16))
+    w.close()
+
+
 def test_long_prefill_layers_sequence():
     """4096 tokens x top-10 over 48 layers of 512 NVFP4 experts in a
     1650-slot pool: all 48 layers forwarded in turn through the slot path
