@@ -380,7 +380,10 @@ int moe_grouped_gemm_workspace_views(const oes_routed_experts *view, int T, int 
  * NVFP4 weights are decoded exactly and the global scales applied to the
  * fp32 sums.  Every reduction order depends only on the routing, never on
  * the slots, so the result over the pool equals the result over a
- * contiguous layer buffer (e2s = identity) bit for bit.
+ * contiguous layer buffer (e2s = identity) bit for bit.  When the GEMM1
+ * tiles of the largest routing of T x k fill at most half the SMs (one-token
+ * decode), each tile's K range is summed in two halves on two SMs, added in
+ * fp32 in a fixed order (half 0 + half 1) before the SwiGLU.
  * x: device [T, H] bf16; ids / weights: the router's [T, k] int32 / fp32
  * (a route whose id is outside [0, E) contributes nothing); sorted_ids,
  * block_expert, n_post_pad: moe_align_block_size with B from oes_tile_plan

@@ -29,6 +29,13 @@
 // pool [S][rows][K]; the slot coordinate comes from the remap, so the same
 // kernel over a contiguous layer buffer (remap = identity) runs the same
 // instructions on the same data in the same order: bit-identical output.
+// K split (GEMM1, weight-major): when the GEMM1 tiles of the largest routing
+// a chunk can have fill at most half the SMs (one token at top-10: 60 tiles
+// of 32 K chunks), every tile becomes two units, one per half of its K
+// range, on neighbouring CTAs.  Each half leaves its fp32 gate and up sums in
+// the workspace; the epilogue warp of the second half to count itself in
+// adds half 0 and half 1 and writes h.  The split is part of the plan, so
+// every launch of a call, and both paths, take it alike.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
