@@ -4,18 +4,27 @@ slot cache, on one GB300 (or N independent replicas, one per GPU).
 A step is one pass of the whole slot path over one chunk: route -> distinct
 experts -> queries of 128 (ensure + miss copies from pinned host memory) ->
 align -> grouped SwiGLU GEMM -> combine.  Before each step the cache tables
-are restored on the device to the workload's seeded pre-fill (a 25 KB
-device-to-device copy inside the timed region), so every step admits the same
-misses and copies the same rows.  Workload: the decode-width step (32 tokens,
-top-10, 512 experts, hidden 2048, intermediate 768, bf16 experts, 1100-slot
-pool shared by 2 layers with 800 slots pre-filled).
+are restored on the device to the workload's seeded state (a device-to-device
+copy of the tables inside the timed region), so every step admits the same
+misses and copies the same rows.
+
+Headline workload: the long prefill, the largest single-GPU workload -- a
+4096-token chunk, top-10 over 512 NVFP4 experts (hidden 2048, intermediate
+768), a 1650-slot pool shared by 48 layers that starts empty, so every step
+loads all of the layer's routed experts (1.36 GB) over the host link and
+runs the GEMM over them.  Only the forwarded layer's rows are pinned on the
+host: with an empty pool no other layer's row is ever read.  The
+decode-width step (32 tokens, bf16 experts, 1100 slots with 800 pre-filled)
+is measured after it and reported under "decode_width".
 
 Output: one JSON line (rank 0).  `value` = tokens of all ranks / max step time
 over ranks; `e2e` = the same through the C ABI with the chunk's inputs copied
 from pinned host memory and the output read back inside every timed step;
 `roofline` = the step with the largest share of the step time, against its
-bound; `cpu_baseline` = the CPU oracle timed on the host cores on a bounded
-sample of the same workload.
+bound; `roofline_gemm` = the grouped GEMM against its own bound (tensor
+cores or HBM, whichever is slower for its flops and bytes); `cpu_baseline` =
+the CPU oracle timed on the host cores on a bounded sample of the same
+workload.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -36,18 +45,19 @@ sys.path.insert(0, ROOT)
 
 from offloaded_expert_slot_gb300.configs import CONFIGS  # noqa: E402
 
-DEFAULT_CONFIG = "c2_decode_width"
+DEFAULT_CONFIG = "c5_long_prefill"
+SECONDARY_CONFIG = "c2_decode_width"
 METRIC = "routed tokens/s per MoE layer (1xGB300)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) on the decode-width workload from one ncu
-# capture of the current kernels, of the launches the breakdown times
-# (`python bench.py --breakdown --steps 2`, profiles/launch_list_c2_decode_width.md):
-# per whole-query copy_misses_kernel launch (three a step, the third query
-# empty) 0.1 MB read + 123.7 MB written; per step the grouped GEMM (GEMM1,
-# GEMM2, combine) 2342.5 MB.  Valid only for that workload and these kernels.
-TRAFFIC_WORKLOAD = "c2_decode_width"
-COPY_TRAFFIC_PER_LAUNCH = 123.77e6
-GEMM_TRAFFIC_PER_STEP = 2342.5e6
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of the launches
+# the breakdown times, from one ncu capture of the current kernels on each
+# workload: per whole-query copy_misses_kernel launch, and per step for the
+# grouped GEMM (GEMM1, GEMM2, combine).  A workload without an entry, or a
+# kernel changed since its capture, reports traffic null.
+TRAFFIC = {
+    "c2_decode_width": {"copy_per_launch": 123.77e6, "gemm_per_step": 2342.5e6},
+    "c5_long_prefill": {"copy_per_launch": 275.66e6, "gemm_per_step": 1934.1e6},
+}
 
 
 def peaks():
@@ -112,10 +122,29 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- oracle
-def oracle_sample(cfg, rin, source_row, prefill, n_tokens, seed):
-    """One bounded sample of the oracle's slot path: routing, distinct
-    experts, every LRU query and the align for the whole chunk; the expert
-    MLP and combine for n_tokens sampled tokens.  Returns seconds."""
+ORACLE_SAMPLE_TOKENS = 1024   # chunk prefix the oracle takes per sample
+ORACLE_MLP_TOKENS = 8         # of which the expert MLP and combine run on this many
+
+
+def oracle_chunk(cfg, rin):
+    """The oracle's bounded sample of a chunk: its first ORACLE_SAMPLE_TOKENS
+    tokens (same experts, pool, weights and query width)."""
+    from offloaded_expert_slot_gb300.configs import scaled
+    Ts = min(cfg.T, ORACLE_SAMPLE_TOKENS)
+    if Ts == cfg.T:
+        return cfg, rin
+    r = dict(rin)
+    r["x"] = rin["x"][:Ts]
+    if rin.get("logits") is not None:
+        r["logits"] = rin["logits"][:Ts]
+    return scaled(cfg, T=Ts), r
+
+
+def oracle_sample(cfg, rin, source_row, prefill, n_tokens, seed, toks=None):
+    """One bounded sample of the oracle's slot path over `cfg`'s chunk:
+    routing, distinct experts, every LRU query and the align for the whole
+    chunk; the expert MLP and combine for n_tokens sampled tokens (or the
+    given `toks`).  Returns seconds."""
     from oracle.layer import forward_slots
     from oracle.slot_cache import SlotCache
     from offloaded_expert_slot_gb300.inputs import empty_slot_row
@@ -124,12 +153,21 @@ def oracle_sample(cfg, rin, source_row, prefill, n_tokens, seed):
             for s, k in enumerate(prefill["slot_key"])}
     cache = SlotCache.from_state(cfg.S, cfg.L, cfg.E, prefill["slot_key"], prefill["slot_ts"],
                                  prefill["clock"])
-    toks = np.random.default_rng(seed).choice(cfg.T, n_tokens, replace=False)
+    if toks is None:
+        toks = np.random.default_rng(seed).choice(cfg.T, n_tokens, replace=False)
     per = -(-(cfg.T * cfg.k) // cfg.E)           # the library's tile plan: routes per expert
     block = 16 if per <= 8 else 128
     t0 = time.perf_counter()
     forward_slots(cfg, rin, source_row, cache, pool, block=block, tokens=toks)
     return time.perf_counter() - t0
+
+
+def sample_text(cfg, cs, n_tok):
+    pre = (f"the first {cs.T} of the chunk's {cfg.T} tokens"
+           if cs.T < cfg.T else f"the whole {cfg.T}-token chunk")
+    return (f"oracle slot path over {pre} (routing, distinct experts, LRU queries, align; "
+            f"the workload's experts, pool and weights) with the expert MLP and combine for "
+            f"{n_tok} of those tokens")
 
 
 def lazy_source(cfg, needed):
@@ -148,31 +186,36 @@ def lazy_source(cfg, needed):
 
 
 def reference_arm(args, cfg):
-    """The CPU oracle as the reference implementation, on the host cores."""
+    """The CPU oracle as the reference implementation, on the host cores.
+    The MLP sample is one fixed set of tokens, so that only their experts'
+    rows need generating on the host (about 0.2 s an NVFP4 expert); every
+    other expert the chunk loads gets a zero row, which the sample never
+    reads."""
     from offloaded_expert_slot_gb300.inputs import pool_prefill, router_inputs
     from oracle.router import gate_logits, route_topk
-    rin = router_inputs(cfg)
+    cs, rin = oracle_chunk(cfg, router_inputs(cfg))
     prefill = pool_prefill(cfg)
     logits = rin["logits"] if rin["logits"] is not None else gate_logits(rin["x"], rin["gate"])
     ids, _ = route_topk(logits, cfg.k)
-    n_tok = min(cfg.T, 8)
-    needed = {(cfg.layer, int(e)) for e in np.unique(ids)}
+    n_tok = min(cs.T, ORACLE_MLP_TOKENS)
+    toks = np.random.default_rng(cfg.seed).choice(cs.T, n_tok, replace=False)
+    needed = {(cfg.layer, int(e)) for e in np.unique(ids[toks])}
     src = lazy_source(cfg, needed)
-    src_row = lambda l, e: src(l, e) if (l, e) in needed else np.zeros(cfg.row_bytes, np.uint8)
+    zero = np.zeros(cfg.row_bytes, np.uint8)
+    src_row = lambda l, e: src(l, e) if (l, e) in needed else zero
     for i in range(args.warmup):
-        oracle_sample(cfg, rin, src_row, prefill, n_tok, i)
-    times = [oracle_sample(cfg, rin, src_row, prefill, n_tok, 100 + i) for i in range(args.steps)]
+        oracle_sample(cs, rin, src_row, prefill, n_tok, i, toks=toks)
+    times = [oracle_sample(cs, rin, src_row, prefill, n_tok, 100 + i, toks=toks)
+             for i in range(args.steps)]
     s = float(np.sum(times))
     value = n_tok * args.steps / s
     cores = len(os.sched_getaffinity(0))
-    sample = (f"oracle slot path on the full chunk (routing, distinct, LRU queries, align) with "
-              f"the expert MLP and combine for {n_tok} of {cfg.T} tokens per step")
+    sample = sample_text(cfg, cs, n_tok) + " (a fixed token sample, the same every step)"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000 * s / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg.name, "T": cfg.T, "k": cfg.k, "E": cfg.E, "H": cfg.H,
-                       "I": cfg.I, "wfmt": cfg.wfmt, "slots": cfg.S, "layers_in_pool": cfg.L},
+            "config": config_of(cfg, args.gpus),
             "cpu_baseline": {"kind": "oracle", "value": value, "unit": "tokens/s", "cores": cores,
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -189,6 +232,11 @@ class Bench:
         from offloaded_expert_slot_gb300.inputs import (empty_slot_row, expert_layer_rows,
                                                         n_source_buffers, pool_prefill,
                                                         router_inputs, source_layer_index)
+        from offloaded_expert_slot_gb300.configs import scaled
+        if cfg.prefill == 0 and cfg.layer == 0 and not cfg.distinct_source_layers:
+            # an empty pool only ever reads the forwarded layer's rows: pin
+            # that layer alone and let every layer's source point at it
+            cfg = scaled(cfg, distinct_source_layers=1)
         self.torch, self.oes, self.cfg = torch, oes, cfg
         oes.load()
         rb = cfg.row_bytes
@@ -381,6 +429,16 @@ def reduce_max(x: float, dist, device) -> float:
     return float(t.item())
 
 
+def replica_config(cfg, rank: int):
+    """The workload of one replica: the same sizes, with rank r > 0 drawing
+    its own seeded chunk, pool pre-fill and expert rows (seed + 101 r).
+    Replicas share nothing: each has its own cache, pool and source."""
+    if rank == 0:
+        return cfg
+    from offloaded_expert_slot_gb300.configs import scaled
+    return scaled(cfg, seed=cfg.seed + 101 * rank)
+
+
 def job_value(tokens_per_rank: int, world: int, ms_max: float) -> float:
     """Whole-job throughput: tokens of all ranks over the slowest rank's step."""
     return tokens_per_rank * world / (ms_max / 1e3)
@@ -406,6 +464,64 @@ def gpu_launches(cfg, with_restore=True):
     return n
 
 
+def config_of(cfg, world):
+    """The workload as both arms report it: sizes only, nothing measured."""
+    routed_rows = min(cfg.T * cfg.k, cfg.E) * cfg.row_bytes
+    return {"workload": cfg.name, "T": cfg.T, "k": cfg.k, "E": cfg.E, "H": cfg.H, "I": cfg.I,
+            "wfmt": cfg.wfmt, "slots": cfg.S, "layers_in_pool": cfg.L, "prefilled": cfg.prefill,
+            "query_width": cfg.query_width, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2: a step reads up to min(T*k, E) expert rows, "
+                  f"{routed_rows / 1e9:.2f} GB"}
+
+
+def gemm_roofline(cfg, info, ms, pk, traffic):
+    """The grouped GEMM of one step (GEMM1 + GEMM2 + combine) against the
+    slower of its two bounds for its algorithmic work: R * 6HI flops on the
+    tensor cores (f16 or bf16 MMAs, both at the bf16 rate; the breakdown
+    times the GEMM alone, so the burst peak) or D expert rows + x + out bytes
+    on HBM."""
+    R = cfg.T * cfg.k
+    flops = R * 6 * cfg.H * cfg.I
+    nbytes = info["distinct"] * cfg.row_bytes + cfg.T * cfg.H * 2 * 2
+    hbm, bf16 = float(pk["hbm_gbs"]), float(pk["bf16_tflops"])
+    t_tensor, t_hbm = flops / (bf16 * 1e12), nbytes / (hbm * 1e9)
+    tflops = flops / (ms / 1e3) / 1e12
+    gbs = nbytes / (ms / 1e3) / 1e9
+    base = {"kernel": "grouped_gemm (gemm1 + gemm2 + combine)", "peak_source": pk["source"],
+            "algorithmic_flops": flops, "algorithmic_bytes": nbytes, "launch_ms": ms,
+            "traffic": traffic, "TFLOP/s": tflops, "GB/s": gbs,
+            "hbm_frac": gbs / hbm, "tensor_frac": tflops / bf16}
+    if t_tensor >= t_hbm:
+        base.update({"bound": "tensor", "achieved": tflops, "peak": bf16, "unit": "TFLOP/s",
+                     "frac": tflops / bf16})
+    else:
+        base.update({"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": gbs / hbm})
+    return base
+
+
+def measure_secondary(name, args, world, dist):
+    """A second workload's step, eager and graph-replayed (no breakdown)."""
+    import torch
+    cfg = CONFIGS[name]
+    rank = dist.get_rank() if dist else 0
+    b = Bench(replica_config(cfg, rank), rank)
+    for _ in range(args.warmup):
+        b.step()
+    torch.cuda.synchronize()
+    ms = reduce_max(b.timed(b.step, args.steps), dist, "cuda")
+    st = int(b.status.item())
+    gms = reduce_max(b.graph_timed(args.steps, args.warmup), dist, "cuda")
+    b.close()
+    del b
+    torch.cuda.empty_cache()
+    if st:
+        raise RuntimeError(f"device status {st} on {name}")
+    return {"workload": name, "value": job_value(cfg.T, world, ms), "unit": "tokens/s",
+            "ms_per_step": ms, "graph_ms_per_step": gms, "T": cfg.T, "wfmt": cfg.wfmt,
+            "slots": cfg.S, "prefilled": cfg.prefill}
+
+
 def gpu_arm(args, cfg):
     import torch
     rank = int(os.environ.get("RANK", "0"))
@@ -427,7 +543,7 @@ def gpu_arm(args, cfg):
         build.build()
     if dist:
         dist.barrier()
-    b = Bench(cfg, rank)
+    b = Bench(replica_config(cfg, rank), rank)
     for _ in range(args.warmup):
         b.step()
     torch.cuda.synchronize()
@@ -461,7 +577,6 @@ def gpu_arm(args, cfg):
     link = b.link_probe()
     pk = peaks()
     hbm = float(pk["hbm_gbs"])
-    bf16 = float(pk["bf16_tflops"])
     R = cfg.T * cfg.k
     H, I, E = cfg.H, cfg.I, cfg.E
     step_bytes = {
@@ -471,7 +586,6 @@ def gpu_arm(args, cfg):
         "copy": info["misses"] * cfg.row_bytes,
         "gemm": info["distinct"] * cfg.row_bytes + cfg.T * H * 2 * 2,
     }
-    flops = R * 6 * H * I
     kernels = {}
     for n, b_ in step_bytes.items():
         t_ms = bd[n]
@@ -480,48 +594,47 @@ def gpu_arm(args, cfg):
         kernels[n] = {"ms": round(t_ms, 5), "bytes": b_, "GB/s": gbs,
                       "bound": "host_link" if n == "copy" else "hbm",
                       "frac": (gbs / bound_peak) if gbs else None}
-    kernels["gemm"]["TFLOP/s"] = flops / (bd["gemm"] / 1e3) / 1e12
-    kernels["gemm"]["tensor_frac"] = kernels["gemm"]["TFLOP/s"] / bf16
     kernels["ensure"] = {"ms": round(bd["ensure"], 5), "queries": info["queries"],
                          "us_per_query": 1e3 * bd["ensure"] / info["queries"], "bound": "latency"}
     kernels["restore"] = {"ms": round(bd["restore"], 5)}
     dom = max(("route", "distinct", "ensure", "copy", "align", "gemm"), key=lambda n: bd[n])
-    # the GEMM is the dominant HBM/tensor kernel of the path; the miss copies are
-    # bound by the host link, whose peak is probed in this run.
-    g = kernels["gemm"]
-    gemm_hbm = g["GB/s"]
-    roof_gemm = {"kernel": "grouped_gemm (gemm1 + gemm2 + combine)", "bound": "hbm",
-                 "achieved": gemm_hbm, "peak": hbm, "unit": "GB/s", "frac": gemm_hbm / hbm,
-                 "traffic": GEMM_TRAFFIC_PER_STEP if cfg.name == TRAFFIC_WORKLOAD else None,
-                 "peak_source": pk["source"],
-                 "algorithmic_bytes": step_bytes["gemm"], "launch_ms": bd["gemm"]}
+    tr = TRAFFIC.get(cfg.name, {})
+    roof_gemm = gemm_roofline(cfg, info, bd["gemm"], pk, tr.get("gemm_per_step"))
+    kernels["gemm"].update({"TFLOP/s": roof_gemm["TFLOP/s"], "tensor_frac": roof_gemm["tensor_frac"],
+                            "bound": roof_gemm["bound"]})
     if dom == "copy":
+        # the miss copies are bound by the host link, whose peak is probed in
+        # this run; the GEMM overlaps them and is reported beside them
         c = kernels["copy"]
         q = info["queries"]
-        traffic = COPY_TRAFFIC_PER_LAUNCH if cfg.name == TRAFFIC_WORKLOAD else None
         roofline = {"kernel": "copy_misses_kernel", "bound": "host_link", "achieved": c["GB/s"],
-                    "peak": link, "unit": "GB/s", "frac": c["frac"], "traffic": traffic,
+                    "peak": link, "unit": "GB/s", "frac": c["frac"],
+                    "traffic": tr.get("copy_per_launch"),
                     "traffic_note": "DRAM read + write per launch from one ncu capture; the rows "
-                                    "are read over the host link, and up to ~40 MB of a launch's "
-                                    "writes is still in L2 when it ends",
+                                    "are read over the host link, and part of a launch's writes "
+                                    "is still in L2 when it ends",
                     "peak_source": "measured in this run: 1 GiB pinned host->device cudaMemcpyAsync",
                     "launches": q, "algorithmic_bytes": step_bytes["copy"] / q,
                     "launch_ms": bd["copy"] / q}
     else:
         roofline = roof_gemm
+    cpu = cpu_baseline(cfg, b) if rank == 0 else None
+    pinned = len(b.src_bufs)
+    b.close()
+    del b
+    torch.cuda.empty_cache()
+    secondary = None
+    if SECONDARY_CONFIG != cfg.name and not args.no_secondary:
+        secondary = measure_secondary(SECONDARY_CONFIG, args, world, dist)
     if rank == 0:
-        cpu = cpu_baseline(cfg, b)
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16" if cfg.wfmt == "bf16" else "nvfp4-w/f16", "data": "synthetic",
-                "config": {"workload": cfg.name, "T": cfg.T, "k": cfg.k, "E": E, "H": H, "I": I,
-                           "wfmt": cfg.wfmt, "slots": cfg.S, "layers_in_pool": cfg.L,
-                           "prefilled": cfg.prefill, "queries": info["queries"],
-                           "misses_per_step": info["misses"], "distinct": info["distinct"],
-                           "block": info["block"], "parallelism": f"replicas x{world}",
-                           "l2": "inputs larger than L2 (expert rows read per step "
-                                 f"{(info['distinct'] * cfg.row_bytes) / 1e9:.2f} GB)"},
+                "config": config_of(cfg, world),
+                "step_info": {"queries": info["queries"], "misses_per_step": info["misses"],
+                              "distinct": info["distinct"], "block": info["block"],
+                              "pinned_source_layers": pinned},
                 "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": bi,
                         "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms},
                 "gpu_launches": gpu_launches(cfg) * args.steps,
@@ -529,9 +642,9 @@ def gpu_arm(args, cfg):
                           "ms_per_step": graph_ms,
                           "what": "the same step captured once as a CUDA graph and replayed"},
                 "clocks": clocks, "roofline": roofline, "roofline_gemm": roof_gemm,
-                "steps_breakdown": kernels, "host_link_gbs": link, "cpu_baseline": cpu}
+                "steps_breakdown": kernels, "host_link_gbs": link, "cpu_baseline": cpu,
+                "decode_width": secondary}
         print(json.dumps(line))
-    b.close()
     if dist:
         dist.barrier()
         dist.destroy_process_group()
@@ -541,16 +654,16 @@ def cpu_baseline(cfg, b):
     """The oracle on the host cores over bounded samples (about 10 s)."""
     srcs = [x.numpy() for x in b.src_bufs]
     row = lambda l, e: srcs[b.source_index(l)][e]
-    n_tok = min(cfg.T, 8)
+    cs, rin = oracle_chunk(cfg, b.rin)
+    n_tok = min(cs.T, ORACLE_MLP_TOKENS)
     total, tokens, i = 0.0, 0, 0
     while total < 10.0 and i < 200:
-        total += oracle_sample(cfg, b.rin, row, b.prefill, n_tok, 1000 + i)
+        total += oracle_sample(cs, rin, row, b.prefill, n_tok, 1000 + i)
         tokens += n_tok
         i += 1
     return {"kind": "oracle", "value": tokens / total, "unit": "tokens/s",
             "cores": len(os.sched_getaffinity(0)),
-            "sample": f"{i} samples of the oracle slot path (full routing, LRU queries and align; "
-                      f"expert MLP and combine for {n_tok} of {cfg.T} tokens each), {total:.1f} s"}
+            "sample": f"{i} samples, {total:.1f} s: " + sample_text(cfg, cs, n_tok)}
 
 
 def sweep(args):
@@ -901,6 +1014,8 @@ def main():
                     help="decode steps with every routed expert resident (GEMM-bound), per width")
     ap.add_argument("--layers", action="store_true",
                     help="every layer of the workload in turn: slot path, staged, streamed")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the decode-width step measured after the headline")
     ap.add_argument("--breakdown", action="store_true",
                     help="only the per-step breakdown (each step's kernels as separate calls, "
                          "timed with events), for a profiler")

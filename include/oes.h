@@ -312,6 +312,10 @@ int moe_align_block_size(const int32_t *ids, int R, int E, int B, int ignore_inv
  * The first call on a device looks the buffer's device address up
  * (cudaGetSymbolAddress, with that device current); make that first call
  * before any stream capture.  The call allocates nothing.
+ * The address is kept per device ordinal for the life of the process: it
+ * does not survive a reset of the device (cudaDeviceReset, or anything else
+ * that destroys the primary context), after which this call must not be
+ * used again in the process.
  * Every call on a device shares the one buffer, which keeps the last call's
  * contents; each call writes all the scratch it reads, so nothing has to
  * start at zero.  Calls whose kernels overlap on the GPU (other streams, or

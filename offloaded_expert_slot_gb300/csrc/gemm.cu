@@ -671,6 +671,9 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
         __syncwarp();
         int last = 0;
         if (lane == 0) last = atom_add_acq_rel_gpu(p.tcount + tile * 4 + q, 1) == 1;
+        // the warp barrier orders lane 0's acquire before the other lanes'
+        // reads of the other half's sums below
+        __syncwarp();
         if (!__shfl_sync(0xffffffffu, last, 0)) continue;
         __threadfence();
         const int64_t uo = (int64_t)p.BN * kTileM;

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 from conftest import GOLDEN
-from gpu_util import Workload, cuda, i32, lib, status
+from gpu_util import Workload, cuda, f32, i32, lib, status
 from offloaded_expert_slot_gb300 import oes
 from offloaded_expert_slot_gb300.configs import C2, C5, scaled
 from offloaded_expert_slot_gb300.inputs import pool_prefill, router_inputs
@@ -297,3 +297,57 @@ def test_reset_returns_the_created_state(policy):
         assert [int(v) for v in crf] == o.crf and [int(v) for v in pin] == o.pin
     oes.slot_cache_destroy(fresh)
     c.close()
+
+
+def test_tiny_workload_queries_of_four_on_its_six_slot_pool():
+    """The tiny workload's own cache traffic: its gate logits, routing and
+    distinct experts computed on the GPU, then every query of 4 ensured and
+    its misses copied on its 6-slot pool with 3 experts pre-resident, each
+    step bit for bit against the oracle (tables, miss lists, pool rows).
+    The 8 distinct experts exceed the 6 slots, so its layer forward is
+    streamed (capacity reading: FreeToken PR #676, the author's reply);
+    the queries themselves fit, and follow the oracle."""
+    from offloaded_expert_slot_gb300.configs import C1
+    from oracle.router import gate_logits
+    cfg = C1
+    w = Workload(cfg, gen_device="cpu")
+    T, k, E, H, W = cfg.T, cfg.k, cfg.E, cfg.H, cfg.query_width
+    R = T * k
+    logits, ids, wts = f32(T * E), i32(R), f32(R)
+    oes.moe_gate_logits(w.x, w.gate, T, H, E, logits)
+    oes.moe_route_topk(logits, T, E, k, ids, wts)
+    Lq = min(R, E)
+    dist_d, dcnt = i32(Lq, -9), i32(1, -9)
+    oes.moe_distinct_experts(ids, R, E, dist_d, dcnt)
+    torch.cuda.synchronize()
+    o_ids, _ = route_topk(gate_logits(w.rin["x"], w.rin["gate"]), k)
+    o_dist, o_D = distinct_experts(o_ids, E)
+    assert np.array_equal(ids.cpu().numpy().reshape(T, k), o_ids)
+    assert np.array_equal(dist_d.cpu().numpy(), o_dist) and int(dcnt.item()) == o_D
+    assert o_D > cfg.S                       # the layer itself is refused by the slot path
+    o = SlotCache.from_state(cfg.S, cfg.L, E, w.prefill["slot_key"], w.prefill["slot_ts"],
+                             w.prefill["clock"])
+    opool = w.oracle_pool()
+    miss, n_miss, st = i32(3 * 128), i32(1), status()
+    for q0 in range(0, Lq, W):
+        n = min(W, Lq - q0)
+        oes.slot_cache_ensure(w.cache, cfg.layer, dist_d.data_ptr() + 4 * q0, n, 0, miss,
+                              n_miss, st)
+        oes.slot_cache_copy_misses(w.src, w.pool, cfg.S, miss, n_miss, n, st)
+        torch.cuda.synchronize()
+        s_, om = o.ensure([int(e) for e in o_dist[q0:q0 + n]])
+        assert s_ == 0 and int(st.item()) == 0
+        nm = int(n_miss.item())
+        got = [tuple(int(v) for v in r) for r in miss.cpu().numpy()[:3 * nm].reshape(nm, 3)]
+        assert got == [tuple(x) for x in om], q0
+        for key, slot, _ in om:
+            opool[slot] = w.source_row(key // E, key % E)
+        now = oes.slot_cache_read_state(w.cache, cfg.S, cfg.L, E)
+        assert np.array_equal(now["slot_key"], o.slot_key)
+        assert np.array_equal(now["slot_ts"], o.slot_ts)
+        assert np.array_equal(now["map"], o.map)
+        assert now["clock"] == o.clock
+        pool = w.pool.cpu().numpy()
+        for s in range(cfg.S):
+            assert np.array_equal(pool[s], opool[s]), (q0, s)
+    w.close()
