@@ -286,34 +286,65 @@ def test_few_token_decode(cfg):
     w.close()
 
 
+def _one_token_out(w: Workload, layer: int, ids: np.ndarray, wts: np.ndarray, t: int) -> np.ndarray:
+    """The oracle's output row of token t of a layer: its k experts' SwiGLU
+    MLPs on the layer's source rows (the rows its slots hold), combined in
+    j order, in fp64."""
+    from oracle.expert_mlp import expert_weights, swiglu_expert
+    from oracle.numerics import bf16_to_f64 as obf16
+    cfg = w.cfg
+    x = obf16(w.rin["x"][t])[None]
+    acc = np.zeros(cfg.H)
+    for j in range(cfg.k):
+        w13, w2 = expert_weights(w.source_row(layer, int(ids[t, j])), cfg.wfmt, cfg.H, cfg.I)
+        acc += np.float64(wts[t, j]) * swiglu_expert(x, w13, w2)[0]
+    return acc
+
+
 def test_long_prefill_layers_sequence():
     """4096 tokens x top-10 over 48 layers of 512 NVFP4 experts in a
     1650-slot pool: all 48 layers forwarded in turn through the slot path
     (each evicting older layers' experts) and the streamed path, slot ==
-    stream byte for byte on every layer; the tables follow the oracle
-    through the first three layers, two of them checked on sampled tokens."""
+    stream byte for byte on every layer.  On every layer the tables follow
+    the oracle's LRU bit for bit and one token's output row (a different
+    token per layer) follows the oracle's MLP; layers 0 and 2 also run the
+    oracle's whole slot path on 12 sampled tokens."""
+    from oracle.distinct import distinct_experts
+    from oracle.layer import route
     lib()
     cfg = C5
     w = Workload(cfg)
     R = cfg.T * cfg.k
     assert oes.oes_tile_plan(R, cfg.E) == 128
     toks = np.random.default_rng(5).choice(cfg.T, 12, replace=False)
+    one = np.random.default_rng(6).choice(cfg.T, cfg.L, replace=False)
     ocache = SlotCache.from_state(cfg.S, cfg.L, cfg.E, w.prefill["slot_key"], w.prefill["slot_ts"],
                                   w.prefill["clock"])
     opool = w.oracle_pool()
+    _l, oids, ow = route(w.rin, cfg.k)
+    odist, _D = distinct_experts(oids, cfg.E)
     for layer in range(cfg.L):
         r = gpu_slots(w, layer=layer)
         assert int(r.status.item()) == 0, layer
         s = gpu_stream(w, layer=layer)
         assert torch.equal(s.out.view(torch.int16), r.out.view(torch.int16)), layer
-        if layer < 3:
+        if layer in (0, 2):
             o = forward_slots(cfg, w.rin, w.source_row, ocache, opool, block=128, layer=layer,
-                              tokens=toks if layer != 1 else np.array([0]))
-            st = oes.slot_cache_read_state(w.cache, cfg.S, cfg.L, cfg.E)
-            assert np.array_equal(st["map"], ocache.map)
-            assert np.array_equal(st["slot_key"], ocache.slot_key)
-            if layer != 1:
-                check_close(r.out, o["out"], "nvfp4", toks)
+                              tokens=toks)
+            assert o["ok"]
+            check_close(r.out, o["out"], "nvfp4", toks)
+        else:
+            for q0 in range(0, odist.size, cfg.query_width):
+                keys = [layer * cfg.E + int(e) if e >= 0 else -1
+                        for e in odist[q0:q0 + cfg.query_width]]
+                assert ocache.ensure(keys)[0] == 0
+        st = oes.slot_cache_read_state(w.cache, cfg.S, cfg.L, cfg.E)
+        assert np.array_equal(st["map"], ocache.map), layer
+        assert np.array_equal(st["slot_key"], ocache.slot_key), layer
+        assert np.array_equal(st["slot_ts"], ocache.slot_ts), layer
+        t = int(one[layer])
+        want = _one_token_out(w, layer, oids, ow, t)
+        check_close(r.out[t:t + 1], want[None], "nvfp4")
     w.close()
 
 
