@@ -9,7 +9,10 @@ renormalised top-k".  Readings taken where the pages are silent:
     equals a softmax over the k selected logits -- computed in fp64 and
     stored as fp32;
   * bf16 logits are widened to fp32 (exact: bf16 is fp32's upper half) and
-    routed the same way.
+    routed the same way;
+  * a NaN logit ranks as -inf (a logit that is not a number is no evidence
+    for its expert): it is taken only after every finite logit, in id order
+    with the -inf ones, and gets weight 0 beside a finite winner.
 """
 from __future__ import annotations
 
@@ -27,6 +30,7 @@ def route_topk(logits: np.ndarray, k: int):
     """Returns ids [T, k] int32 (descending logit, ties to the lower id) and
     weights [T, k] fp32."""
     logits = np.asarray(logits, dtype=np.float32)
+    logits = np.where(np.isnan(logits), np.float32(-np.inf), logits)
     T, E = logits.shape
     assert 1 <= k <= E
     ids = np.empty((T, k), dtype=np.int32)

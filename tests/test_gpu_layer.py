@@ -28,6 +28,11 @@ MEDIUM_BF16 = scaled(C2, name="medium_bf16", T=96, k=4, E=16, H=256, I=192, S=40
 MEDIUM_NVFP4 = scaled(C4, name="medium_nvfp4", T=96, k=4, E=16, H=256, I=192, S=40, L=2, prefill=20)
 WIDE_BLOCKS = scaled(C2, name="wide_blocks_bf16", T=160, k=8, E=12, H=128, I=128, S=30, L=2,
                      prefill=10)
+# NVFP4 blocks of more than 96 routes (a unit then takes both of the NVFP4
+# kernel's accumulator slots), a GEMM2 tile pair whose second tile lies past
+# H, and K loops of two chunks
+WIDE_BLOCKS_NVFP4 = scaled(C4, name="wide_blocks_nvfp4", T=160, k=8, E=12, H=128, I=128, S=30,
+                           L=2, prefill=10)
 # few routes per expert: blocks of 16 on the weight-major kernel, ragged I
 MEDIUM_SWAP_BF16 = scaled(C2, name="medium_swap_bf16", T=40, k=3, E=16, H=256, I=192, S=40, L=2,
                           prefill=20)
@@ -151,8 +156,8 @@ def full_check(w: Workload, tokens=None):
     return r
 
 
-@pytest.mark.parametrize("cfg", [MEDIUM_BF16, WIDE_BLOCKS, MEDIUM_NVFP4, MEDIUM_SWAP_BF16,
-                                 MEDIUM_SWAP_NVFP4], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [MEDIUM_BF16, WIDE_BLOCKS, MEDIUM_NVFP4, WIDE_BLOCKS_NVFP4,
+                                 MEDIUM_SWAP_BF16, MEDIUM_SWAP_NVFP4], ids=lambda c: c.name)
 def test_medium_layers_match_oracle_and_stream(cfg):
     """Several tiles with a ragged last tile (I = 192), several K chunks,
     experts with several blocks and ragged block tails, on both kernels

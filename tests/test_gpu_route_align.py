@@ -64,6 +64,24 @@ def test_topk_signed_zeros_infinities_and_k16():
         np.testing.assert_allclose(w, ow, rtol=2e-6, atol=1e-7)
 
 
+def test_topk_nan_logits_rank_as_minus_infinity():
+    """NaN logits (the router's reading: NaN ranks as -inf) mixed with -inf
+    and finite ones, including rows with fewer than k finite logits: ids and
+    weights against the oracle."""
+    lib()
+    g = np.random.default_rng(14)
+    for E, k in [(512, 10), (33, 16), (2100, 32)]:
+        logits = g.standard_normal((24, E)).astype(np.float32)
+        logits[g.random((24, E)) < 0.2] = np.nan
+        logits[g.random((24, E)) < 0.1] = -np.inf
+        logits[2] = np.nan
+        logits[2, :3] = [1.0, -np.inf, 0.5]
+        ids, w = gpu_route(logits, k)
+        oids, ow = route_topk(logits, k)
+        assert np.array_equal(ids, oids), (E, k)
+        np.testing.assert_allclose(w, ow, rtol=2e-6, atol=1e-7)
+
+
 def test_topk_bf16_logits():
     """bf16 logits route as their exact fp32 widening: ids bit-exact against
     the oracle, weights within its bound, and both identical bit for bit to the

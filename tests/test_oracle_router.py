@@ -100,3 +100,16 @@ def test_distinct_brute_force(seed):
     assert d.size == min(R, E)
     assert d[:D].tolist() == want.tolist()
     assert (d[D:] == -1).all()
+
+
+def test_router_nan_ranks_as_minus_infinity():
+    """A NaN logit ranks with the -inf ones: after every finite logit, ties to
+    the lower id, weight 0 beside a finite winner."""
+    nan, inf = np.float32(np.nan), np.float32(np.inf)
+    logits = np.array([[0.5, nan, -inf, 1.0, nan, -2.0]], dtype=np.float32)
+    ids, w = route_topk(logits, 5)
+    assert ids.tolist() == [[3, 0, 5, 1, 2]]
+    assert w[0, 3] == 0.0 and w[0, 4] == 0.0 and abs(float(w.sum()) - 1.0) < 1e-6
+    # the same as writing -inf in their place
+    ids2, w2 = route_topk(np.where(np.isnan(logits), -inf, logits), 5)
+    assert np.array_equal(ids, ids2) and np.array_equal(w, w2)
