@@ -7,14 +7,18 @@
 // ignore_invalid_experts).
 //
 //   count:   CTA g histograms its contiguous range of routes -> cnt[g][e]
-//   scan:    one CTA: per expert, its total over CTAs; padded sizes;
-//            exclusive scan over experts -> expert offsets; cnt[g][e] becomes
-//            the first output position of CTA g's routes of expert e (the
-//            expert's offset plus its routes in CTAs before g)
-//   scatter: CTA g re-reads its range; each warp walks its 32-route groups
-//            in order and places them with __match_any_sync ranks, so routes
-//            of one expert keep ascending route order (bit-exact, stable);
-//            extra CTAs write the padding and block_expert.
+//            (eight loads in flight a thread)
+//   scan:    CTA c takes experts [32c, 32c + 32): its [G x 32] tile of counts
+//            in shared memory, scanned over g by all its warps at once;
+//            cnt[g][e] becomes the routes of expert e in CTAs before g, and
+//            tot[e] the expert's routes
+//   scatter: every CTA first scans the padded expert sizes itself (E <= 4096)
+//            -> expert offsets; CTA g re-reads its range; each warp walks its
+//            32-route groups in order, eight groups' ids loaded at once, and
+//            places them by their rank among the group's lanes of the same
+//            expert (found with one ballot per bit of the expert id), so
+//            routes of one expert keep ascending route order (bit-exact,
+//            stable); extra CTAs write the padding and block_expert.
 #include <algorithm>
 #include <mutex>
 
@@ -26,7 +30,6 @@ namespace {
 
 constexpr int kAlignThreads = 256;  // 8 warps
 constexpr int kAlignWarps = kAlignThreads / 32;
-constexpr int kScanBatch = 8;   // per-CTA counts one scan thread loads at once
 
 struct AlignWs {
   int32_t* cnt;   // [G][E]
@@ -34,6 +37,20 @@ struct AlignWs {
   int32_t* tot;   // [E] routes of each expert
   int32_t* nblk;  // [1] used blocks
 };
+
+constexpr int kAlignUnroll = 8;  // routes (or 32-route groups) loaded at once per thread
+
+// Lanes of the warp whose key equals this lane's, for keys below 2^nbits:
+// one ballot per bit (cheaper than a match instruction per 32 keys).
+__device__ __forceinline__ unsigned same_key_lanes(int key, int nbits) {
+  unsigned m = 0xffffffffu;
+  for (int b = 0; b < nbits; ++b) {
+    const bool bit = (key >> b) & 1;
+    const unsigned bal = __ballot_sync(0xffffffffu, bit);
+    m &= bit ? bal : ~bal;
+  }
+  return m;
+}
 
 __global__ void __launch_bounds__(kAlignThreads)
     align_count_kernel(const int32_t* __restrict__ ids, int R, int E, int C, int ignore_invalid,
@@ -44,44 +61,77 @@ __global__ void __launch_bounds__(kAlignThreads)
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   const int r0 = g * C, r1 = min(R, r0 + C);
+  const int step = blockDim.x * kAlignUnroll;
   bool bad = false;
-  for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
-    const int v = __ldg(ids + r);
-    if (v >= 0 && v < E) atomicAdd(&hist[v], 1);
-    else bad = true;
+  for (int rb = r0 + threadIdx.x; rb < r1; rb += step) {
+    int v[kAlignUnroll];
+#pragma unroll
+    for (int i = 0; i < kAlignUnroll; ++i) {
+      const int r = rb + i * blockDim.x;
+      v[i] = (r < r1) ? __ldg(ids + r) : 0;
+    }
+#pragma unroll
+    for (int i = 0; i < kAlignUnroll; ++i) {
+      if (rb + i * (int)blockDim.x >= r1) continue;  // past the range
+      if (v[i] >= 0 && v[i] < E) atomicAdd(&hist[v[i]], 1);
+      else bad = true;
+    }
   }
   if (bad && !ignore_invalid) set_status(status, OES_DEV_BAD_ID);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) ws.cnt[(size_t)g * E + e] = hist[e];
 }
 
-__global__ void __launch_bounds__(1024)
-    align_scan_kernel(int G, int E, int B, AlignWs ws, int32_t* __restrict__ n_post_pad,
-                      int32_t* __restrict__ zero, int nzero) {
+// CTA c: experts [32c, 32c + 32).  Bands of up to kScanRows rows of the
+// [G x 32] tile of per-CTA counts are loaded into shared memory at once (row
+// stride 33: no bank conflicts); in a band, warp w sums its rows for the 32
+// experts (lane = expert), the warps' sums are scanned, and each warp writes
+// its rows' exclusive prefixes back, carrying the band's total to the next.
+constexpr int kScanWarps = 32;
+constexpr int kScanRows = 1024;
+__global__ void __launch_bounds__(32 * kScanWarps)
+    align_colscan_kernel(int G, int E, AlignWs ws) {
   pdl_begin();
-  extern __shared__ int32_t padded[];  // [E]
-  __shared__ int warp_tot[32];
-  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, w = tid >> 5;
-  for (int i = tid; i < nzero; i += nt) zero[i] = 0;
-  // column totals: the loads of a batch are issued together (one round
-  // trip per kScanBatch CTAs instead of one per CTA)
-  for (int e = tid; e < E; e += nt) {
-    int run = 0;
-    for (int g0 = 0; g0 < G; g0 += kScanBatch) {
-      int c[kScanBatch];
-#pragma unroll
-      for (int j = 0; j < kScanBatch; ++j) c[j] = (g0 + j < G) ? ws.cnt[(size_t)(g0 + j) * E + e] : 0;
-#pragma unroll
-      for (int j = 0; j < kScanBatch; ++j) run += c[j];
+  extern __shared__ int32_t tile[];  // [min(G, kScanRows)][33]
+  __shared__ int32_t band[kScanWarps][33];
+  const int c0 = blockIdx.x * 32;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  int carry = 0;  // this lane's expert: routes in the bands before
+  for (int gb = 0; gb < G; gb += kScanRows) {
+    const int rows = min(kScanRows, G - gb);
+    for (int i = tid; i < rows * 32; i += blockDim.x) {
+      const int g = i >> 5, j = i & 31;
+      tile[g * 33 + j] = (c0 + j < E) ? ws.cnt[(size_t)(gb + g) * E + c0 + j] : 0;
     }
-    ws.tot[e] = run;
-    padded[e] = (run + B - 1) / B * B;
+    __syncthreads();
+    const int per = (rows + kScanWarps - 1) / kScanWarps;
+    const int g0 = min(rows, w * per), g1 = min(rows, g0 + per);
+    int sum = 0;
+    for (int g = g0; g < g1; ++g) sum += tile[g * 33 + lane];
+    band[w][lane] = sum;
+    __syncthreads();
+    int run = carry;
+    for (int q = 0; q < w; ++q) run += band[q][lane];
+    for (int g = g0; g < g1; ++g) {
+      const int x = tile[g * 33 + lane];
+      if (c0 + lane < E) ws.cnt[(size_t)(gb + g) * E + c0 + lane] = run;
+      run += x;
+    }
+    for (int q = 0; q < kScanWarps; ++q) carry += band[q][lane];
+    __syncthreads();  // the tile and band are reused by the next band
   }
-  __syncthreads();
+  if (w == 0 && c0 + lane < E) ws.tot[c0 + lane] = carry;
+}
+
+// Exclusive scan of the padded expert sizes into off[] (shared memory, E <=
+// OES_MAX_EXPERTS) by one CTA; returns the padded total.  All threads call it.
+__device__ int padded_offsets(const int32_t* __restrict__ tot, int E, int B, int32_t* off,
+                              int* warp_tot) {
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, w = tid >> 5;
   const int per = (E + nt - 1) / nt;
   const int b0 = min(E, tid * per), b1 = min(E, b0 + per);
   int sum = 0;
-  for (int e = b0; e < b1; ++e) sum += padded[e];
+  for (int e = b0; e < b1; ++e) sum += (tot[e] + B - 1) / B * B;
   int incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -103,52 +153,51 @@ __global__ void __launch_bounds__(1024)
   __syncthreads();
   int run = incl - sum + (w ? warp_tot[w - 1] : 0);
   for (int e = b0; e < b1; ++e) {
-    ws.off[e] = run;
-    run += padded[e];
+    off[e] = run;
+    run += (tot[e] + B - 1) / B * B;
   }
   const int total = warp_tot[(nt >> 5) - 1];
-  if (tid == 0) {
-    *n_post_pad = total;
-    *ws.nblk = total / B;
-  }
   __syncthreads();
-  // cnt[g][e] <- offset of expert e + routes of e in CTAs before g
-  for (int e = tid; e < E; e += nt) {
-    int run = ws.off[e];
-    for (int g0 = 0; g0 < G; g0 += kScanBatch) {
-      int c[kScanBatch];
-#pragma unroll
-      for (int j = 0; j < kScanBatch; ++j) c[j] = (g0 + j < G) ? ws.cnt[(size_t)(g0 + j) * E + e] : 0;
-#pragma unroll
-      for (int j = 0; j < kScanBatch; ++j) {
-        if (g0 + j < G) ws.cnt[(size_t)(g0 + j) * E + e] = run;
-        run += c[j];
-      }
-    }
-  }
+  return total;
 }
 
 __global__ void __launch_bounds__(kAlignThreads)
     align_scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int B, int C, int G,
                          int64_t cap, AlignWs ws, int32_t* __restrict__ sorted_ids,
-                         int32_t* __restrict__ block_expert) {
+                         int32_t* __restrict__ block_expert, int32_t* __restrict__ n_post_pad,
+                         int32_t* __restrict__ zero, int nzero) {
   pdl_begin();
   extern __shared__ int32_t sm[];
+  __shared__ int warp_tot[32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int32_t* off = sm;  // [E] first position of each expert
+  const int total = padded_offsets(ws.tot, E, B, off, warp_tot);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *n_post_pad = total;
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
   if ((int)blockIdx.x < G) {
-    int32_t* wpos = sm;  // [kAlignWarps][E]
+    int32_t* wpos = sm + E;  // [kAlignWarps][E]
     const int g = blockIdx.x;
+    int nbits = 1;  // bits of the keys: experts 0..E-1, invalid lanes E..E+31
+    while ((1 << nbits) < E + 32) ++nbits;
     for (int i = threadIdx.x; i < kAlignWarps * E; i += blockDim.x) wpos[i] = 0;
     __syncthreads();
     const int seg = C / kAlignWarps;
     const int r0 = g * C + w * seg, r1 = min(R, r0 + seg);
-    for (int r = r0 + lane; r < r1; r += 32) {
-      const int v = __ldg(ids + r);
-      if (v >= 0 && v < E) atomicAdd(&wpos[w * E + v], 1);
+    for (int rb = r0 + lane; rb < r1; rb += 32 * kAlignUnroll) {
+      int v[kAlignUnroll];
+#pragma unroll
+      for (int i = 0; i < kAlignUnroll; ++i) {
+        const int r = rb + 32 * i;
+        v[i] = (r < r1) ? __ldg(ids + r) : -1;
+      }
+#pragma unroll
+      for (int i = 0; i < kAlignUnroll; ++i)
+        if (v[i] >= 0 && v[i] < E) atomicAdd(&wpos[w * E + v[i]], 1);
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-      int run = ws.cnt[(size_t)g * E + e];
+      int run = off[e] + ws.cnt[(size_t)g * E + e];
       for (int q = 0; q < kAlignWarps; ++q) {
         const int c = wpos[q * E + e];
         wpos[q * E + e] = run;
@@ -156,24 +205,29 @@ __global__ void __launch_bounds__(kAlignThreads)
       }
     }
     __syncthreads();
-    for (int rb = r0; rb < r1; rb += 32) {
-      const int r = rb + lane;
-      const int v = (r < r1) ? __ldg(ids + r) : -1;
-      const bool ok = v >= 0 && v < E;
-      const int m = ok ? v : -2 - lane;  // invalid lanes never group
-      const unsigned grp = __match_any_sync(0xffffffffu, m);
-      const int rank = __popc(grp & ((1u << lane) - 1u));
-      if (ok) sorted_ids[wpos[w * E + v] + rank] = r;
-      __syncwarp();
-      if (ok && rank == 0) wpos[w * E + v] += __popc(grp);
-      __syncwarp();
+    for (int rb = r0; rb < r1; rb += 32 * kAlignUnroll) {
+      int v[kAlignUnroll];
+#pragma unroll
+      for (int i = 0; i < kAlignUnroll; ++i) {
+        const int r = rb + 32 * i + lane;
+        v[i] = (r < r1) ? __ldg(ids + r) : -1;
+      }
+#pragma unroll
+      for (int i = 0; i < kAlignUnroll; ++i) {
+        const int r = rb + 32 * i + lane;
+        const bool ok = v[i] >= 0 && v[i] < E;
+        const int key = ok ? v[i] : E + lane;  // invalid lanes never group
+        const unsigned grp = same_key_lanes(key, nbits);
+        const int rank = __popc(grp & ((1u << lane) - 1u));
+        if (ok) sorted_ids[wpos[w * E + v[i]] + rank] = r;
+        __syncwarp();
+        if (ok && rank == 0) wpos[w * E + v[i]] += __popc(grp);
+        __syncwarp();
+      }
     }
   } else {
     // padding and block experts; one warp per block of B entries
-    int32_t* off = sm;  // [E]
-    for (int e = threadIdx.x; e < E; e += blockDim.x) off[e] = ws.off[e];
-    __syncthreads();
-    const int nblk = *ws.nblk;
+    const int nblk = total / B;
     const int64_t nb_cap = cap / B;
     const int fill_ctas = gridDim.x - G;
     const int fw = (blockIdx.x - G) * kAlignWarps + w;
@@ -365,20 +419,26 @@ int align_run(const int32_t* ids, int R, int E, int B, int ignore_invalid, int32
   ws.nblk = ws.tot + E;
 
   const size_t hist_smem = (size_t)E * 4;
-  const size_t scat_smem = (size_t)kAlignWarps * E * 4;
+  const size_t scat_smem = (size_t)(kAlignWarps + 1) * E * 4;
+  const size_t scan_smem = (size_t)std::min(G, kScanRows) * 33 * 4;
   if (scat_smem > 48 * 1024) {
     const int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(align_scatter_kernel),
                                         scat_smem, "align_scatter_kernel: shared memory limit");
     if (rc) return rc;
   }
+  if (scan_smem > 48 * 1024) {
+    const int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(align_colscan_kernel),
+                                        scan_smem, "align_colscan_kernel: shared memory limit");
+    if (rc) return rc;
+  }
   launch_kernel(align_count_kernel, G, kAlignThreads, hist_smem, stream, ids, R, E, C, ignore_invalid, ws, status);
   OES_CHECK_LAUNCH("align_count_kernel");
-  launch_kernel(align_scan_kernel, 1, 1024, hist_smem, stream, G, E, B, ws, n_post_pad, zero, nzero);
-  OES_CHECK_LAUNCH("align_scan_kernel");
+  launch_kernel(align_colscan_kernel, ceil_div(E, 32), 32 * kScanWarps, scan_smem, stream, G, E, ws);
+  OES_CHECK_LAUNCH("align_colscan_kernel");
   const int fill_ctas = (int)std::min<int64_t>(
       std::max<int64_t>(1, ceil_div64(cap / B, kAlignWarps * 4)), (int64_t)num_sms());
-  launch_kernel(align_scatter_kernel, G + fill_ctas, kAlignThreads, scat_smem, stream, 
-      ids, R, E, B, C, G, cap, ws, sorted_ids, block_expert);
+  launch_kernel(align_scatter_kernel, G + fill_ctas, kAlignThreads, scat_smem, stream,
+      ids, R, E, B, C, G, cap, ws, sorted_ids, block_expert, n_post_pad, zero, nzero);
   OES_CHECK_LAUNCH("align_scatter_kernel");
   return OES_OK;
 }

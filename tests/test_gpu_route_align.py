@@ -198,3 +198,38 @@ def test_align_edges_and_invalid_ids(R, E, B):
         assert n == on
         assert np.array_equal(s, os_) and np.array_equal(b, ob)
         assert (st == oes.OES_DEV_BAD_ID) == bad
+
+
+def _stable_sort_layout(ids: np.ndarray, E: int, B: int):
+    """The align's definition written with numpy's stable argsort: routes of
+    each expert in ascending order, each expert padded to a multiple of B with
+    the value R, block b holding its expert (-1 past the last block)."""
+    R = ids.size
+    cnt = np.bincount(ids, minlength=E).astype(np.int64)
+    padded = (cnt + B - 1) // B * B
+    off = np.concatenate([[0], np.cumsum(padded)[:-1]])
+    cap = oes.align_capacity(R, E, B)
+    s = np.full(cap, R, dtype=np.int32)
+    order = np.argsort(ids, kind="stable").astype(np.int32)
+    starts = np.concatenate([[0], np.cumsum(cnt)[:-1]])
+    pos = off[ids[order]] + (np.arange(R) - starts[ids[order]])
+    s[pos] = order
+    be = np.full(cap // B, -1, dtype=np.int32)
+    for e in np.nonzero(padded)[0]:
+        be[off[e] // B:(off[e] + padded[e]) // B] = e
+    return s, be, int(padded.sum())
+
+
+def test_align_large_chunk_count():
+    """2^25 + 123 routes over 600 experts: about two thousand CTA ranges, so
+    the per-CTA counts are scanned over several bands, each CTA's routes are
+    ordered in shared memory and written as runs; bit-exact against the
+    stable-sort definition."""
+    lib()
+    R, E, B = (1 << 25) + 123, 600, 64
+    ids = np.random.default_rng(21).integers(0, E, size=R).astype(np.int32)
+    s, b, n, st = gpu_align(ids, E, B)
+    ws, wb, wn = _stable_sort_layout(ids, E, B)
+    assert st == 0 and n == wn
+    assert np.array_equal(b, wb)
+    assert np.array_equal(s, ws)
