@@ -85,8 +85,31 @@ struct Unit {
 
 constexpr int kFiltered = -2;  // Unit::slot of a block another launch computes
 
+// A routing-table entry: through L2 alone (ld.global.cg) for a kernel that
+// reads the tables before its dependency wait (GEMM2, see the kernel), else
+// a plain load.
+template <bool CG>
+__device__ __forceinline__ int32_t ld_tab(const int32_t* p) { return CG ? __ldcg(p) : *p; }
+template <bool CG>
+__device__ __forceinline__ int32_t ld_tab(const uint8_t* p) { return CG ? __ldcg(p) : *p; }
+
+// Number of routes of block b (padding, value R, only at its end).
+template <bool CG>
+__device__ __forceinline__ int block_nvalid(const GemmParams& p, int b) {
+  const int32_t* s = p.sorted_ids + (int64_t)b * p.BN;
+  if (ld_tab<CG>(s + p.BN - 1) < p.R) return p.BN;
+  int lo = 0, hi = p.BN - 1;  // first index holding padding
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (ld_tab<CG>(s + mid) < p.R) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
 // Which block / tile a unit is, the slot of its expert, and how many of the
 // block's entries are real routes (padding, value R, only at the end).
+template <bool CG>
 __device__ __forceinline__ Unit unit_info(const GemmParams& p, int u, int nb) {
   // tile index fastest (after the K half): the units of one block run on
   // neighbouring CTAs at the same time, so the block's token rows (GEMM1) or
@@ -97,22 +120,11 @@ __device__ __forceinline__ Unit unit_info(const GemmParams& p, int u, int nb) {
   t.b = u / upb;
   t.m = (u % upb) / p.ks;
   t.h = (u % upb) % p.ks;
-  const int e = p.block_expert[t.b];
+  const int e = ld_tab<CG>(p.block_expert + t.b);
   const bool valid_e = e >= 0 && e < p.E;
-  const bool filtered = p.filter && valid_e && p.flags[e] != p.filter;
-  t.slot = filtered ? kFiltered : (valid_e ? p.e2s[e] : -1);
-  const int32_t* s = p.sorted_ids + (int64_t)t.b * p.BN;
-  if (s[p.BN - 1] < p.R) {
-    t.nvalid = p.BN;
-  } else {
-    int lo = 0, hi = p.BN - 1;  // first index holding padding
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (s[mid] < p.R) lo = mid + 1;
-      else hi = mid;
-    }
-    t.nvalid = lo;
-  }
+  const bool filtered = p.filter && valid_e && ld_tab<CG>(p.flags + e) != p.filter;
+  t.slot = filtered ? kFiltered : (valid_e ? ld_tab<CG>(p.e2s + e) : -1);
+  t.nvalid = block_nvalid<CG>(p, t.b);
   t.skip = t.slot < 0 || t.slot >= p.S || t.nvalid == 0;
   return t;
 }
@@ -129,18 +141,6 @@ struct UnitRec {  // shared-memory copy of a Unit; m holds tile * ks + K half
   int b, m, slot, nvalid;
 };
 
-// Number of routes of block b (padding, value R, only at its end).
-__device__ __forceinline__ int block_nvalid(const GemmParams& p, int b) {
-  const int32_t* s = p.sorted_ids + (int64_t)b * p.BN;
-  if (s[p.BN - 1] < p.R) return p.BN;
-  int lo = 0, hi = p.BN - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (s[mid] < p.R) lo = mid + 1;
-    else hi = mid;
-  }
-  return lo;
-}
 
 // A filtered launch deals out only the units of the selected blocks, densely,
 // so that its CTAs get equal shares: the selected block of rank g (blocks in
@@ -150,16 +150,29 @@ __device__ __forceinline__ int block_nvalid(const GemmParams& p, int b) {
 // same ranks.  Returns the number of units, or -1 when this CTA's share would
 // not fit the table (the caller then numbers units as an unfiltered launch and
 // skips the filtered ones).  All threads of the CTA call it.
+template <bool CG>
 __device__ int fill_filtered_units(const GemmParams& p, int nb, UnitRec* utab, int* s_scan) {
   const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5;
   const int nw = nthr >> 5;
   auto selected = [&](int b) {
-    const int e = p.block_expert[b];
-    return e >= 0 && e < p.E && p.flags[e] == p.filter && p.sorted_ids[(int64_t)b * p.BN] < p.R;
+    const int e = ld_tab<CG>(p.block_expert + b);
+    return e >= 0 && e < p.E && ld_tab<CG>(p.flags + e) == p.filter &&
+           ld_tab<CG>(p.sorted_ids + (int64_t)b * p.BN) < p.R;
   };
   if (nb <= nthr) {
-    // one block per thread: count and rank from one round of loads
-    const bool sel = tid < nb && selected(tid);
+    // one block per thread: its expert and its ids, then the expert's group
+    // and slot, two rounds of independent loads
+    bool sel = false;
+    int nvalid = 0, slot = -1;
+    if (tid < nb) {
+      const int e = ld_tab<CG>(p.block_expert + tid);
+      nvalid = block_nvalid<CG>(p, tid);
+      if (e >= 0 && e < p.E) {
+        const int f = ld_tab<CG>(p.flags + e);
+        slot = ld_tab<CG>(p.e2s + e);
+        sel = f == p.filter && nvalid > 0;
+      }
+    }
     const unsigned bal = __ballot_sync(0xffffffffu, sel);
     if (lane == 0) s_scan[warp] = __popc(bal);
     __syncthreads();
@@ -173,8 +186,6 @@ __device__ int fill_filtered_units(const GemmParams& p, int nb, UnitRec* utab, i
     if (units > kMaxUnitsPerCta * (int)gridDim.x) return -1;
     if (sel) {
       const int g = off + __popc(bal & ((1u << lane) - 1u));
-      const int nvalid = block_nvalid(p, tid);
-      const int slot = p.e2s[p.block_expert[tid]];
       for (int m = 0; m < upb; ++m) {
         const int v = g * upb + m;
         if (v % (int)gridDim.x == (int)blockIdx.x) utab[v / gridDim.x] = UnitRec{tid, m, slot, nvalid};
@@ -212,8 +223,8 @@ __device__ int fill_filtered_units(const GemmParams& p, int nb, UnitRec* utab, i
     }
     if (sel) {
       const int g = off + __popc(bal & ((1u << lane) - 1u));
-      const int nvalid = block_nvalid(p, b);
-      const int slot = p.e2s[p.block_expert[b]];
+      const int nvalid = block_nvalid<CG>(p, b);
+      const int slot = ld_tab<CG>(p.e2s + ld_tab<CG>(p.block_expert + b));
       for (int m = 0; m < upb; ++m) {
         const int v = g * upb + m;
         if (v % (int)gridDim.x == (int)blockIdx.x) utab[v / gridDim.x] = UnitRec{b, m, slot, nvalid};
@@ -227,6 +238,7 @@ __device__ int fill_filtered_units(const GemmParams& p, int nb, UnitRec* utab, i
 
 // The CTA's u-th unit (u counted in this CTA's sequence), from the table
 // filled at kernel start, or computed directly past the table's end.
+template <bool CG>
 __device__ __forceinline__ Unit my_unit(const GemmParams& p, const UnitRec* tab, int idx, int u, int nb) {
   if (idx < kMaxUnitsPerCta) {
     const UnitRec r = tab[idx];
@@ -239,7 +251,7 @@ __device__ __forceinline__ Unit my_unit(const GemmParams& p, const UnitRec* tab,
     t.skip = t.slot < 0 || t.slot >= p.S || t.nvalid == 0;
     return t;
   }
-  return unit_info(p, u, nb);
+  return unit_info<CG>(p, u, nb);
 }
 
 __device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
@@ -391,9 +403,6 @@ __device__ __forceinline__ void store_h(const GemmParams& p, const Unit& t, int 
 template <int MODE, int WF>
 __global__ void __launch_bounds__(gemm_threads(WF), 1)
     grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
-  pdl_wait();
-  // a filtered launch over a group with no experts has nothing to do
-  if (p.filter && p.gcount && p.gcount[p.filter] == 0) return;
   constexpr int kA = (MODE == 1) ? 2 : 1;  // weight tiles per stage (gate + up, or w2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
@@ -416,28 +425,8 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
   UnitRec* utab = reinterpret_cast<UnitRec*>(tmem_holder + 4);  // [kMaxUnitsPerCta]
 
-  const int nb = *p.n_post_pad / p.BN;
-  int total = nb * p.n_mtiles * p.ks;
-  const uint32_t acc_cols = (MODE == 1) ? 2 * p.BN : p.BN;
-  __shared__ int s_scan[33];
-  const int dense = p.filter ? fill_filtered_units(p, nb, utab, s_scan) : -1;
-  if (dense >= 0) {
-    total = dense;
-  } else {
-    // every thread looks up one of this CTA's units (independent loads in
-    // parallel), so the roles below never wait on global memory for them
-    for (int i = threadIdx.x; i < kMaxUnitsPerCta; i += blockDim.x) {
-      const int u = blockIdx.x + i * gridDim.x;
-      if (u >= total) break;
-      const Unit t = unit_info(p, u, nb);
-      utab[i] = UnitRec{t.b, t.m * p.ks + t.h, t.slot, t.nvalid};
-    }
-  }
-  __syncthreads();
-  // a CTA without units leaves before it sets up barriers or takes TMEM
-  // (a small or filtered launch leaves most CTAs idle)
-  if ((int)blockIdx.x >= total) return;
-
+  // set-up that reads and writes no global memory runs before the wait for
+  // the previous kernel: barrier initialisation and the tensor-map prefetch
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
@@ -465,6 +454,39 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
       tma_prefetch_desc(&maps.a);
     }
   }
+  // GEMM1 waits here for the kernels before it.  GEMM2 is launched while
+  // GEMM1 runs (GEMM1 releases it after its set-up): everything GEMM2 reads
+  // but h -- the routing tables, the groups, the slot map and the weights --
+  // was complete before GEMM1 passed this wait, so GEMM2 builds its unit
+  // table, takes TMEM and streams its first weight stages now, and only the
+  // h producer waits for GEMM1 to complete.  Its table reads go to L2
+  // (ld.global.cg), not to a possibly stale L1 line.
+  if (MODE == 1) pdl_wait();
+  // a filtered launch over a group with no experts has nothing to do
+  if (p.filter && p.gcount && ld_tab<MODE == 2>(p.gcount + p.filter) == 0) return;
+
+  const int nb = ld_tab<MODE == 2>(p.n_post_pad) / p.BN;
+  int total = nb * p.n_mtiles * p.ks;
+  const uint32_t acc_cols = (MODE == 1) ? 2 * p.BN : p.BN;
+  __shared__ int s_scan[33];
+  const int dense = p.filter ? fill_filtered_units<MODE == 2>(p, nb, utab, s_scan) : -1;
+  if (dense >= 0) {
+    total = dense;
+  } else {
+    // every thread looks up one of this CTA's units (independent loads in
+    // parallel), so the roles below never wait on global memory for them
+    for (int i = threadIdx.x; i < kMaxUnitsPerCta; i += blockDim.x) {
+      const int u = blockIdx.x + i * gridDim.x;
+      if (u >= total) break;
+      const Unit t = unit_info<MODE == 2>(p, u, nb);
+      utab[i] = UnitRec{t.b, t.m * p.ks + t.h, t.slot, t.nvalid};
+    }
+  }
+  __syncthreads();
+  // a CTA without units leaves before it takes TMEM (a small or filtered
+  // launch leaves most CTAs idle)
+  if ((int)blockIdx.x >= total) return;
+
   if (warp == 2) {
     tmem_alloc(tmem_holder, p.tmem_cols);
     tmem_relinquish();
@@ -473,6 +495,12 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // A GEMM1 of at most two units a CTA lets GEMM2, the next kernel on its
+  // stream, launch now: GEMM2's CTAs take the SMs this launch leaves idle or
+  // frees and set up while it runs (see the wait above).  A longer GEMM1
+  // does not: CTAs of GEMM2 resident early would hold the SMs its CTAs free
+  // against kernels of other streams that have work before GEMM2 can start.
+  if (MODE == 1 && total <= 2 * (int)gridDim.x) pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -480,7 +508,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
       int s = 0, ph = 0, r = 0, rph = 0;
       bool ok = true;
       for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
-        const Unit t = my_unit(p, utab, ui, u, nb);
+        const Unit t = my_unit<MODE == 2>(p, utab, ui, u, nb);
         if (t.skip) continue;
         const int row0 = t.m * kTileM;
         for (int kc = kc_lo(p, t), ke = kc_hi(p, t); kc < ke && ok; ++kc) {
@@ -520,7 +548,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
       int a = 0;
       bool ok = true;
       for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
-        const Unit t = my_unit(p, utab, ui, u, nb);
+        const Unit t = my_unit<MODE == 2>(p, utab, ui, u, nb);
         if (t.skip) continue;
         const uint32_t N = round16(t.nvalid);
         const uint32_t idesc = idesc_f16(WF ? 0u : 1u, kTileM, N);
@@ -557,10 +585,11 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
   } else if (warp == 3) {
     // ------------------------------------------------ h producer (GEMM2)
     if (MODE == 2 && lane == 0) {
+      pdl_wait();  // h is GEMM1's output
       int s = 0, ph = 0;
       bool ok = true;
       for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
-        const Unit t = my_unit(p, utab, ui, u, nb);
+        const Unit t = my_unit<MODE == 2>(p, utab, ui, u, nb);
         if (t.skip) continue;
         for (int kc = kc_lo(p, t), ke = kc_hi(p, t); kc < ke; ++kc) {
           ok = mbar_wait(&empty[s], ph ^ 1, p.status);
@@ -583,7 +612,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
       int s = 0, ph = 0;
       bool ok = true;
       for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
-        const Unit t = my_unit(p, utab, ui, u, nb);
+        const Unit t = my_unit<MODE == 2>(p, utab, ui, u, nb);
         if (t.skip) continue;
         const int N = round16(t.nvalid);
         int64_t src_off[8];
@@ -618,7 +647,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
     int a = 0;
     bool ok = true;
     for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
-      const Unit t = my_unit(p, utab, ui, u, nb);
+      const Unit t = my_unit<MODE == 2>(p, utab, ui, u, nb);
       if (t.skip) {
         if (MODE == 2 && t.nvalid > 0 && t.slot != kFiltered) {
           // an expert without a slot: its routes get zeros (and a status bit)
@@ -738,7 +767,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
     const int c_begin = (MODE == 1) ? 0 : (ct >> 7) * 4;
     const int c_end = (MODE == 1) ? 8 : c_begin + 4;
     for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
-      const Unit t = my_unit(p, utab, ui, u, nb);
+      const Unit t = my_unit<MODE == 2>(p, utab, ui, u, nb);
       if (t.skip) continue;
       for (int kc = kc_lo(p, t), ke = kc_hi(p, t); kc < ke; ++kc) {
         ok = mbar_wait(&rfull[r], rph, p.status) && mbar_wait(&empty[s], ph ^ 1, p.status);
@@ -787,9 +816,6 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
 template <int MODE, int WF>
 __global__ void __maxnreg__(64)
     grouped_gemm_tm_kernel(const __grid_constant__ GemmMaps maps, const GemmParams p) {
-  pdl_wait();
-  // a filtered launch over a group with no experts has nothing to do
-  if (p.filter && p.gcount && p.gcount[p.filter] == 0) return;
   constexpr int kN = 256;                  // weight rows per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
@@ -812,25 +838,8 @@ __global__ void __maxnreg__(64)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
   UnitRec* utab = reinterpret_cast<UnitRec*>(tmem_holder + 4);
 
-  const int nb = *p.n_post_pad / p.BN;
-  int total = nb * p.n_mtiles * p.ks;
-  __shared__ int s_scan[33];
-  const int dense = p.filter ? fill_filtered_units(p, nb, utab, s_scan) : -1;
-  if (dense >= 0) {
-    total = dense;
-  } else {
-    for (int i = threadIdx.x; i < kMaxUnitsPerCta; i += blockDim.x) {
-      const int u = blockIdx.x + i * gridDim.x;
-      if (u >= total) break;
-      const Unit t = unit_info(p, u, nb);
-      utab[i] = UnitRec{t.b, t.m * p.ks + t.h, t.slot, t.nvalid};
-    }
-  }
-  __syncthreads();
-  // a CTA without units leaves before it sets up barriers or takes TMEM
-  // (a small or filtered launch leaves most CTAs idle)
-  if ((int)blockIdx.x >= total) return;
-
+  // set-up that reads and writes no global memory runs before the wait for
+  // the previous kernel: barrier initialisation and the tensor-map prefetch
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
@@ -856,6 +865,29 @@ __global__ void __maxnreg__(64)
       tma_prefetch_desc(&maps.a);
     }
   }
+  pdl_wait();
+  // a filtered launch over a group with no experts has nothing to do
+  if (p.filter && p.gcount && p.gcount[p.filter] == 0) return;
+
+  const int nb = *p.n_post_pad / p.BN;
+  int total = nb * p.n_mtiles * p.ks;
+  __shared__ int s_scan[33];
+  const int dense = p.filter ? fill_filtered_units<false>(p, nb, utab, s_scan) : -1;
+  if (dense >= 0) {
+    total = dense;
+  } else {
+    for (int i = threadIdx.x; i < kMaxUnitsPerCta; i += blockDim.x) {
+      const int u = blockIdx.x + i * gridDim.x;
+      if (u >= total) break;
+      const Unit t = unit_info<false>(p, u, nb);
+      utab[i] = UnitRec{t.b, t.m * p.ks + t.h, t.slot, t.nvalid};
+    }
+  }
+  __syncthreads();
+  // a CTA without units leaves before it takes TMEM (a small or filtered
+  // launch leaves most CTAs idle)
+  if ((int)blockIdx.x >= total) return;
+
   if (warp == 2) {
     tmem_alloc(tmem_holder, p.tmem_cols);
     tmem_relinquish();
@@ -876,7 +908,7 @@ __global__ void __maxnreg__(64)
       int s = 0, ph = 0, r = 0, rph = 0;
       bool ok = true;
       for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
-        const Unit t = my_unit(p, utab, ui, u, nb);
+        const Unit t = my_unit<false>(p, utab, ui, u, nb);
         if (t.skip) continue;
         const int ra = row_a(t.m), rb = row_b(t.m);
         for (int kc = 0; kc < p.n_kc && ok; ++kc) {
@@ -912,7 +944,7 @@ __global__ void __maxnreg__(64)
       bool ok = true;
       const uint32_t idesc = idesc_f16(WF ? 0u : 1u, kTileM, kN);
       for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
-        const Unit t = my_unit(p, utab, ui, u, nb);
+        const Unit t = my_unit<false>(p, utab, ui, u, nb);
         if (t.skip) continue;
         ok = mbar_wait(&tempty[a], (use[a] & 1) ^ 1, p.status);
         if (!ok) break;
@@ -944,7 +976,7 @@ __global__ void __maxnreg__(64)
       int s = 0, ph = 0;
       bool ok = true;
       for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
-        const Unit t = my_unit(p, utab, ui, u, nb);
+        const Unit t = my_unit<false>(p, utab, ui, u, nb);
         if (t.skip) continue;
         for (int kc = 0; kc < p.n_kc; ++kc) {
           ok = mbar_wait(&empty[s], ph ^ 1, p.status);
@@ -964,7 +996,7 @@ __global__ void __maxnreg__(64)
       int s = 0, ph = 0;
       bool ok = true;
       for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
-        const Unit t = my_unit(p, utab, ui, u, nb);
+        const Unit t = my_unit<false>(p, utab, ui, u, nb);
         if (t.skip) continue;
         const int N = round16(t.nvalid);
         int64_t src_off[8];
@@ -999,7 +1031,7 @@ __global__ void __maxnreg__(64)
     int a = 0;
     bool ok = true;
     for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
-      const Unit t = my_unit(p, utab, ui, u, nb);
+      const Unit t = my_unit<false>(p, utab, ui, u, nb);
       const bool live = row < t.nvalid;
       if (t.skip) {
         if (MODE == 2 && live && t.slot != kFiltered) {
@@ -1095,7 +1127,7 @@ __global__ void __maxnreg__(64)
     int s = 0, ph = 0, r = 0, rph = 0, n = 0;
     bool ok = true;
     for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
-      const Unit t = my_unit(p, utab, ui, u, nb);
+      const Unit t = my_unit<false>(p, utab, ui, u, nb);
       if (t.skip) continue;
       for (int kc = 0; kc < p.n_kc; ++kc, ++n) {
         if ((n & 1) == group) {
@@ -1566,6 +1598,8 @@ int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
     g->p1.part = ws.part;
     g->p1.tcount = ws.tcount;
   }
+  g->counters = ws.tcount;
+  g->n_counters = g->split_tiles * 4;
   return OES_OK;
 }
 
@@ -1632,7 +1666,7 @@ extern "C" int moe_grouped_gemm_slots(const oes_routed_experts* v, const uint16_
   int rc = gemm_prepare(v, x, T, k, sorted_ids, block_expert, n_post_pad, B, workspace,
                         workspace_bytes, status, &g);
   if (rc) return rc;
-  const SplitCounters sc = split_counters(g);
+  const GemmCounters sc = gemm_counters(g);
   if (sc.n > 0) OES_TRY_CUDA(cudaMemsetAsync(sc.ptr, 0, (size_t)sc.n * 4, stream));
   if ((rc = gemm_prepare_x(g, stream))) return rc;
   if ((rc = gemm_run(g, 0, nullptr, nullptr, stream))) return rc;

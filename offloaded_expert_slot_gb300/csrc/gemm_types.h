@@ -49,6 +49,8 @@ struct GemmPlan {
   GemmParams p1, p2;
   bool empty, tm;
   int split_tiles;  // > 0: GEMM1 splits K over this many tiles at most
+  int32_t* counters;  // GEMM1's split counts
+  int n_counters;
   int wf, a4, T, k, H, E;
   uint16_t* y;
   const uint16_t* x;        // the chunk's x (bf16)
@@ -64,16 +66,16 @@ int gemm_prepare(const oes_routed_experts* v, const uint16_t* x, int T, int k,
                  int B, void* workspace, size_t workspace_bytes, int32_t* status, GemmPlan* plan);
 // the x kernels of a prepared GEMM (NVFP4 weights), on `stream`
 int gemm_prepare_x(const GemmPlan& plan, cudaStream_t stream);
-// The int32 words GEMM1's K split needs zeroed before the plan's first
-// gemm_run (none when it does not split); a composite call has its align
-// zero them.
-struct SplitCounters {
+// The int32 words GEMM1's K split counts in, to be zeroed before the plan's
+// first gemm_run (none when it does not split); a composite call has its
+// align zero them.
+struct GemmCounters {
   int32_t* ptr;
   int n;
 };
-inline SplitCounters split_counters(const GemmPlan& plan) {
-  if (plan.empty || plan.split_tiles <= 0) return {nullptr, 0};
-  return {plan.p1.tcount, plan.split_tiles * 4};
+inline GemmCounters gemm_counters(const GemmPlan& plan) {
+  if (plan.empty || plan.n_counters <= 0) return {nullptr, 0};
+  return {plan.counters, plan.n_counters};
 }
 // filter: 0 every block; g > 0 the blocks of experts with flags[e] == g
 int gemm_run(const GemmPlan& plan, int filter, const uint8_t* flags, const int32_t* gcount,

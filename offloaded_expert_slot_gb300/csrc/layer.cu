@@ -6,14 +6,19 @@
 // query's copies done before the next query, and then reuses the decode
 // GEMM over the slots; Problem: streaming moves all of the layer's experts
 // for every chunk.
+#include <cuda_fp16.h>
+
 #include <algorithm>
 #include <climits>
 #include <utility>
 #include <vector>
 
+#include "align_dev.cuh"
 #include "common.cuh"
+#include "ensure_dev.cuh"
 #include "gemm_types.h"
 #include "internal.h"
+#include "route_dev.cuh"
 
 namespace oes {
 namespace {
@@ -91,11 +96,9 @@ LayerWs carve_layer(void* base, const oes_layer_desc* d, int T, int k) {
 // has no such guarantee: an earlier query may evict it, and it is then a
 // miss of its own query like any other.
 
-__global__ void group_flags_kernel(const int32_t* __restrict__ distinct, int n, int E, int layer,
-                                   const int32_t* __restrict__ miss,
-                                   const int32_t* __restrict__ n_miss, int Q,
-                                   uint8_t* __restrict__ group, int32_t* __restrict__ gcount) {
-  pdl_begin();
+__device__ __forceinline__ void group_flags_cta(const int32_t* distinct, int n, int E, int layer,
+                                                const int32_t* miss, const int32_t* n_miss, int Q,
+                                                uint8_t* group, int32_t* __restrict__ gcount) {
   __shared__ int32_t cnt[kGroups];
   for (int e = threadIdx.x; e < E; e += blockDim.x) group[e] = 0;
   for (int g = threadIdx.x; g < kGroups; g += blockDim.x) cnt[g] = 0;
@@ -123,6 +126,98 @@ __global__ void group_flags_kernel(const int32_t* __restrict__ distinct, int n, 
   }
   __syncthreads();
   for (int g = threadIdx.x; g < kGroups; g += blockDim.x) gcount[g] = cnt[g];
+}
+
+__global__ void group_flags_kernel(const int32_t* __restrict__ distinct, int n, int E, int layer,
+                                   const int32_t* __restrict__ miss,
+                                   const int32_t* __restrict__ n_miss, int Q,
+                                   uint8_t* __restrict__ group, int32_t* __restrict__ gcount) {
+  pdl_begin();
+  group_flags_cta(distinct, n, E, layer, miss, n_miss, Q, group, gcount);
+}
+
+// The front of a small chunk's slot path in one launch of two CTAs (at most
+// kSmallR routes, one ensure query, E <= kFrontMaxExperts): route, distinct
+// experts, the query's ensure, the expert groups, the align and, for NVFP4
+// weights, the f16 copy of x -- the device code of the separate kernels, so
+// every table and output is the same bit for bit.  A decode step's chain of
+// six launches and two cross-stream waits becomes one launch.
+constexpr int kFrontMaxExperts = 1024;
+struct FrontArgs {
+  const float* logits;
+  int T, k, E, H, layer, record_stats, B, nzero;
+  int64_t cap;
+  CacheView c;
+  int32_t *ids, *distinct, *d_count, *miss, *n_miss, *gcount, *sorted_ids, *block_expert,
+      *n_post_pad, *zero, *status;
+  float* w;
+  uint8_t* group;
+  const uint16_t* x;  // [T, H] bf16
+  uint16_t* x16;      // [T, H] its f16 copy (NVFP4 weights), or null
+};
+
+template <int EPL>
+__global__ void __launch_bounds__(kEnsureThreads) decode_front_kernel(const FrontArgs a) {
+  pdl_begin();
+  extern __shared__ uint64_t dsm[];  // each step's own scratch, in turn
+  // what one step hands the next stays in shared memory; the global copies
+  // the later kernels read are written at the end
+  __shared__ int32_t s_ids[kSmallR];
+  __shared__ float s_w[kSmallR];
+  __shared__ int32_t s_distinct[OES_QUERY_MAX];
+  __shared__ int32_t s_miss[3 * OES_QUERY_MAX];
+  __shared__ int32_t s_dcount, s_nmiss;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
+  const int R = a.T * a.k, Lq = min(R, a.E);
+  // both CTAs route (the same routes, bit for bit); CTA 0 then asks the
+  // cache and sets the groups while CTA 1 aligns the routes and converts x
+  for (int t = warp; t < a.T; t += kEnsureThreads / 32)
+    topk_row<EPL, float>(a.logits + (size_t)t * a.E, a.E, a.k, lane, s_ids + t * a.k, s_w + t * a.k);
+  __syncthreads();
+  if (blockIdx.x == 1) {
+    align_small_cta(s_ids, R, a.E, a.B, a.cap, 1, a.sorted_ids, a.block_expert, a.n_post_pad,
+                    a.status, a.zero, a.nzero, reinterpret_cast<int32_t*>(dsm));
+    if (a.x16) {
+      const int64_t n = (int64_t)a.T * a.H;
+      for (int64_t i = tid; i < n; i += nt) {
+        const float f = __uint_as_float(static_cast<uint32_t>(a.x[i]) << 16);
+        a.x16[i] = __half_as_ushort(__float2half_rn(f));
+      }
+    }
+    return;
+  }
+  for (int i = tid; i < R; i += nt) {
+    a.ids[i] = s_ids[i];
+    a.w[i] = s_w[i];
+  }
+  for (int e = tid; e < a.E; e += nt) a.group[e] = 0;
+  distinct_cta(s_ids, R, a.E, s_distinct, &s_dcount, reinterpret_cast<uint8_t*>(dsm));
+  __syncthreads();
+  ensure_query(a.c, a.layer, s_distinct, Lq, a.record_stats, OES_TAG_NEW_CHUNK, s_miss, &s_nmiss,
+               a.status, dsm);
+  __syncthreads();
+  // the groups of one query (group_flags_cta with Q = 1): every distinct
+  // expert a hit, then each miss its part; the counts follow from D and the
+  // misses (each miss is one of the D experts)
+  const int D = s_dcount, m = min(s_nmiss, OES_QUERY_MAX);
+  const int split = Lq > kSplitIds ? miss_split(m) : m;
+  for (int i = tid; i < Lq; i += nt) {
+    const int e = s_distinct[i];
+    a.distinct[i] = e;
+    if (e >= 0 && e < a.E) a.group[e] = kGroupHit;
+  }
+  for (int i = tid; i < 3 * m; i += nt) a.miss[i] = s_miss[i];
+  for (int g = tid; g < kGroups; g += nt)
+    a.gcount[g] = g == kGroupHit ? D - m : g == kGroupMiss0 ? split : g == kGroupMiss0 + 1 ? m - split : 0;
+  if (tid == 0) {
+    *a.d_count = D;
+    *a.n_miss = s_nmiss;
+  }
+  __syncthreads();  // the hits' group bytes before the misses' overwrite them
+  for (int i = tid; i < m; i += nt) {
+    const int e = s_miss[3 * i] - a.layer * a.E;
+    if (e >= 0 && e < a.E) a.group[e] = (uint8_t)(kGroupMiss0 + (i >= split));
+  }
 }
 
 __global__ void iota_kernel(int32_t* a, int n) {
@@ -234,6 +329,75 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
   if ((rc = gemm_prepare(&v, c->x, T, k, w.sorted_ids, w.block_expert, w.n_post_pad, B, w.gemm_ws,
                          w.gemm_bytes, c->status, &g)))
     return rc;
+  if (R <= kSmallR && Q == 1 && E <= kFrontMaxExperts) {
+    // A small chunk (a decode step): the front in one launch, then the GEMM
+    // over the hits right behind it on the caller's stream; the query's
+    // copies on the side stream and each part's copied experts on the gemm
+    // stream, as below.
+    if (g.a4 && (rc = gemm_prepare_x(g, stream))) return rc;
+    const float* logits = c->logits;
+    if (!logits) {
+      if ((rc = moe_gate_logits(c->x, c->gate, T, d->H, E, w.logits, stream))) return rc;
+      logits = w.logits;
+    }
+    const GemmCounters sc = gemm_counters(g);
+    FrontArgs a{};
+    a.logits = logits;
+    a.T = T;
+    a.k = k;
+    a.E = E;
+    a.H = d->H;
+    a.layer = layer;
+    a.record_stats = record_stats;
+    a.B = B;
+    a.cap = OES_ALIGN_CAPACITY(R, E, B);
+    a.c = view_of(cache);
+    a.ids = w.ids;
+    a.w = w.w;
+    a.distinct = w.distinct;
+    a.d_count = w.d_count;
+    a.miss = miss_of(0);
+    a.n_miss = w.n_miss;
+    a.group = w.resident;
+    a.gcount = w.gcount;
+    a.sorted_ids = w.sorted_ids;
+    a.block_expert = w.block_expert;
+    a.n_post_pad = w.n_post_pad;
+    a.zero = sc.ptr;
+    a.nzero = sc.n;
+    a.status = c->status;
+    a.x = c->x;
+    a.x16 = (g.wf && !g.a4) ? g.x16 : nullptr;
+    int spad = 2;
+    while (spad < cache->S) spad <<= 1;
+    const size_t smem =
+        std::max({(size_t)E, (size_t)spad * 8, ((size_t)2 * E + (size_t)std::max(R, 1)) * 4});
+    const void* fn = E <= 512 ? reinterpret_cast<const void*>(decode_front_kernel<16>)
+                              : reinterpret_cast<const void*>(decode_front_kernel<32>);
+    if ((rc = set_max_dynamic_smem(fn, smem, "decode_front_kernel: shared memory limit"))) return rc;
+    if ((rc = prefer_max_shared_carveout(fn, "decode_front_kernel: carveout"))) return rc;
+    if (E <= 512) launch_kernel(decode_front_kernel<16>, 2, kEnsureThreads, smem, stream, a);
+    else launch_kernel(decode_front_kernel<32>, 2, kEnsureThreads, smem, stream, a);
+    OES_CHECK_LAUNCH("decode_front_kernel");
+    OES_TRY_CUDA(cudaEventRecord(cache->fork, stream));
+    const int np = Lq > kSplitIds ? 2 : 1;
+    OES_TRY_CUDA(cudaStreamWaitEvent(side, cache->fork, 0));
+    for (int p = 0; p < np; ++p) {
+      if ((rc = copy(0, np == 2 ? p : -1, side))) return rc;
+      OES_TRY_CUDA(cudaEventRecord(cache->copied[p], side));
+    }
+    OES_TRY_CUDA(cudaEventRecord(cache->join, side));
+    if ((rc = gemm_run(g, kGroupHit, w.resident, w.gcount, stream))) return rc;
+    cudaStream_t gs = cache->gemm;
+    for (int p = 0; p < np; ++p) {
+      OES_TRY_CUDA(cudaStreamWaitEvent(gs, cache->copied[p], 0));
+      if ((rc = gemm_run(g, kGroupMiss0 + p, w.resident, w.gcount, gs))) return rc;
+    }
+    OES_TRY_CUDA(cudaEventRecord(cache->gjoin, gs));
+    OES_TRY_CUDA(cudaStreamWaitEvent(stream, cache->join, 0));
+    OES_TRY_CUDA(cudaStreamWaitEvent(stream, cache->gjoin, 0));
+    return gemm_combine(g, w.ids, w.w, c->out, stream);
+  }
   // caller's stream: route, distinct experts, the first query
   if ((rc = route(d, c, w, stream))) return rc;
   OES_TRY_CUDA(cudaEventRecord(cache->routed, stream));
@@ -244,7 +408,7 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
   // while the queries are ensured
   cudaStream_t gs = cache->gemm;
   OES_TRY_CUDA(cudaStreamWaitEvent(gs, cache->routed, 0));
-  const SplitCounters sc = split_counters(g);
+  const GemmCounters sc = gemm_counters(g);
   if ((rc = align_run(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad, c->status,
                       w.align_ws, w.align_bytes, sc.ptr, sc.n, gs)))
     return rc;
@@ -343,7 +507,7 @@ extern "C" int moe_layer_forward_stream(const oes_expert_source* src, void* laye
   launch_kernel(iota_kernel, ceil_div(E, 256), 256, 0, compute_stream, w.e2s_identity, E);
   OES_CHECK_LAUNCH("iota_kernel");
   if ((rc = route(d, c, w, compute_stream))) return rc;
-  const SplitCounters sc = split_counters(g);
+  const GemmCounters sc = gemm_counters(g);
   if ((rc = align_run(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad, c->status,
                       w.align_ws, w.align_bytes, sc.ptr, sc.n, compute_stream)))
     return rc;
@@ -576,7 +740,7 @@ extern "C" int moe_layers_forward_staged(const oes_stage_plan* p, const oes_expe
       const LayerWs w = carve_layer(c->workspace, d, T, k);
       const int B = tile_plan(R, E);
       int rc = route(d, c, w, compute_stream);
-      const SplitCounters sc = split_counters(plans[i]);
+      const GemmCounters sc = gemm_counters(plans[i]);
       if (!rc)
         rc = align_run(w.ids, R, E, B, 1, w.sorted_ids, w.block_expert, w.n_post_pad, c->status,
                        w.align_ws, w.align_bytes, sc.ptr, sc.n, compute_stream);

@@ -1,0 +1,163 @@
+// Device code of the routing steps, shared by their own kernels and by the
+// fused decode step (top-k of a token by one warp, distinct experts by one
+// CTA).  FreeToken PR #676, Solution: the chunk's distinct experts are what
+// the cache is asked for.
+#pragma once
+#include "common.cuh"
+
+namespace oes {
+
+__device__ __forceinline__ float load_logit(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float load_logit(const uint16_t* p) {
+  return __uint_as_float(static_cast<uint32_t>(__ldg(p)) << 16);  // bf16 -> fp32, exact
+}
+
+// Order key of a routing logit: a larger logit has a larger key, and the
+// key order is the order the router ranks by.  NaN ranks as -inf (fmaxf
+// returns the number when one operand is NaN) and -0 as +0 (x + 0 is +0 for
+// x = -0), so that equal logits get equal keys; key 0 marks an entry that is
+// not an expert or is already taken (every logit's key is at least that of
+// -inf, 0x007FFFFF).
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  const uint32_t u = __float_as_uint(fmaxf(v, -INFINITY) + 0.0f);
+  return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// The two best entries (key, position j) of a lane's EPL keys, skipping the
+// positions set in `taken`; ties go to the lower j (strict comparisons in
+// ascending j).  Position EPL and key 0 mean none.
+template <int EPL>
+__device__ __forceinline__ void lane_top2(const uint32_t (&key)[EPL], uint32_t taken, uint32_t& k1,
+                                          int& j1, uint32_t& k2, int& j2) {
+  k1 = k2 = 0u;
+  j1 = j2 = EPL;
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    const uint32_t kj = (j < 32 && ((taken >> (j & 31)) & 1u)) ? 0u : key[j];
+    if (kj > k1) {
+      k2 = k1;
+      j2 = j1;
+      k1 = kj;
+      j1 = j;
+    } else if (kj > k2) {
+      k2 = kj;
+      j2 = j;
+    }
+  }
+}
+
+// One token's top-k by one warp.  Lane l holds the keys of experts l, l + 32, ...
+// (logits widened to fp32, bf16 exactly) and its two best.  Each of the k
+// rounds takes the warp's largest key (one redux.sync), then the lowest
+// expert id holding it (another): larger logit first, ties to the lower id.
+// Only the winning lane moves on to its next entry: its second best, or, once
+// that is used, a rescan of its keys without the taken ones (a bit mask of
+// taken positions up to 32 keys a lane; past that the key is cleared).  Lane r keeps
+// round r's winner; the weights are a softmax over the k selected logits.
+template <int EPL, typename LT>
+__device__ __forceinline__ void topk_row(const LT* __restrict__ row, int E, int k, int lane,
+                                         int32_t* __restrict__ ids_t, float* __restrict__ w_t) {
+  uint32_t key[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    const int e = lane + 32 * j;
+    key[j] = (e < E) ? logit_key(load_logit(row + e)) : 0u;
+  }
+  uint32_t k1, k2;
+  int j1, j2;
+  lane_top2<EPL>(key, 0u, k1, j1, k2, j2);
+  uint32_t taken = 0u;
+  bool have2 = true;
+  uint32_t my_k = 0u, my_e = 0u;
+  for (int r = 0; r < k; ++r) {
+    const uint32_t g = __reduce_max_sync(0xffffffffu, k1);
+    const uint32_t cand = (k1 == g) ? (uint32_t)(lane + 32 * j1) : 0xffffffffu;
+    const uint32_t we = __reduce_min_sync(0xffffffffu, cand);
+    if (lane == r) {
+      my_k = g;
+      my_e = we;
+    }
+    if (lane == (int)(we & 31u)) {
+      if (EPL <= 32) {
+        taken |= 1u << (j1 & 31);
+      } else {
+        // wider rows (more than 1024 experts) clear the taken key in place
+#pragma unroll
+        for (int j = 0; j < EPL; ++j)
+          if (j == j1) key[j] = 0u;
+      }
+      if (have2) {
+        k1 = k2;
+        j1 = j2;
+        have2 = false;
+      } else {
+        lane_top2<EPL>(key, taken, k1, j1, k2, j2);
+        have2 = true;
+      }
+    }
+  }
+  const float my_v = key_logit(my_k);
+  const float top = __shfl_sync(0xffffffffu, my_v, 0);
+  const float ex = (lane < k) ? expf(my_v - top) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane < k) {
+    ids_t[lane] = (int32_t)my_e;
+    w_t[lane] = ex / sum;
+  }
+}
+
+// The distinct experts of R routes by one CTA: presence flags over the E
+// experts in shared memory (flag: E bytes), then a block-wide exclusive scan
+// turns flags into output positions.  Plain loads of ids: the fused decode
+// step writes them in the same kernel.
+__device__ __forceinline__ void distinct_cta(const int32_t* ids, int R, int E,
+                                             int32_t* __restrict__ distinct,
+                                             int32_t* __restrict__ d_count, uint8_t* flag) {
+  __shared__ int warp_tot[32];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  for (int i = tid; i < E; i += nt) flag[i] = 0;
+  __syncthreads();
+  for (int r = tid; r < R; r += nt) {
+    const int v = ids[r];
+    if (v >= 0 && v < E) flag[v] = 1;
+  }
+  __syncthreads();
+  const int per = (E + nt - 1) / nt;
+  const int b0 = min(E, tid * per), b1 = min(E, b0 + per);
+  int cnt = 0;
+  for (int i = b0; i < b1; ++i) cnt += flag[i];
+  const int lane = tid & 31, w = tid >> 5;
+  int incl = cnt;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    const int nw = nt >> 5;
+    int s = (lane < nw) ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, s, off);
+      if (lane >= off) s += o;
+    }
+    if (lane < nw) warp_tot[lane] = s;  // inclusive per warp
+  }
+  __syncthreads();
+  int pos = incl - cnt + (w ? warp_tot[w - 1] : 0);
+  for (int i = b0; i < b1; ++i)
+    if (flag[i]) distinct[pos++] = i;
+  const int D = warp_tot[(nt >> 5) - 1];
+  const int Lq = min(R, E);
+  for (int i = D + tid; i < Lq; i += nt) distinct[i] = -1;
+  if (tid == 0) *d_count = D;
+}
+
+}  // namespace oes
