@@ -838,8 +838,29 @@ __global__ void __maxnreg__(64)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
   UnitRec* utab = reinterpret_cast<UnitRec*>(tmem_holder + 4);
 
-  // set-up that reads and writes no global memory runs before the wait for
-  // the previous kernel: barrier initialisation and the tensor-map prefetch
+  pdl_wait();
+  // a filtered launch over a group with no experts has nothing to do
+  if (p.filter && p.gcount && p.gcount[p.filter] == 0) return;
+
+  const int nb = *p.n_post_pad / p.BN;
+  int total = nb * p.n_mtiles * p.ks;
+  __shared__ int s_scan[33];
+  const int dense = p.filter ? fill_filtered_units<false>(p, nb, utab, s_scan) : -1;
+  if (dense >= 0) {
+    total = dense;
+  } else {
+    for (int i = threadIdx.x; i < kMaxUnitsPerCta; i += blockDim.x) {
+      const int u = blockIdx.x + i * gridDim.x;
+      if (u >= total) break;
+      const Unit t = unit_info<false>(p, u, nb);
+      utab[i] = UnitRec{t.b, t.m * p.ks + t.h, t.slot, t.nvalid};
+    }
+  }
+  __syncthreads();
+  // a CTA without units leaves before it sets up barriers or takes TMEM
+  // (a small or filtered launch leaves most CTAs idle)
+  if ((int)blockIdx.x >= total) return;
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
@@ -865,28 +886,6 @@ __global__ void __maxnreg__(64)
       tma_prefetch_desc(&maps.a);
     }
   }
-  pdl_wait();
-  // a filtered launch over a group with no experts has nothing to do
-  if (p.filter && p.gcount && p.gcount[p.filter] == 0) return;
-
-  const int nb = *p.n_post_pad / p.BN;
-  int total = nb * p.n_mtiles * p.ks;
-  __shared__ int s_scan[33];
-  const int dense = p.filter ? fill_filtered_units<false>(p, nb, utab, s_scan) : -1;
-  if (dense >= 0) {
-    total = dense;
-  } else {
-    for (int i = threadIdx.x; i < kMaxUnitsPerCta; i += blockDim.x) {
-      const int u = blockIdx.x + i * gridDim.x;
-      if (u >= total) break;
-      const Unit t = unit_info<false>(p, u, nb);
-      utab[i] = UnitRec{t.b, t.m * p.ks + t.h, t.slot, t.nvalid};
-    }
-  }
-  __syncthreads();
-  // a CTA without units leaves before it takes TMEM (a small or filtered
-  // launch leaves most CTAs idle)
-  if ((int)blockIdx.x >= total) return;
 
   if (warp == 2) {
     tmem_alloc(tmem_holder, p.tmem_cols);
