@@ -123,9 +123,10 @@ enum { OES_LOGITS_F32 = 0, OES_LOGITS_BF16 = 1 };
  * ties to the lower expert id; weights[t, j] = softmax over the k selected
  * logits (equal to the full softmax renormalised over the top k).
  * logits: device [T, E] of `dtype` (OES_LOGITS_F32, or OES_LOGITS_BF16 as
- * uint16_t bit patterns, widened exactly to fp32 before any comparison), not
- * NaN (-inf is allowed); ids: device [T, k] int32; weights: device [T, k]
- * fp32.  1 <= k <= min(E, OES_MAX_TOPK), E <= OES_MAX_EXPERTS. */
+ * uint16_t bit patterns, widened exactly to fp32 before any comparison); a
+ * NaN logit ranks as -inf (then by id), -0 as +0; ids: device [T, k] int32;
+ * weights: device [T, k] fp32.  1 <= k <= min(E, OES_MAX_TOPK),
+ * E <= OES_MAX_EXPERTS. */
 int moe_route_topk(const void *logits, int dtype, int T, int E, int k, int32_t *ids,
                    float *weights, oes_stream_t stream);
 
@@ -446,7 +447,12 @@ int moe_layer_workspace_views(const oes_layer_desc *layer, int T, int k, void *w
  * GEMM over each query's copied experts once they are in.  A query of more
  * than 32 ids copies its misses in two launches (the last min(n/2, 16) of
  * its n misses second), each part with its own GEMM, so that after the last
- * copy at most 16 experts' GEMM remains.  The later ensures may run before
+ * copy at most 16 experts' GEMM remains.  A chunk of one query and at most
+ * 1024 routes (a decode step) takes a shorter schedule with the same
+ * results: routing, distinct experts, the ensure, the expert groups and the
+ * align in one kernel on `stream`, the GEMM over the hits right behind it
+ * on `stream`, the copies on the side stream and the GEMM over the copied
+ * experts on the second side stream.  The later ensures may run before
  * earlier copies finish: ensure reads no pool bytes, and with the chunk
  * fitting the pool no query evicts a slot an earlier query touched, so the
  * tables, the slots written and the bytes are those of ensuring and
