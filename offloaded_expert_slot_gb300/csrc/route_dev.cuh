@@ -26,37 +26,45 @@ __device__ __forceinline__ float key_logit(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// The two best entries (key, position j) of a lane's EPL keys, skipping the
+// The three best entries (key, position j) of a lane's EPL keys, skipping the
 // positions set in `taken`; ties go to the lower j (strict comparisons in
 // ascending j).  Position EPL and key 0 mean none.
 template <int EPL>
-__device__ __forceinline__ void lane_top2(const uint32_t (&key)[EPL], uint32_t taken, uint32_t& k1,
-                                          int& j1, uint32_t& k2, int& j2) {
-  k1 = k2 = 0u;
-  j1 = j2 = EPL;
+__device__ __forceinline__ void lane_top3(const uint32_t (&key)[EPL], uint32_t taken, uint32_t (&kb)[3],
+                                          int (&jb)[3]) {
+  kb[0] = kb[1] = kb[2] = 0u;
+  jb[0] = jb[1] = jb[2] = EPL;
 #pragma unroll
   for (int j = 0; j < EPL; ++j) {
     const uint32_t kj = (j < 32 && ((taken >> (j & 31)) & 1u)) ? 0u : key[j];
-    if (kj > k1) {
-      k2 = k1;
-      j2 = j1;
-      k1 = kj;
-      j1 = j;
-    } else if (kj > k2) {
-      k2 = kj;
-      j2 = j;
+    if (kj > kb[0]) {
+      kb[2] = kb[1];
+      jb[2] = jb[1];
+      kb[1] = kb[0];
+      jb[1] = jb[0];
+      kb[0] = kj;
+      jb[0] = j;
+    } else if (kj > kb[1]) {
+      kb[2] = kb[1];
+      jb[2] = jb[1];
+      kb[1] = kj;
+      jb[1] = j;
+    } else if (kj > kb[2]) {
+      kb[2] = kj;
+      jb[2] = j;
     }
   }
 }
 
 // One token's top-k by one warp.  Lane l holds the keys of experts l, l + 32, ...
-// (logits widened to fp32, bf16 exactly) and its two best.  Each of the k
+// (logits widened to fp32, bf16 exactly) and its three best.  Each of the k
 // rounds takes the warp's largest key (one redux.sync), then the lowest
 // expert id holding it (another): larger logit first, ties to the lower id.
-// Only the winning lane moves on to its next entry: its second best, or, once
-// that is used, a rescan of its keys without the taken ones (a bit mask of
-// taken positions up to 32 keys a lane; past that the key is cleared).  Lane r keeps
-// round r's winner; the weights are a softmax over the k selected logits.
+// Only the winning lane moves on to its next entry: its next best, or, once
+// its three are used, a rescan of its keys without the taken ones (a bit
+// mask of taken positions up to 32 keys a lane; past that the key is
+// cleared).  Lane r keeps round r's winner; the weights are a softmax over
+// the k selected logits.
 template <int EPL, typename LT>
 __device__ __forceinline__ void topk_row(const LT* __restrict__ row, int E, int k, int lane,
                                          int32_t* __restrict__ ids_t, float* __restrict__ w_t) {
@@ -66,15 +74,16 @@ __device__ __forceinline__ void topk_row(const LT* __restrict__ row, int E, int 
     const int e = lane + 32 * j;
     key[j] = (e < E) ? logit_key(load_logit(row + e)) : 0u;
   }
-  uint32_t k1, k2;
-  int j1, j2;
-  lane_top2<EPL>(key, 0u, k1, j1, k2, j2);
+  // the lane's three best untaken keys; `left` of them after the first
+  uint32_t kb[3];
+  int jb[3];
+  lane_top3<EPL>(key, 0u, kb, jb);
+  int left = 2;
   uint32_t taken = 0u;
-  bool have2 = true;
   uint32_t my_k = 0u, my_e = 0u;
   for (int r = 0; r < k; ++r) {
-    const uint32_t g = __reduce_max_sync(0xffffffffu, k1);
-    const uint32_t cand = (k1 == g) ? (uint32_t)(lane + 32 * j1) : 0xffffffffu;
+    const uint32_t g = __reduce_max_sync(0xffffffffu, kb[0]);
+    const uint32_t cand = (kb[0] == g) ? (uint32_t)(lane + 32 * jb[0]) : 0xffffffffu;
     const uint32_t we = __reduce_min_sync(0xffffffffu, cand);
     if (lane == r) {
       my_k = g;
@@ -82,20 +91,22 @@ __device__ __forceinline__ void topk_row(const LT* __restrict__ row, int E, int 
     }
     if (lane == (int)(we & 31u)) {
       if (EPL <= 32) {
-        taken |= 1u << (j1 & 31);
+        taken |= 1u << (jb[0] & 31);
       } else {
         // wider rows (more than 1024 experts) clear the taken key in place
 #pragma unroll
         for (int j = 0; j < EPL; ++j)
-          if (j == j1) key[j] = 0u;
+          if (j == jb[0]) key[j] = 0u;
       }
-      if (have2) {
-        k1 = k2;
-        j1 = j2;
-        have2 = false;
+      if (left > 0) {
+        kb[0] = kb[1];
+        jb[0] = jb[1];
+        kb[1] = kb[2];
+        jb[1] = jb[2];
+        --left;
       } else {
-        lane_top2<EPL>(key, taken, k1, j1, k2, j2);
-        have2 = true;
+        lane_top3<EPL>(key, taken, kb, jb);
+        left = 2;
       }
     }
   }
