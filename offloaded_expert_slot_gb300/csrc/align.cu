@@ -7,7 +7,7 @@
 // ignore_invalid_experts).
 //
 //   count:   CTA g histograms its contiguous range of routes -> cnt[g][e]
-//            (eight loads in flight a thread)
+//            (eight 16-byte loads, 32 routes, in flight a thread)
 //   scan:    CTA c takes experts [32c, 32c + 32): its [G x 32] tile of counts
 //            in shared memory, scanned over g by all its warps at once;
 //            cnt[g][e] becomes the routes of expert e in CTAs before g, and
@@ -53,9 +53,17 @@ __device__ __forceinline__ unsigned same_key_lanes(int key, int nbits) {
   return m;
 }
 
+__device__ __forceinline__ void count_id(int v, int E, int32_t* hist, bool& bad) {
+  if (v >= 0 && v < E) atomicAdd(&hist[v], 1);
+  else bad = true;
+}
+
+// vec: ids 16-byte aligned; C is a multiple of 256, so every CTA's range
+// starts on a 16-byte boundary and is read four ids a load (32 ids in flight
+// a thread), its ragged end id by id.
 __global__ void __launch_bounds__(kAlignThreads)
     align_count_kernel(const int32_t* __restrict__ ids, int R, int E, int C, int ignore_invalid,
-                       AlignWs ws, int32_t* __restrict__ status) {
+                       int vec, AlignWs ws, int32_t* __restrict__ status) {
   pdl_begin();
   extern __shared__ int32_t hist[];
   const int g = blockIdx.x;
@@ -64,7 +72,29 @@ __global__ void __launch_bounds__(kAlignThreads)
   const int r0 = g * C, r1 = min(R, r0 + C);
   const int step = blockDim.x * kAlignUnroll;
   bool bad = false;
-  for (int rb = r0 + threadIdx.x; rb < r1; rb += step) {
+  int rs = r0;  // first id the id-by-id loop below counts
+  if (vec) {
+    const int4* v4 = reinterpret_cast<const int4*>(ids);
+    const int q0 = r0 / 4, q1 = r1 / 4;
+    for (int qb = q0 + threadIdx.x; qb < q1; qb += step) {
+      int4 v[kAlignUnroll];
+#pragma unroll
+      for (int i = 0; i < kAlignUnroll; ++i) {
+        const int q = qb + i * blockDim.x;
+        if (q < q1) v[i] = __ldg(v4 + q);
+      }
+#pragma unroll
+      for (int i = 0; i < kAlignUnroll; ++i) {
+        if (qb + i * (int)blockDim.x >= q1) continue;  // past the range
+        count_id(v[i].x, E, hist, bad);
+        count_id(v[i].y, E, hist, bad);
+        count_id(v[i].z, E, hist, bad);
+        count_id(v[i].w, E, hist, bad);
+      }
+    }
+    rs = q1 * 4;
+  }
+  for (int rb = rs + threadIdx.x; rb < r1; rb += step) {
     int v[kAlignUnroll];
 #pragma unroll
     for (int i = 0; i < kAlignUnroll; ++i) {
@@ -74,8 +104,7 @@ __global__ void __launch_bounds__(kAlignThreads)
 #pragma unroll
     for (int i = 0; i < kAlignUnroll; ++i) {
       if (rb + i * (int)blockDim.x >= r1) continue;  // past the range
-      if (v[i] >= 0 && v[i] < E) atomicAdd(&hist[v[i]], 1);
-      else bad = true;
+      count_id(v[i], E, hist, bad);
     }
   }
   if (bad && !ignore_invalid) set_status(status, OES_DEV_BAD_ID);
@@ -343,7 +372,9 @@ int align_run(const int32_t* ids, int R, int E, int B, int ignore_invalid, int32
                                         scan_smem, "align_colscan_kernel: shared memory limit");
     if (rc) return rc;
   }
-  launch_kernel(align_count_kernel, G, kAlignThreads, hist_smem, stream, ids, R, E, C, ignore_invalid, ws, status);
+  const int vec = ((uintptr_t)ids & 15) == 0 && C % 4 == 0;
+  launch_kernel(align_count_kernel, G, kAlignThreads, hist_smem, stream, ids, R, E, C, ignore_invalid,
+                vec, ws, status);
   OES_CHECK_LAUNCH("align_count_kernel");
   launch_kernel(align_colscan_kernel, ceil_div(E, 32), 32 * kScanWarps, scan_smem, stream, G, E, ws);
   OES_CHECK_LAUNCH("align_colscan_kernel");
