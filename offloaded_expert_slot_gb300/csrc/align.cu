@@ -16,9 +16,10 @@
 //            -> expert offsets; CTA g re-reads its range; each warp walks its
 //            32-route groups in order, eight groups' ids loaded at once, and
 //            places them by their rank among the group's lanes of the same
-//            expert (found with one ballot per bit of the expert id), so
-//            routes of one expert keep ascending route order (bit-exact,
-//            stable); extra CTAs write the padding and block_expert.
+//            expert (found with one ballot per bit of the expert id, the
+//            eight groups' ballots interleaved), so routes of one expert keep
+//            ascending route order (bit-exact, stable); extra CTAs write each
+//            expert's block ids and padding, and the unused tail.
 #include <algorithm>
 #include <mutex>
 
@@ -40,18 +41,6 @@ struct AlignWs {
 };
 
 constexpr int kAlignUnroll = 8;  // routes (or 32-route groups) loaded at once per thread
-
-// Lanes of the warp whose key equals this lane's, for keys below 2^nbits:
-// one ballot per bit (cheaper than a match instruction per 32 keys).
-__device__ __forceinline__ unsigned same_key_lanes(int key, int nbits) {
-  unsigned m = 0xffffffffu;
-  for (int b = 0; b < nbits; ++b) {
-    const bool bit = (key >> b) & 1;
-    const unsigned bal = __ballot_sync(0xffffffffu, bit);
-    m &= bit ? bal : ~bal;
-  }
-  return m;
-}
 
 __device__ __forceinline__ void count_id(int v, int E, int32_t* hist, bool& bad) {
   if (v >= 0 && v < E) atomicAdd(&hist[v], 1);
@@ -242,46 +231,52 @@ __global__ void __launch_bounds__(kAlignThreads)
         const int r = rb + 32 * i + lane;
         v[i] = (r < r1) ? __ldg(ids + r) : -1;
       }
+      // the same-key lanes of all eight groups, bit by bit: eight independent
+      // ballots a bit rather than one group's chain of nbits at a time
+      int key[kAlignUnroll];
+      unsigned grp[kAlignUnroll];
+#pragma unroll
+      for (int i = 0; i < kAlignUnroll; ++i) {
+        key[i] = (v[i] >= 0 && v[i] < E) ? v[i] : E + lane;  // invalid lanes never group
+        grp[i] = 0xffffffffu;
+      }
+      for (int b = 0; b < nbits; ++b) {
+#pragma unroll
+        for (int i = 0; i < kAlignUnroll; ++i) {
+          const bool bit = (key[i] >> b) & 1;
+          const unsigned bal = __ballot_sync(0xffffffffu, bit);
+          grp[i] &= bit ? bal : ~bal;
+        }
+      }
 #pragma unroll
       for (int i = 0; i < kAlignUnroll; ++i) {
         const int r = rb + 32 * i + lane;
         const bool ok = v[i] >= 0 && v[i] < E;
-        const int key = ok ? v[i] : E + lane;  // invalid lanes never group
-        const unsigned grp = same_key_lanes(key, nbits);
-        const int rank = __popc(grp & ((1u << lane) - 1u));
+        const int rank = __popc(grp[i] & ((1u << lane) - 1u));
         if (ok) sorted_ids[wpos[w * E + v[i]] + rank] = r;
         __syncwarp();
-        if (ok && rank == 0) wpos[w * E + v[i]] += __popc(grp);
+        if (ok && rank == 0) wpos[w * E + v[i]] += __popc(grp[i]);
         __syncwarp();
       }
     }
   } else {
-    // padding and block experts; one warp per block of B entries
+    // padding and block experts, expert by expert: expert e owns the blocks
+    // [off[e] / B, (off[e] + padded) / B) and pads [off[e] + tot[e],
+    // off[e] + padded) with R; past the last block, blocks get -1 and
+    // entries R up to the capacity
     const int nblk = total / B;
     const int64_t nb_cap = cap / B;
-    const int fill_ctas = gridDim.x - G;
+    const int fill_warps = (gridDim.x - G) * kAlignWarps;
     const int fw = (blockIdx.x - G) * kAlignWarps + w;
-    for (int64_t b = fw; b < nb_cap; b += (int64_t)fill_ctas * kAlignWarps) {
-      int e = -1;
-      int64_t first_pad = b * B;
-      if (b < nblk) {
-        // largest e with off[e] <= b*B
-        int lo = 0, hi = E - 1;
-        const int x = (int)(b * B);
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (off[mid] <= x) lo = mid;
-          else hi = mid - 1;
-        }
-        e = lo;
-        first_pad = (int64_t)off[e] + ws.tot[e];
-      }
-      if (lane == 0) block_expert[b] = e;
-      for (int i = lane; i < B; i += 32) {
-        const int64_t p = b * B + i;
-        if (p >= first_pad) sorted_ids[p] = R;
-      }
+    for (int e = fw; e < E; e += fill_warps) {
+      const int64_t s0 = off[e], cnt = ws.tot[e];
+      const int64_t end = s0 + (cnt + B - 1) / B * B;
+      for (int64_t b = s0 / B + lane; b < end / B; b += 32) block_expert[b] = e;
+      for (int64_t p = s0 + cnt + lane; p < end; p += 32) sorted_ids[p] = R;
     }
+    const int64_t ft = (int64_t)fw * 32 + lane, nft = (int64_t)fill_warps * 32;
+    for (int64_t b = nblk + ft; b < nb_cap; b += nft) block_expert[b] = -1;
+    for (int64_t p = (int64_t)total + ft; p < cap; p += nft) sorted_ids[p] = R;
   }
 }
 
@@ -378,8 +373,9 @@ int align_run(const int32_t* ids, int R, int E, int B, int ignore_invalid, int32
   OES_CHECK_LAUNCH("align_count_kernel");
   launch_kernel(align_colscan_kernel, ceil_div(E, 32), 32 * kScanWarps, scan_smem, stream, G, E, ws);
   OES_CHECK_LAUNCH("align_colscan_kernel");
-  const int fill_ctas = (int)std::min<int64_t>(
-      std::max<int64_t>(1, ceil_div64(cap / B, kAlignWarps * 4)), (int64_t)num_sms());
+  // fill CTAs: a warp for every four experts (the padding past the last
+  // block is at most E * (B - 1) entries)
+  const int fill_ctas = (int)std::min<int64_t>(std::max(1, ceil_div(E, kAlignWarps * 4)), (int64_t)num_sms());
   launch_kernel(align_scatter_kernel, G + fill_ctas, kAlignThreads, scat_smem, stream,
       ids, R, E, B, C, G, cap, ws, sorted_ids, block_expert, n_post_pad, zero, nzero);
   OES_CHECK_LAUNCH("align_scatter_kernel");
