@@ -29,6 +29,8 @@ __global__ void gate_logits_kernel(const uint16_t* __restrict__ x, const uint16_
   }
 }
 
+constexpr int kTopkThreads = 128;
+
 // One warp per token (topk_row).
 template <int EPL, typename LT>
 __global__ void topk_kernel(const LT* __restrict__ logits, int T, int E, int k,
@@ -38,6 +40,22 @@ __global__ void topk_kernel(const LT* __restrict__ logits, int T, int E, int k,
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps)
     topk_row<EPL, LT>(logits + (size_t)t * E, E, k, lane, ids + (size_t)t * k, weights + (size_t)t * k);
+}
+
+// One warp per token (topk_row_filtered), 16-byte loads: E a multiple of V,
+// rows 16-byte aligned, E <= 32 * V * Q.
+template <int V, int Q, typename LT>
+__global__ void __launch_bounds__(kTopkThreads)
+    topk_filtered_kernel(const LT* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
+                         float* __restrict__ weights) {
+  pdl_begin();
+  __shared__ uint2 cand[kTopkThreads / 32][32];
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  uint2* my_cand = cand[threadIdx.x >> 5];
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps)
+    topk_row_filtered<V, Q, LT>(logits + (size_t)t * E, E, k, lane, ids + (size_t)t * k,
+                                weights + (size_t)t * k, my_cand);
 }
 
 // Single CTA (distinct_cta).
@@ -70,8 +88,21 @@ namespace {
 template <typename LT>
 void launch_topk(const LT* logits, int T, int E, int k, int32_t* ids, float* weights,
                  cudaStream_t stream) {
-  const int threads = 128;
+  const int threads = kTopkThreads;
   const int blocks = (int)std::min<int64_t>(ceil_div64((int64_t)T * 32, threads), (int64_t)num_sms() * 16);
+  // the threshold filter with 16-byte loads where the rows allow them
+  constexpr int V = 16 / (int)sizeof(LT);
+  if (E <= 32 * 32 && E % V == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0) {
+    const int q = ceil_div(E, 32 * V);
+#define OES_TOPKF(Q) \
+  launch_kernel(topk_filtered_kernel<V, Q, LT>, blocks, threads, 0, stream, logits, T, E, k, ids, weights)
+    if (q <= 1) OES_TOPKF(1);
+    else if (q <= 2) OES_TOPKF(2);
+    else if (q <= 4) OES_TOPKF(4);
+    else OES_TOPKF(32 / V);
+#undef OES_TOPKF
+    return;
+  }
   const int epl = ceil_div(E, 32);
 #define OES_TOPK(N) \
   launch_kernel(topk_kernel<N, LT>, blocks, threads, 0, stream, logits, T, E, k, ids, weights)

@@ -56,6 +56,23 @@ __device__ __forceinline__ void lane_top3(const uint32_t (&key)[EPL], uint32_t t
   }
 }
 
+// Lane r < k holds the key and expert id of rank r: writes the ids and the
+// softmax over the k selected logits (a butterfly sum over the lanes in rank
+// order, so the weights depend only on the selected logits and their ranks).
+__device__ __forceinline__ void topk_write(uint32_t my_k, uint32_t my_e, int k, int lane,
+                                           int32_t* __restrict__ ids_t, float* __restrict__ w_t) {
+  const float my_v = key_logit(my_k);
+  const float top = __shfl_sync(0xffffffffu, my_v, 0);
+  const float ex = (lane < k) ? expf(my_v - top) : 0.f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane < k) {
+    ids_t[lane] = (int32_t)my_e;
+    w_t[lane] = ex / sum;
+  }
+}
+
 // One token's top-k by one warp.  Lane l holds the keys of experts l, l + 32, ...
 // (logits widened to fp32, bf16 exactly) and its three best.  Each of the k
 // rounds takes the warp's largest key (one redux.sync), then the lowest
@@ -110,16 +127,130 @@ __device__ __forceinline__ void topk_row(const LT* __restrict__ row, int E, int 
       }
     }
   }
-  const float my_v = key_logit(my_k);
-  const float top = __shfl_sync(0xffffffffu, my_v, 0);
-  const float ex = (lane < k) ? expf(my_v - top) : 0.f;
-  float sum = ex;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-  if (lane < k) {
-    ids_t[lane] = (int32_t)my_e;
-    w_t[lane] = ex / sum;
+  topk_write(my_k, my_e, k, lane, ids_t, w_t);
+}
+
+// V consecutive logits from p, widened to fp32 (bf16 exactly); V > 1 wants p
+// 16-byte aligned.
+template <int V>
+__device__ __forceinline__ void load_logits(const float* p, float* o) {
+  if constexpr (V == 4) {
+    const float4 f = __ldg(reinterpret_cast<const float4*>(p));
+    o[0] = f.x;
+    o[1] = f.y;
+    o[2] = f.z;
+    o[3] = f.w;
+  } else {
+    static_assert(V == 1, "fp32 logits: 1 or 4 a load");
+    o[0] = __ldg(p);
   }
+}
+template <int V>
+__device__ __forceinline__ void load_logits(const uint16_t* p, float* o) {
+  if constexpr (V == 8) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  } else {
+    static_assert(V == 1, "bf16 logits: 1 or 8 a load");
+    o[0] = load_logit(p);
+  }
+}
+
+// The same top-k as topk_row, by a threshold filter.  Lane l holds experts
+// V l + 32 V q + i (q < Q, i < V).  Let tau be the k-th largest of the 32
+// lane maxima: at least k logits are >= tau (those maxima), so every logit of
+// the top k is >= tau, and for random rows only a few more are.  The
+// candidates (logit >= tau) are compacted into `cand` (32 entries, this
+// warp's own) and each ranks itself against the others by (key, lower id);
+// rank r goes to lane r.  A row whose tau is -inf (fewer than k lanes with a
+// number above -inf: NaN and missing experts rank lowest) or that has more
+// than 32 candidates (many equal logits) takes topk_row instead.  Both give
+// the same ids and, through topk_write, the same weights bit for bit.
+template <int V, int Q, typename LT>
+__device__ __forceinline__ void topk_row_filtered(const LT* __restrict__ row, int E, int k, int lane,
+                                                  int32_t* __restrict__ ids_t, float* __restrict__ w_t,
+                                                  uint2* cand) {
+  constexpr int EPL = V * Q;
+  float v[EPL];
+#pragma unroll
+  for (int q = 0; q < Q; ++q) {
+    const int e0 = V * lane + 32 * V * q;
+    if (e0 + V <= E) {
+      load_logits<V>(row + e0, v + V * q);
+    } else {
+#pragma unroll
+      for (int i = 0; i < V; ++i) v[V * q + i] = __int_as_float(0x7fffffff);  // NaN: no expert
+    }
+  }
+  float m = -INFINITY;  // fmaxf skips NaN
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) m = fmaxf(m, v[j]);
+  // tau: take the largest lane maximum k times, counting equal ones at once
+  uint32_t u = __float_as_uint(m);
+  u ^= (uint32_t)((int32_t)u >> 31) | 0x80000000u;
+  int need = k;
+  uint32_t tk;
+  for (;;) {
+    const uint32_t g = __reduce_max_sync(0xffffffffu, u);
+    const int c = __popc(__ballot_sync(0xffffffffu, u == g));
+    if (c >= need) {
+      tk = g;
+      break;
+    }
+    need -= c;
+    if (u == g) u = 0u;
+  }
+  int n = 0, N = 33;
+  float tau = INFINITY;
+  if (tk > 0x007FFFFFu) {  // tau above -inf
+    tau = key_logit(tk);
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) n += (v[j] >= tau);
+    N = __reduce_add_sync(0xffffffffu, (uint32_t)n);
+  }
+  if (N > 32) {
+    topk_row<EPL, LT>(row, E, k, lane, ids_t, w_t);
+    return;
+  }
+  int pos = n;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, pos, off);
+    if (lane >= off) pos += o;
+  }
+  pos -= n;
+  __syncwarp();  // the previous row's reads of cand are done
+#pragma unroll
+  for (int q = 0; q < Q; ++q)
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+      if (v[V * q + i] >= tau) cand[pos++] = make_uint2(__float_as_uint(v[V * q + i]), V * lane + 32 * V * q + i);
+  __syncwarp();
+  uint32_t ck = 0u, ce = 0u;
+  uint64_t pk = 0u;
+  if (lane < N) {
+    const uint2 c = cand[lane];
+    ck = logit_key(__uint_as_float(c.x));
+    ce = c.y;
+    pk = ((uint64_t)ck << 32) | (uint32_t)~ce;  // larger key first, then the lower id
+  }
+  int r = 0;
+  for (int c = 0; c < N; ++c) r += (__shfl_sync(0xffffffffu, pk, c) > pk);
+  __syncwarp();
+  if (lane < N && r < k) cand[r] = make_uint2(ck, ce);
+  __syncwarp();
+  uint32_t my_k = 0u, my_e = 0u;
+  if (lane < k) {
+    const uint2 c = cand[lane];
+    my_k = c.x;
+    my_e = c.y;
+  }
+  topk_write(my_k, my_e, k, lane, ids_t, w_t);
 }
 
 // The distinct experts of R routes by one CTA: presence flags over the E

@@ -48,8 +48,8 @@ def test_topk_ties_and_wide_experts():
 
 def test_topk_signed_zeros_infinities_and_k16():
     """The per-logit ordering the kernel keys on: -0 ties with +0 (lower id
-    first), -inf ranks below every finite logit and gets weight 0; and k = 16,
-    the largest k of the candidate-filter path, on 512 and 33 experts."""
+    first), -inf ranks below every finite logit and gets weight 0; and k = 16
+    on 512 and 33 experts."""
     lib()
     g = np.random.default_rng(12)
     for E, k in [(512, 10), (512, 16), (33, 16), (33, 3)]:
@@ -109,6 +109,74 @@ def test_topk_bf16_logits():
         wide = (bits.astype(np.uint32) << 16).view(np.float32)
         fi, fw = gpu_route(wide, k)
         assert np.array_equal(gi, fi) and np.array_equal(gw.view(np.uint32), fw.view(np.uint32))
+
+
+def _filter_rows(g, E, k, V, n_rand):
+    """Rows around the threshold filter's edges for a lane layout of V logits a
+    load: c copies of the top value spread over distinct lanes (c candidates
+    exactly once c >= k: 31, 32 fit, 33 and 40 take the fallback), fewer than k
+    copies, one lane's entries all equal, -inf below k finite lanes, signed
+    zeros at the threshold, then random rows whose ties straddle it."""
+    rows = []
+    spread = lambda c: (V * (np.arange(c) % 32) + 32 * V * (np.arange(c) // 32)) % E
+    for c in (1, k - 1, k, k + 1, 31, 32, 33, 40):
+        r = np.minimum(g.standard_normal(E), 1.0).astype(np.float32)
+        r[spread(c)] = 3.5
+        rows.append(r)
+    r = np.minimum(g.standard_normal(E), 1.0).astype(np.float32)
+    lane0 = (np.arange(E) // V) % 32 == 0
+    r[lane0] = 2.0
+    rows.append(r)
+    r = np.full(E, -np.inf, np.float32)
+    r[spread(k - 1)] = g.standard_normal(k - 1)
+    rows.append(r)
+    r = np.minimum(g.standard_normal(E), -1.0).astype(np.float32)
+    r[spread(2 * k)] = np.where(np.arange(2 * k) % 2, 0.0, -0.0)
+    rows.append(r)
+    for _ in range(n_rand):
+        r = np.minimum(g.standard_normal(E), 1.0).astype(np.float32)
+        for val, hi in ((3.0, k + 2), (2.0, 40), (1.5, 40)):
+            r[g.choice(E, g.integers(0, min(hi, E)), replace=False)] = val
+        if g.random() < 0.2:
+            r[g.random(E) < 0.1] = np.nan
+        rows.append(r)
+    return np.stack(rows)
+
+
+def test_topk_threshold_filter_edges():
+    """The threshold-filter top-k (rows of at most 1024 experts, 16-byte
+    aligned, E a multiple of the load width) on rows built around its edges:
+    ids bit-exact against the oracle and weights within its bound; and the
+    same rows through an unaligned pointer, which takes the round-based
+    kernel, give the same ids and the same weights bit for bit."""
+    lib()
+    g = np.random.default_rng(15)
+    for E, k in [(512, 10), (512, 8), (512, 16), (128, 10), (200, 10), (1024, 10), (96, 20),
+                 (64, 32), (4, 2)]:
+        logits = _filter_rows(g, E, k, 4, 150)
+        T = logits.shape[0]
+        ids, w = gpu_route(logits, k)
+        oids, ow = route_topk(logits, k)
+        assert np.array_equal(ids, oids), (E, k)
+        np.testing.assert_allclose(w, ow, rtol=2e-6, atol=1e-7)
+        buf = torch.zeros(T * E + 1, dtype=torch.float32, device="cuda")
+        buf[1:] = cuda(logits).reshape(-1)
+        ui, uw = i32(T * k), f32(T * k)
+        oes.moe_route_topk(buf[1:], T, E, k, ui, uw)
+        torch.cuda.synchronize()
+        assert np.array_equal(ui.cpu().numpy().reshape(T, k), ids), (E, k)
+        assert np.array_equal(uw.cpu().numpy().view(np.uint32).reshape(T, k), w.view(np.uint32)), (E, k)
+    for E, k in [(512, 10), (256, 8), (1024, 16), (8, 2)]:
+        f = _filter_rows(g, E, k, 8, 100)
+        bits = (f.view(np.uint32) >> 16).astype(np.uint16)
+        T = bits.shape[0]
+        ids, w = i32(T * k), f32(T * k)
+        oes.moe_route_topk(bits16(bits), T, E, k, ids, w, dtype=oes.OES_LOGITS_BF16)
+        torch.cuda.synchronize()
+        gi, gw = ids.cpu().numpy().reshape(T, k), w.cpu().numpy().reshape(T, k)
+        oids, ow = route_topk_bf16(bits, k)
+        assert np.array_equal(gi, oids), (E, k)
+        np.testing.assert_allclose(gw, ow, rtol=2e-6, atol=1e-7)
 
 
 def test_gate_logits_tiny_workload():
