@@ -171,12 +171,12 @@ __global__ void __launch_bounds__(kEnsureThreads) decode_front_kernel(const Fron
   const int R = a.T * a.k, Lq = min(R, a.E);
   // both CTAs route (the same routes, bit for bit); CTA 0 then asks the
   // cache and sets the groups while CTA 1 aligns the routes and converts x
-  // (the threshold filter up to 512 experts; past that its registers beside
-  // the fallback's would spill at this kernel's 64 a thread)
+  // (the threshold filter up to 512 experts; past that its 32 logits a lane
+  // would spill at this kernel's 64 registers a thread)
   for (int t = warp; t < a.T; t += kEnsureThreads / 32) {
     if constexpr (EPL <= 16)
       topk_row_filtered<1, EPL, float>(a.logits + (size_t)t * a.E, a.E, a.k, lane, s_ids + t * a.k,
-                                       s_w + t * a.k, reinterpret_cast<uint2*>(dsm) + 32 * warp);
+                                       s_w + t * a.k, reinterpret_cast<uint2*>(dsm) + 33 * warp);
     else
       topk_row<EPL, float>(a.logits + (size_t)t * a.E, a.E, a.k, lane, s_ids + t * a.k, s_w + t * a.k);
   }
@@ -379,7 +379,7 @@ extern "C" int moe_layer_forward_slots(oes_slot_cache* cache, const oes_expert_s
     while (spad < cache->S) spad <<= 1;
     const size_t smem =
         std::max({(size_t)E, (size_t)spad * 8, ((size_t)2 * E + (size_t)std::max(R, 1)) * 4,
-                  (size_t)kEnsureThreads * sizeof(uint2)});
+                  (size_t)kEnsureThreads / 32 * 33 * sizeof(uint2)});
     const void* fn = E <= 512 ? reinterpret_cast<const void*>(decode_front_kernel<16>)
                               : reinterpret_cast<const void*>(decode_front_kernel<32>);
     if ((rc = set_max_dynamic_smem(fn, smem, "decode_front_kernel: shared memory limit"))) return rc;

@@ -43,13 +43,15 @@ __global__ void topk_kernel(const LT* __restrict__ logits, int T, int E, int k,
 }
 
 // One warp per token (topk_row_filtered), 16-byte loads: E a multiple of V,
-// rows 16-byte aligned, E <= 32 * V * Q.
+// rows 16-byte aligned, E <= 32 * V * Q.  Up to 16 logits a lane the kernel
+// fits 48 registers a thread without spilling, so that ten CTAs (40 warps)
+// share an SM.
 template <int V, int Q, typename LT>
-__global__ void __launch_bounds__(kTopkThreads)
+__global__ void __launch_bounds__(kTopkThreads, V * Q <= 16 ? 10 : 1)
     topk_filtered_kernel(const LT* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
                          float* __restrict__ weights) {
   pdl_begin();
-  __shared__ uint2 cand[kTopkThreads / 32][32];
+  __shared__ uint2 cand[kTopkThreads / 32][33];
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   uint2* my_cand = cand[threadIdx.x >> 5];
@@ -85,17 +87,32 @@ extern "C" int moe_gate_logits(const uint16_t* x, const uint16_t* gate, int T, i
 }
 
 namespace {
+// One wave: as many CTAs as fit on the SMs at once (the kernel loops over
+// tokens), at most one warp a token.
+template <auto Kernel>
+int topk_grid(int T) {
+  static const int per_sm = [] {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, Kernel, kTopkThreads, 0) != cudaSuccess || n < 1) {
+      (void)cudaGetLastError();
+      n = 1;
+    }
+    return n;
+  }();
+  return (int)std::min<int64_t>(ceil_div64((int64_t)T * 32, kTopkThreads), (int64_t)num_sms() * per_sm);
+}
+
 template <typename LT>
 void launch_topk(const LT* logits, int T, int E, int k, int32_t* ids, float* weights,
                  cudaStream_t stream) {
   const int threads = kTopkThreads;
-  const int blocks = (int)std::min<int64_t>(ceil_div64((int64_t)T * 32, threads), (int64_t)num_sms() * 16);
   // the threshold filter with 16-byte loads where the rows allow them
   constexpr int V = 16 / (int)sizeof(LT);
   if (E <= 32 * 32 && E % V == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0) {
     const int q = ceil_div(E, 32 * V);
-#define OES_TOPKF(Q) \
-  launch_kernel(topk_filtered_kernel<V, Q, LT>, blocks, threads, 0, stream, logits, T, E, k, ids, weights)
+#define OES_TOPKF(Q)                                                                                   \
+  launch_kernel(topk_filtered_kernel<V, Q, LT>, topk_grid<topk_filtered_kernel<V, Q, LT>>(T), threads, 0, \
+                stream, logits, T, E, k, ids, weights)
     if (q <= 1) OES_TOPKF(1);
     else if (q <= 2) OES_TOPKF(2);
     else if (q <= 4) OES_TOPKF(4);
@@ -104,8 +121,9 @@ void launch_topk(const LT* logits, int T, int E, int k, int32_t* ids, float* wei
     return;
   }
   const int epl = ceil_div(E, 32);
-#define OES_TOPK(N) \
-  launch_kernel(topk_kernel<N, LT>, blocks, threads, 0, stream, logits, T, E, k, ids, weights)
+#define OES_TOPK(N)                                                                             \
+  launch_kernel(topk_kernel<N, LT>, topk_grid<topk_kernel<N, LT>>(T), threads, 0, stream, logits, T, E, \
+                k, ids, weights)
   if (epl <= 1) OES_TOPK(1);
   else if (epl <= 2) OES_TOPK(2);
   else if (epl <= 4) OES_TOPK(4);

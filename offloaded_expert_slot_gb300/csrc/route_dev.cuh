@@ -73,8 +73,9 @@ __device__ __forceinline__ void topk_write(uint32_t my_k, uint32_t my_e, int k, 
   }
 }
 
-// One token's top-k by one warp.  Lane l holds the keys of experts l, l + 32, ...
-// (logits widened to fp32, bf16 exactly) and its three best.  Each of the k
+// One token's top-k by one warp, in rounds.  Lane l holds the keys of its
+// experts (topk_row: l, l + 32, ...; logits widened to fp32, bf16 exactly)
+// and its three best.  Each of the k
 // rounds takes the warp's largest key (one redux.sync), then the lowest
 // expert id holding it (another): larger logit first, ties to the lower id.
 // Only the winning lane moves on to its next entry: its next best, or, once
@@ -82,15 +83,17 @@ __device__ __forceinline__ void topk_write(uint32_t my_k, uint32_t my_e, int k, 
 // mask of taken positions up to 32 keys a lane; past that the key is
 // cleared).  Lane r keeps round r's winner; the weights are a softmax over
 // the k selected logits.
-template <int EPL, typename LT>
-__device__ __forceinline__ void topk_row(const LT* __restrict__ row, int E, int k, int lane,
-                                         int32_t* __restrict__ ids_t, float* __restrict__ w_t) {
-  uint32_t key[EPL];
-#pragma unroll
-  for (int j = 0; j < EPL; ++j) {
-    const int e = lane + 32 * j;
-    key[j] = (e < E) ? logit_key(load_logit(row + e)) : 0u;
-  }
+// Expert id of a lane's j-th key when each lane holds V consecutive experts
+// of every 32 V: V lane + 32 V (j / V) + j % V (lane + 32 j for V = 1),
+// increasing in j, so the lower j of a lane is the lower id.
+template <int V>
+__device__ __forceinline__ uint32_t lane_expert(int lane, int j) {
+  return (uint32_t)(V * lane + 32 * V * (j / V) + j % V);
+}
+
+template <int EPL, int V>
+__device__ __forceinline__ void topk_rounds(uint32_t (&key)[EPL], int k, int lane, int32_t* __restrict__ ids_t,
+                                            float* __restrict__ w_t) {
   // the lane's three best untaken keys; `left` of them after the first
   uint32_t kb[3];
   int jb[3];
@@ -100,13 +103,13 @@ __device__ __forceinline__ void topk_row(const LT* __restrict__ row, int E, int 
   uint32_t my_k = 0u, my_e = 0u;
   for (int r = 0; r < k; ++r) {
     const uint32_t g = __reduce_max_sync(0xffffffffu, kb[0]);
-    const uint32_t cand = (kb[0] == g) ? (uint32_t)(lane + 32 * jb[0]) : 0xffffffffu;
+    const uint32_t cand = (kb[0] == g) ? lane_expert<V>(lane, jb[0]) : 0xffffffffu;
     const uint32_t we = __reduce_min_sync(0xffffffffu, cand);
     if (lane == r) {
       my_k = g;
       my_e = we;
     }
-    if (lane == (int)(we & 31u)) {
+    if (lane == (int)((we / V) & 31u)) {  // the lane holding expert we
       if (EPL <= 32) {
         taken |= 1u << (jb[0] & 31);
       } else {
@@ -128,6 +131,18 @@ __device__ __forceinline__ void topk_row(const LT* __restrict__ row, int E, int 
     }
   }
   topk_write(my_k, my_e, k, lane, ids_t, w_t);
+}
+
+template <int EPL, typename LT>
+__device__ __forceinline__ void topk_row(const LT* __restrict__ row, int E, int k, int lane,
+                                         int32_t* __restrict__ ids_t, float* __restrict__ w_t) {
+  uint32_t key[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    const int e = lane + 32 * j;
+    key[j] = (e < E) ? logit_key(load_logit(row + e)) : 0u;
+  }
+  topk_rounds<EPL, 1>(key, k, lane, ids_t, w_t);
 }
 
 // V consecutive logits from p, widened to fp32 (bf16 exactly); V > 1 wants p
@@ -163,19 +178,23 @@ __device__ __forceinline__ void load_logits(const uint16_t* p, float* o) {
 
 // The same top-k as topk_row, by a threshold filter.  Lane l holds experts
 // V l + 32 V q + i (q < Q, i < V).  Let tau be the k-th largest of the 32
-// lane maxima: at least k logits are >= tau (those maxima), so every logit of
-// the top k is >= tau, and for random rows only a few more are.  The
-// candidates (logit >= tau) are compacted into `cand` (32 entries, this
-// warp's own) and each ranks itself against the others by (key, lower id);
-// rank r goes to lane r.  A row whose tau is -inf (fewer than k lanes with a
-// number above -inf: NaN and missing experts rank lowest) or that has more
-// than 32 candidates (many equal logits) takes topk_row instead.  Both give
-// the same ids and, through topk_write, the same weights bit for bit.
+// lane maxima (a bitonic sort of them): at least k logits are >= tau (those
+// maxima), so every logit of the top k is >= tau, and for random rows only a
+// few more are.  The
+// candidates (logit >= tau) go to `cand` (this warp's own 33 entries: 32
+// candidates, then the count) at positions from a shared counter, in any
+// order; each ranks itself against the others by (key, lower id) and rank r
+// goes to lane r.  A row whose tau is -inf (fewer than k lanes with a number
+// above -inf: NaN and missing experts rank lowest) or that has more than 32
+// candidates (many equal logits) is ranked in rounds over the same keys.
+// Both give the same ids and, through topk_write, the same weights bit for
+// bit.
 template <int V, int Q, typename LT>
 __device__ __forceinline__ void topk_row_filtered(const LT* __restrict__ row, int E, int k, int lane,
                                                   int32_t* __restrict__ ids_t, float* __restrict__ w_t,
                                                   uint2* cand) {
   constexpr int EPL = V * Q;
+  int* count = reinterpret_cast<int*>(cand + 32);
   float v[EPL];
 #pragma unroll
   for (int q = 0; q < Q; ++q) {
@@ -190,47 +209,45 @@ __device__ __forceinline__ void topk_row_filtered(const LT* __restrict__ row, in
   float m = -INFINITY;  // fmaxf skips NaN
 #pragma unroll
   for (int j = 0; j < EPL; ++j) m = fmaxf(m, v[j]);
-  // tau: take the largest lane maximum k times, counting equal ones at once
-  uint32_t u = __float_as_uint(m);
-  u ^= (uint32_t)((int32_t)u >> 31) | 0x80000000u;
-  int need = k;
-  uint32_t tk;
-  for (;;) {
-    const uint32_t g = __reduce_max_sync(0xffffffffu, u);
-    const int c = __popc(__ballot_sync(0xffffffffu, u == g));
-    if (c >= need) {
-      tk = g;
-      break;
-    }
-    need -= c;
-    if (u == g) u = 0u;
-  }
-  int n = 0, N = 33;
-  float tau = INFINITY;
-  if (tk > 0x007FFFFFu) {  // tau above -inf
-    tau = key_logit(tk);
+  // tau: the k-th largest lane maximum, from a bitonic sort of the 32
+  // maxima into descending order (lane i the i-th largest)
+  float srt = m;
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) n += (v[j] >= tau);
-    N = __reduce_add_sync(0xffffffffu, (uint32_t)n);
+  for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+    for (int d = size >> 1; d > 0; d >>= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, srt, d);
+      srt = (((lane & d) == 0) == ((lane & size) == 0)) ? fmaxf(srt, o) : fminf(srt, o);
+    }
+  const float tau = __shfl_sync(0xffffffffu, srt, k - 1);
+  bool rounds = tau == -INFINITY;
+  int N = 0;
+  if (!rounds) {
+    __syncwarp();  // the previous row's reads of cand are done
+    if (lane == 0) *count = 0;
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < Q; ++q)
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+        if (v[V * q + i] >= tau) {
+          const int p = atomicAdd(count, 1);
+          if (p < 32) cand[p] = make_uint2(__float_as_uint(v[V * q + i]), V * lane + 32 * V * q + i);
+        }
+    __syncwarp();
+    N = *count;
+    rounds = N > 32;
   }
-  if (N > 32) {
-    topk_row<EPL, LT>(row, E, k, lane, ids_t, w_t);
+  if (rounds) {
+    uint32_t key[EPL];
+#pragma unroll
+    for (int q = 0; q < Q; ++q)
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+        key[V * q + i] = (V * lane + 32 * V * q + V <= E) ? logit_key(v[V * q + i]) : 0u;
+    topk_rounds<EPL, V>(key, k, lane, ids_t, w_t);
     return;
   }
-  int pos = n;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(0xffffffffu, pos, off);
-    if (lane >= off) pos += o;
-  }
-  pos -= n;
-  __syncwarp();  // the previous row's reads of cand are done
-#pragma unroll
-  for (int q = 0; q < Q; ++q)
-#pragma unroll
-    for (int i = 0; i < V; ++i)
-      if (v[V * q + i] >= tau) cand[pos++] = make_uint2(__float_as_uint(v[V * q + i]), V * lane + 32 * V * q + i);
-  __syncwarp();
   uint32_t ck = 0u, ce = 0u;
   uint64_t pk = 0u;
   if (lane < N) {
