@@ -13,8 +13,8 @@
 //            cnt[g][e] becomes the routes of expert e in CTAs before g, and
 //            tot[e] the expert's routes
 //   scatter: every CTA first scans the padded expert sizes itself (E <= 4096)
-//            -> expert offsets; CTA g re-reads its range; each warp walks its
-//            32-route groups in order, eight groups' ids loaded at once, and
+//            -> expert offsets; CTA g re-reads its range; each warp counts its
+//            segment (16-byte loads), then walks its 32-route groups in order, eight groups' ids loaded at once, and
 //            places them by their rank among the group's lanes of the same
 //            expert (found with one ballot per bit of the expert id, the
 //            eight groups' ballots interleaved), so routes of one expert keep
@@ -182,7 +182,7 @@ __device__ int padded_offsets(const int32_t* __restrict__ tot, int E, int B, int
 
 __global__ void __launch_bounds__(kAlignThreads)
     align_scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int B, int C, int G,
-                         int64_t cap, AlignWs ws, int32_t* __restrict__ sorted_ids,
+                         int64_t cap, int vec, AlignWs ws, int32_t* __restrict__ sorted_ids,
                          int32_t* __restrict__ block_expert, int32_t* __restrict__ n_post_pad,
                          int32_t* __restrict__ zero, int nzero) {
   pdl_begin();
@@ -203,7 +203,31 @@ __global__ void __launch_bounds__(kAlignThreads)
     __syncthreads();
     const int seg = C / kAlignWarps;
     const int r0 = g * C + w * seg, r1 = min(R, r0 + seg);
-    for (int rb = r0 + lane; rb < r1; rb += 32 * kAlignUnroll) {
+    // the warp's counts (order does not matter here): four ids a load when
+    // the ids are 16-byte aligned (seg is a multiple of 32 routes, so r0 is
+    // a multiple of four), its ragged end id by id
+    int rs = r0;
+    if (vec) {
+      const int4* v4 = reinterpret_cast<const int4*>(ids);
+      const int q1 = r1 / 4;
+      for (int qb = r0 / 4 + lane; qb < q1; qb += 32 * kAlignUnroll) {
+        int4 v[kAlignUnroll];
+#pragma unroll
+        for (int i = 0; i < kAlignUnroll; ++i) {
+          const int q = qb + 32 * i;
+          v[i] = (q < q1) ? __ldg(v4 + q) : make_int4(-1, -1, -1, -1);
+        }
+#pragma unroll
+        for (int i = 0; i < kAlignUnroll; ++i) {
+          const int x[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (x[j] >= 0 && x[j] < E) atomicAdd(&wpos[w * E + x[j]], 1);
+        }
+      }
+      rs = max(r0, q1 * 4);
+    }
+    for (int rb = rs + lane; rb < r1; rb += 32 * kAlignUnroll) {
       int v[kAlignUnroll];
 #pragma unroll
       for (int i = 0; i < kAlignUnroll; ++i) {
@@ -291,10 +315,15 @@ __global__ void __launch_bounds__(1024)
                   zero, nzero, sm);
 }
 
-// CTA range: a multiple of 256 routes, at least 2048, about 2 CTAs per SM.
+// CTA range: a multiple of 256 routes, at least 2048, and about 8 CTAs per
+// SM (5 past 1024 experts, where each CTA's zeroing and scan of its warps'
+// counters, 8 E of them, weighs more): enough warps to cover the scatter's
+// load latency.  Measured at 2^24 routes: 201 -> 163 us over 512 experts
+// (2 CTAs per SM before), 223 -> 191 us over 2100.
 void align_geometry(int R, int E, int* G, int* C, size_t* ws_bytes) {
   const int sms = num_sms();
-  int64_t c = std::max<int64_t>(2048, ceil_div64(R, (int64_t)sms * 2));
+  const int per_sm = E <= 1024 ? 8 : 5;
+  int64_t c = std::max<int64_t>(2048, ceil_div64(R, (int64_t)sms * per_sm));
   c = (c + 255) / 256 * 256;
   *C = (int)c;
   *G = std::max(1, (int)ceil_div64(R, c));
@@ -377,7 +406,7 @@ int align_run(const int32_t* ids, int R, int E, int B, int ignore_invalid, int32
   // block is at most E * (B - 1) entries)
   const int fill_ctas = (int)std::min<int64_t>(std::max(1, ceil_div(E, kAlignWarps * 4)), (int64_t)num_sms());
   launch_kernel(align_scatter_kernel, G + fill_ctas, kAlignThreads, scat_smem, stream,
-      ids, R, E, B, C, G, cap, ws, sorted_ids, block_expert, n_post_pad, zero, nzero);
+      ids, R, E, B, C, G, cap, vec, ws, sorted_ids, block_expert, n_post_pad, zero, nzero);
   OES_CHECK_LAUNCH("align_scatter_kernel");
   return OES_OK;
 }
