@@ -118,9 +118,19 @@ __global__ void __launch_bounds__(32 * kScanWarps)
   int carry = 0;  // this lane's expert: routes in the bands before
   for (int gb = 0; gb < G; gb += kScanRows) {
     const int rows = min(kScanRows, G - gb);
-    for (int i = tid; i < rows * 32; i += blockDim.x) {
-      const int g = i >> 5, j = i & 31;
-      tile[g * 33 + j] = (c0 + j < E) ? ws.cnt[(size_t)(gb + g) * E + c0 + j] : 0;
+    // eight loads in flight a thread (the rows are independent)
+    for (int i0 = tid; i0 < rows * 32; i0 += blockDim.x * kAlignUnroll) {
+      int x[kAlignUnroll];
+#pragma unroll
+      for (int u = 0; u < kAlignUnroll; ++u) {
+        const int i = i0 + u * (int)blockDim.x, g = i >> 5, j = i & 31;
+        x[u] = (i < rows * 32 && c0 + j < E) ? ws.cnt[(size_t)(gb + g) * E + c0 + j] : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < kAlignUnroll; ++u) {
+        const int i = i0 + u * (int)blockDim.x;
+        if (i < rows * 32) tile[(i >> 5) * 33 + (i & 31)] = x[u];
+      }
     }
     __syncthreads();
     const int per = (rows + kScanWarps - 1) / kScanWarps;
