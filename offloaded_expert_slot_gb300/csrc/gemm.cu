@@ -51,6 +51,7 @@ namespace {
 constexpr int kTileM = 128;  // weight rows per MMA
 constexpr int kChunkK = 64;  // K elements per pipeline stage (128 bytes of 16-bit)
 constexpr int kConvWarps = 8;    // NVFP4 converter warps
+constexpr int kConvGroupWarps = kConvWarps / 2;  // two groups take alternate stages
 constexpr int kGatherWarps = 4;  // GEMM1 token-gather warps
 constexpr int kGatherW0 = 8;     // first gather warp
 constexpr int kMaxUnitsPerCta = 256;  // units whose info is tabled in shared memory
@@ -76,6 +77,7 @@ __host__ __device__ constexpr int gemm_threads(int wf) { return 32 * (wf ? 23 : 
 // eight that take alternate pipeline stages
 constexpr int kTmConvW0 = 12;
 constexpr int kTmConvWarps = 16;
+constexpr int kTmConvGroupWarps = kTmConvWarps / 2;  // a stage's converter arrivals
 __host__ __device__ constexpr int gemm_threads_tm(int wf) { return 32 * (wf ? kTmConvW0 + kTmConvWarps : 12); }
 
 struct Unit {
@@ -432,12 +434,12 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
     for (int s = 0; s < p.NS; ++s) {
       // arrivals per stage: the weight side (TMA producer, or the converter
       // warps) and the token side (32 gather lanes, or the h TMA producer)
-      mbar_init(&full[s], (WF ? kConvWarps : 1) + (MODE == 1 ? 32 * kGatherWarps : 1));
+      mbar_init(&full[s], (WF ? kConvGroupWarps : 1) + (MODE == 1 ? 32 * kGatherWarps : 1));
       mbar_init(&empty[s], 1);
     }
     for (int r = 0; r < p.NR; ++r) {
       mbar_init(&rfull[r], 1);
-      mbar_init(&rempty[r], kConvWarps);
+      mbar_init(&rempty[r], kConvGroupWarps);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -758,30 +760,37 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
     }
   } else if (WF && conv_index(warp) >= 0) {
     // --------------------------------------------------- NVFP4 converters
-    // 256 threads: GEMM1 (256 weight rows per stage) one row each; GEMM2
-    // (128 rows) half a row each.
-    const int ct = conv_index(warp) * 32 + lane;
-    int s = 0, ph = 0, r = 0, rph = 0;
+    // Two groups of four warps take alternate K chunks, so that one group's
+    // hand-off of a stage to the MMA (proxy fence, arrivals, the next
+    // waits) overlaps the other group's conversion.  NS and NR are even, so
+    // every stage and raw stage is always used by the same group, and a
+    // group never waits on a barrier phase the other group has yet to
+    // release.  Thread rr of a group converts row rr of each 128-row tile:
+    // GEMM1's gate and up rows rr, GEMM2's row rr.
+    const int ci = conv_index(warp);
+    const int group = ci / kConvGroupWarps;
+    const int rr = (ci % kConvGroupWarps) * 32 + lane;
+    int s = 0, ph = 0, r = 0, rph = 0, n = 0;
     bool ok = true;
-    const int rr = (MODE == 1) ? ct : (ct & (kTileM - 1));
-    const int c_begin = (MODE == 1) ? 0 : (ct >> 7) * 4;
-    const int c_end = (MODE == 1) ? 8 : c_begin + 4;
     for (int u = blockIdx.x, ui = 0; u < total && ok; u += gridDim.x, ++ui) {
       const Unit t = my_unit<MODE == 2>(p, utab, ui, u, nb);
       if (t.skip) continue;
-      for (int kc = kc_lo(p, t), ke = kc_hi(p, t); kc < ke; ++kc) {
-        ok = mbar_wait(&rfull[r], rph, p.status) && mbar_wait(&empty[s], ph ^ 1, p.status);
-        if (!ok) break;
-        const uint8_t* Q = raw + r * raw_stage;
-        const uint32_t* SC = reinterpret_cast<const uint32_t*>(Q + rq_bytes);
-        uint8_t* A = stages + s * stage_bytes;
-        convert_row(Q + rr * 32, SC[rr], A + (rr / kTileM) * kTileM * 128, rr & (kTileM - 1),
-                    c_begin, c_end);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&rempty[r]);
-          mbar_arrive(&full[s]);
+      for (int kc = kc_lo(p, t), ke = kc_hi(p, t); kc < ke; ++kc, ++n) {
+        if ((n & 1) == group) {
+          ok = mbar_wait(&rfull[r], rph, p.status) && mbar_wait(&empty[s], ph ^ 1, p.status);
+          if (!ok) break;
+          const uint8_t* Q = raw + r * raw_stage;
+          const uint32_t* SC = reinterpret_cast<const uint32_t*>(Q + rq_bytes);
+          uint8_t* A = stages + s * stage_bytes;
+#pragma unroll
+          for (int a = 0; a < kA; ++a)
+            convert_row(Q + (a * kTileM + rr) * 32, SC[a * kTileM + rr], A + a * kTileM * 128, rr, 0, 8);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&rempty[r]);
+            mbar_arrive(&full[s]);
+          }
         }
         if (++r == p.NR) { r = 0; rph ^= 1; }
         if (++s == p.NS) { s = 0; ph ^= 1; }
@@ -864,12 +873,12 @@ __global__ void __maxnreg__(64)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.NS; ++s) {
-      mbar_init(&full[s], (WF ? kConvWarps : 1) + (MODE == 1 ? 32 * kGatherWarps : 1));
+      mbar_init(&full[s], (WF ? kTmConvGroupWarps : 1) + (MODE == 1 ? 32 * kGatherWarps : 1));
       mbar_init(&empty[s], 1);
     }
     for (int r = 0; r < p.NR; ++r) {
       mbar_init(&rfull[r], 1);
-      mbar_init(&rempty[r], kConvWarps);
+      mbar_init(&rempty[r], kTmConvGroupWarps);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -1353,8 +1362,10 @@ int smem_plan(int MODE, int wf, int BN, int* NS, int* NR, size_t* bytes) {
   const int stage = kA * kTileM * 128 + BN * 128;
   const int raw_stage = ((kA * kTileM * 36) + 1023) / 1024 * 1024;
   const int budget = 200 * 1024 - kMaxUnitsPerCta * (int)sizeof(UnitRec);
-  const int nr = wf ? (MODE == 1 ? 5 : 8) : 0;
-  const int ns = std::min(8, (budget - nr * raw_stage) / stage);
+  // NVFP4: even ring sizes, one stage in two for each converter group
+  const int nr = wf ? (MODE == 1 ? 4 : 8) : 0;
+  int ns = std::min(8, (budget - nr * raw_stage) / stage);
+  if (wf) ns &= ~1;
   if (ns < 2) return OES_ERR_UNSUPPORTED;
   *NS = ns;
   *NR = wf ? nr : 1;
