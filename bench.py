@@ -38,7 +38,14 @@ import sys
 import tempfile
 import time
 
-import numpy as np
+# The CPU oracle (cpu_baseline and --impl reference) does its matrix products
+# in numpy's BLAS and everything else in single-threaded Python.  The BLAS
+# thread pool is sized here, before numpy loads it, to the cores this process
+# may run on, and the baselines report that number.
+CPU_THREADS = len(os.sched_getaffinity(0))
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(CPU_THREADS))
+
+import numpy as np  # noqa: E402
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -167,7 +174,8 @@ def sample_text(cfg, cs, n_tok):
            if cs.T < cfg.T else f"the whole {cfg.T}-token chunk")
     return (f"oracle slot path over {pre} (routing, distinct experts, LRU queries, align; "
             f"the workload's experts, pool and weights) with the expert MLP and combine for "
-            f"{n_tok} of those tokens")
+            f"{n_tok} of those tokens; its matrix products on numpy's BLAS with {blas_threads()} "
+            f"threads, the rest single-threaded Python")
 
 
 def lazy_source(cfg, needed):
@@ -209,7 +217,7 @@ def reference_arm(args, cfg):
              for i in range(args.steps)]
     s = float(np.sum(times))
     value = n_tok * args.steps / s
-    cores = len(os.sched_getaffinity(0))
+    cores = blas_threads()
     sample = sample_text(cfg, cs, n_tok) + " (a fixed token sample, the same every step)"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -650,6 +658,15 @@ def gpu_arm(args, cfg):
         dist.destroy_process_group()
 
 
+def blas_threads() -> int:
+    """Threads of numpy's BLAS pool (the oracle's matrix products; its other
+    steps run on one): OPENBLAS_NUM_THREADS as set before numpy loaded."""
+    try:
+        return max(1, int(os.environ.get("OPENBLAS_NUM_THREADS", CPU_THREADS)))
+    except ValueError:
+        return CPU_THREADS
+
+
 def cpu_baseline(cfg, b):
     """The oracle on the host cores over bounded samples (about 10 s)."""
     srcs = [x.numpy() for x in b.src_bufs]
@@ -662,7 +679,7 @@ def cpu_baseline(cfg, b):
         tokens += n_tok
         i += 1
     return {"kind": "oracle", "value": tokens / total, "unit": "tokens/s",
-            "cores": len(os.sched_getaffinity(0)),
+            "cores": blas_threads(),
             "sample": f"{i} samples, {total:.1f} s: " + sample_text(cfg, cs, n_tok)}
 
 
