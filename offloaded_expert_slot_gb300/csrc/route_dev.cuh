@@ -180,15 +180,14 @@ __device__ __forceinline__ void load_logits(const uint16_t* p, float* o) {
 // V l + 32 V q + i (q < Q, i < V).  Let tau be the k-th largest of the 32
 // lane maxima (a bitonic sort of them): at least k logits are >= tau (those
 // maxima), so every logit of the top k is >= tau, and for random rows only a
-// few more are.  The
-// candidates (logit >= tau) go to `cand` (this warp's own 33 entries: 32
-// candidates, then the count) at positions from a shared counter, in any
-// order; each ranks itself against the others by (key, lower id) and rank r
-// goes to lane r.  A row whose tau is -inf (fewer than k lanes with a number
-// above -inf: NaN and missing experts rank lowest) or that has more than 32
-// candidates (many equal logits) is ranked in rounds over the same keys.
-// Both give the same ids and, through topk_write, the same weights bit for
-// bit.
+// few more are.  The candidates (logit >= tau) go to `cand` (this warp's own
+// 33 entries: 32 candidates, then the count) at positions from a shared
+// counter, in any order; each ranks itself against the others by (key, lower
+// id) and rank r goes to lane r.  A row whose tau is -inf (fewer than k lanes
+// with a number above -inf: NaN and missing experts rank lowest) or that has
+// more than 32 candidates (many equal logits) is ranked in rounds over the
+// same keys.  Both give the same ids and, through topk_write, the same
+// weights bit for bit.
 template <int V, int Q, typename LT>
 __device__ __forceinline__ void topk_row_filtered(const LT* __restrict__ row, int E, int k, int lane,
                                                   int32_t* __restrict__ ids_t, float* __restrict__ w_t,
