@@ -28,6 +28,8 @@ def test_reference_arm_prints_one_contract_line():
     assert d["warmup"] >= 3 and d["steps"] == 1 and d["n_gpus"] == 1
     assert d["config"]["workload"] == "c1_tiny" and d["data"] == "synthetic"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    # cores is numpy's BLAS pool, which bench.py sizes before numpy loads
+    assert "numpy's BLAS with %d threads" % d["cpu_baseline"]["cores"] in d["cpu_baseline"]["sample"]
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
@@ -49,3 +51,18 @@ def test_reference_arm_prints_one_contract_line():
 ], ids=["decode_width", "tiny", "long_prefill", "one_token"])
 def test_gpu_launch_count_follows_the_slot_path(cfg, want):
     assert bench.gpu_launches(cfg) == want
+
+
+def test_blas_pool_is_sized_before_numpy_loads():
+    """A caller's OPENBLAS_NUM_THREADS stands; otherwise bench.py sets it to
+    the cores the process may run on, and the baselines report that."""
+    code = ("import os, bench; print(os.environ['OPENBLAS_NUM_THREADS'], bench.blas_threads(), "
+            "len(os.sched_getaffinity(0)))")
+    env = {k: v for k, v in os.environ.items() if k != "OPENBLAS_NUM_THREADS"}
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT,
+                         env=env, timeout=300, check=True).stdout.split()
+    assert out[0] == out[1] == out[2]
+    env["OPENBLAS_NUM_THREADS"] = "3"
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT,
+                         env=env, timeout=300, check=True).stdout.split()
+    assert out[0] == out[1] == "3"
