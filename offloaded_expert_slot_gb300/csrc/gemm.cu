@@ -342,7 +342,7 @@ __device__ __forceinline__ uint16_t quant_lane_act(float v, float a) {
 // product e2m1 * e4m3 has at most 6 significant bits and lies in
 // [2^-10, 2688], so it is exact in f16.
 __device__ __forceinline__ void convert_row(const uint8_t* q, uint32_t scales, uint8_t* tile,
-                                            int row, int c_begin, int c_end) {
+                                            int row) {
   const uint4 q0 = *reinterpret_cast<const uint4*>(q);
   const uint4 q1 = *reinterpret_cast<const uint4*>(q + 16);
   const uint32_t s01 = cvt_e4m3x2_f16x2(scales & 0xFFFFu);
@@ -354,7 +354,6 @@ __device__ __forceinline__ void convert_row(const uint8_t* q, uint32_t scales, u
   const int sw = row & 7;
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
-    if (c < c_begin || c >= c_end) continue;
     const uint32_t wd = words[c];
     const uint32_t s = sc[c >> 1];
     uint32_t f[4];
@@ -784,7 +783,7 @@ __global__ void __launch_bounds__(gemm_threads(WF), 1)
           uint8_t* A = stages + s * stage_bytes;
 #pragma unroll
           for (int a = 0; a < kA; ++a)
-            convert_row(Q + (a * kTileM + rr) * 32, SC[a * kTileM + rr], A + a * kTileM * 128, rr, 0, 8);
+            convert_row(Q + (a * kTileM + rr) * 32, SC[a * kTileM + rr], A + a * kTileM * 128, rr);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -1144,7 +1143,7 @@ __global__ void __maxnreg__(64)
           const uint8_t* Q = raw + r * raw_stage;
           const uint32_t* SC = reinterpret_cast<const uint32_t*>(Q + rq_bytes);
           uint8_t* W = stages + s * stage_bytes;
-          convert_row(Q + rr * 32, SC[rr], W + (rr / kTileM) * kTileM * 128, rr & (kTileM - 1), 0, 8);
+          convert_row(Q + rr * 32, SC[rr], W + (rr / kTileM) * kTileM * 128, rr & (kTileM - 1));
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
